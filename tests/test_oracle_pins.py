@@ -1,0 +1,323 @@
+"""Pins of the fp64 oracle to facts fixed outside the oracle itself.
+
+Each test checks the oracle against a library routine, a closed form, an
+invariant the method guarantees, or an independent brute-force restatement on
+tiny inputs, chosen so that a plausible slip (a dropped self term, a wrong
+softmax axis, an off-by-one recent window, argmax for argmin, a wrong tie
+rule) fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import h2o_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rand_seq(rng, L, D, key_mean=None):
+    q = rng.standard_normal((L, D))
+    k = rng.standard_normal((L, D)) * 1.3
+    v = rng.standard_normal((L, D))
+    if key_mean is not None:
+        k += key_mean
+    return q, k, v
+
+
+def run_pair(q_all, k_all, v_all, L, heavy, recent, scale):
+    """Prefill positions < L, then decode the rest; returns per-step results."""
+    st, colsum, out_prefill = O.prefill_pair(q_all[:L], k_all[:L], v_all[:L], heavy, recent, scale)
+    steps = []
+    for p in range(L, q_all.shape[0]):
+        before = st.copy()
+        r = O.decode_step_pair(st, q_all[p], k_all[p], v_all[p], scale, heavy, recent)
+        steps.append((before, r, st.copy()))
+    return st, colsum, out_prefill, steps
+
+
+def sdpa_causal(q, k, v, scale):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))[None, None]
+    o = torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v), is_causal=True, scale=scale)
+    return o[0, 0].numpy()
+
+
+# ------------------------------------------------------------------ library routine
+@pytest.mark.parametrize("L,T,heavy,recent", [(12, 6, 10, 8), (5, 9, 7, 7), (0, 10, 4, 6), (16, 1, 9, 8)])
+def test_full_budget_equals_causal_attention(L, T, heavy, recent):
+    """Budget >= L+T: nothing is ever evicted, so every output is plain causal
+    attention (the report's "local H2O ~ Full" at full budget), checked against
+    torch's fp64 scaled_dot_product_attention."""
+    rng = np.random.default_rng(1)
+    D = 8
+    scale = 1 / math.sqrt(D)
+    q, k, v = rand_seq(rng, L + T, D)
+    st, colsum, out_prefill, steps = run_pair(q, k, v, L, heavy, recent, scale)
+    ref = sdpa_causal(q, k, v, scale)
+    if L:
+        np.testing.assert_allclose(out_prefill, ref[:L], rtol=0, atol=1e-12)
+    for t, (_, r, _) in enumerate(steps):
+        assert r.evicted == -1
+        np.testing.assert_allclose(r.out, ref[L + t], rtol=0, atol=1e-12)
+    assert st.count == L + T
+
+
+@pytest.mark.parametrize("L,recent", [(20, 5), (3, 4), (0, 1), (9, 1)])
+def test_no_heavy_budget_is_sliding_window(L, recent):
+    """heavy = 0 reduces H2O to the Local baseline: the token at p attends to
+    positions p-recent..p exactly (closed form), here via torch SDPA on the
+    sliced window."""
+    rng = np.random.default_rng(2)
+    D, T = 4, 15
+    scale = 0.7
+    q, k, v = rand_seq(rng, L + T, D)
+    _, _, _, steps = run_pair(q, k, v, L, 0, recent, scale)
+    for t, (_, r, after) in enumerate(steps):
+        p = L + t
+        lo = max(0, p - recent)
+        qt = torch.from_numpy(q[p:p + 1])[None, None]
+        kt = torch.from_numpy(k[lo:p + 1])[None, None]
+        vt = torch.from_numpy(v[lo:p + 1])[None, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale)[0, 0, 0].numpy()
+        np.testing.assert_allclose(r.out, ref, rtol=0, atol=1e-12)
+        assert sorted(after.pos[after.pos >= 0].tolist()) == list(range(max(0, p + 1 - recent), p + 1))
+
+
+# ------------------------------------------------------------------ closed forms
+def test_colsum_mass_is_prompt_length():
+    """Every causal softmax row sums to one, so the column sums add up to L."""
+    rng = np.random.default_rng(3)
+    for L in (1, 2, 7, 64):
+        q, k, v = rand_seq(rng, L, 16)
+        _, colsum, _ = O.causal_attention_stats(q, k, v, 0.25)
+        assert abs(colsum.sum() - L) < 1e-10 * L
+        assert np.all(colsum > 0)
+
+
+def test_colsum_constant_keys_harmonic():
+    """Equal keys give uniform rows p_ij = 1/(i+1), so
+    colsum_j = sum_{i=j}^{L-1} 1/(i+1) = H_L - H_j (harmonic numbers)."""
+    rng = np.random.default_rng(4)
+    L, D = 50, 6
+    q = rng.standard_normal((L, D))
+    k = np.tile(rng.standard_normal(D), (L, 1))
+    v = rng.standard_normal((L, D))
+    _, colsum, out = O.causal_attention_stats(q, k, v, 0.9)
+    Hn = np.concatenate([[0.0], np.cumsum(1.0 / np.arange(1, L + 1))])
+    np.testing.assert_allclose(colsum, Hn[L] - Hn[:L], rtol=1e-13, atol=0)
+    # and the output is the running mean of v
+    np.testing.assert_allclose(out, np.cumsum(v, axis=0) / np.arange(1, L + 1)[:, None], atol=1e-12)
+
+
+def test_golden_uniform_three_tokens():
+    """Hand-worked example stored as a fixture (uniform attention, L = 3)."""
+    vals = {}
+    with open(os.path.join(GOLDEN, "uniform_colsum_L3.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                key, val = line.split("=")
+                vals[key.strip()] = [float(eval(x, {})) for x in val.split(",")]
+    q = np.zeros((3, 2))
+    k = np.ones((3, 2))
+    v = np.array([[1.0, 0.0], [0.0, 1.0], [1.0, 1.0]])
+    _, colsum, out = O.causal_attention_stats(q, k, v, 1.0)
+    np.testing.assert_allclose(colsum, vals["colsum"], rtol=1e-15)
+    np.testing.assert_allclose(out[:, 0], vals["out0"], rtol=1e-15)
+    np.testing.assert_allclose(out[:, 1], vals["out1"], rtol=1e-15)
+
+
+def test_constant_values_give_that_value():
+    """Probabilities sum to one, so with every V row equal to c, out = c."""
+    rng = np.random.default_rng(5)
+    L, T, D = 30, 40, 8
+    q, k, _ = rand_seq(rng, L + T, D)
+    c = rng.standard_normal(D)
+    v = np.tile(c, (L + T, 1))
+    _, _, out_prefill, steps = run_pair(q, k, v, L, 6, 5, 0.5)
+    np.testing.assert_allclose(out_prefill, np.tile(c, (L, 1)), atol=1e-13)
+    for _, r, _ in steps:
+        np.testing.assert_allclose(r.out, c, atol=1e-13)
+
+
+# ------------------------------------------------------------------ invariants
+@pytest.mark.parametrize("L,heavy,recent", [(40, 6, 5), (8, 6, 5), (0, 3, 2), (11, 0, 3), (25, 4, 1)])
+def test_budget_window_and_single_eviction(L, heavy, recent):
+    """Section 3.1/3.4 invariants after every step: |S| <= heavy+recent, the last
+    `recent` positions are always kept, at most one entry leaves per step, the
+    ring lists the recent window oldest-first, and probabilities sum to one."""
+    rng = np.random.default_rng(6)
+    T, D = 60, 4
+    q, k, v = rand_seq(rng, L + T, D, key_mean=rng.standard_normal(D))
+    C = heavy + recent
+    _, _, _, steps = run_pair(q, k, v, L, heavy, recent, 0.8)
+    for t, (before, r, after) in enumerate(steps):
+        p = L + t
+        kept_before = set(before.pos[before.pos >= 0].tolist())
+        kept_after = set(after.pos[after.pos >= 0].tolist())
+        assert len(kept_after) == after.count <= C
+        assert set(range(max(0, p + 1 - recent), p + 1)) <= kept_after
+        assert len(kept_before - kept_after) <= 1
+        assert kept_after - kept_before == {p}
+        assert abs(r.prob.sum() - 1) < 1e-12
+        ring_pos = [after.pos[s] for s in np.roll(after.ring, -after.head) if s >= 0]
+        assert ring_pos == list(range(max(0, p + 1 - recent), p + 1))
+        if r.evicted >= 0:
+            assert before.pos[r.evicted] <= p - recent
+            assert before.count == C
+
+
+def test_score_mass_conservation():
+    """Each query row hands out probability mass exactly 1, so after t decode
+    steps: sum of kept scores + scores of evicted tokens at eviction time
+    + prompt mass of tokens dropped at prefill = L + t (up to the float32
+    rounding of the score buffer)."""
+    rng = np.random.default_rng(7)
+    L, T, D, heavy, recent = 48, 80, 8, 7, 6
+    q, k, v = rand_seq(rng, L + T, D, key_mean=rng.standard_normal(D))
+    st, colsum, _, steps = run_pair(q, k, v, L, heavy, recent, 0.6)
+    kept0 = steps[0][0]
+    dropped_prefill = colsum.sum() - colsum[kept0.pos[kept0.pos >= 0]].sum()
+    evicted_mass = 0.0
+    for before, r, _ in steps:
+        if r.evicted >= 0:
+            n = before.count
+            evicted_mass += before.score[r.evicted] + r.prob[r.evicted]
+    total = st.score[st.pos >= 0].sum() + evicted_mass + dropped_prefill
+    assert abs(total - (L + T)) < 1e-5
+
+
+# ------------------------------------------------------------------ brute force
+def brute_force_run(q, k, v, L, heavy, recent, scale):
+    """Independent restatement on position sets with pure-Python arithmetic.
+
+    Prefill: colsum by explicit double sums; the heavy set is found by evicting
+    the lowest (score, position) candidate one at a time.  Decode: Algorithm 1
+    taken literally, u = argmax_v F(S + {p} - {v}) with F the sum of scores,
+    enumerated over every candidate v outside the recent window (ties: lowest
+    position evicted).
+    """
+    C = heavy + recent
+    D = len(q[0])
+    f32 = lambda x: float(np.float32(x))
+    dot = lambda a, b: sum(a[d] * b[d] for d in range(D))
+    score = {}
+    if L:
+        colsum = [0.0] * L
+        for i in range(L):
+            s = [scale * dot(q[i], k[j]) for j in range(i + 1)]
+            mx = max(s)
+            z = sum(math.exp(x - mx) for x in s)
+            for j in range(i + 1):
+                colsum[j] += math.exp(s[j] - mx) / z
+        if L <= C:
+            kept = set(range(L))
+        else:
+            cand = set(range(L - recent))
+            while len(cand) > heavy:
+                cand.remove(min(cand, key=lambda j: (f32(colsum[j]), j)))
+            kept = cand | set(range(L - recent, L))
+        score = {j: f32(colsum[j]) for j in kept}
+    outs, kept_sets, evictions = [], [], []
+    for p in range(L, len(q)):
+        S = sorted(score) + [p]
+        s = [scale * dot(q[p], k[j]) for j in S]
+        mx = max(s)
+        z = sum(math.exp(x - mx) for x in s)
+        pr = [math.exp(x - mx) / z for x in s]
+        outs.append([sum(pr[a] * v[j][d] for a, j in enumerate(S)) for d in range(D)])
+        for a, j in enumerate(S[:-1]):
+            score[j] = f32(score[j] + pr[a])
+        ev = None
+        if len(S) - 1 == C:
+            cand = [j for j in S[:-1] if j <= p - recent]
+            total = sum(score.values())
+            best = max(total - score[j] for j in cand)
+            ev = min(j for j in cand if total - score[j] == best)
+            del score[ev]
+        score[p] = f32(pr[-1])
+        evictions.append(ev)
+        kept_sets.append(set(score))
+    return outs, kept_sets, evictions
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("L,heavy,recent", [(12, 3, 2), (5, 2, 3), (0, 2, 2), (9, 0, 2), (7, 4, 1)])
+def test_against_position_set_brute_force(seed, L, heavy, recent):
+    rng = np.random.default_rng(100 + seed)
+    T, D = 40, 3
+    mean = rng.standard_normal(D)
+    q, k, v = rand_seq(rng, L + T, D, key_mean=mean)
+    # a few repeated keys make heavy hitters and near ties likely
+    k[rng.integers(0, L + T, 6)] = k[0]
+    _, _, _, steps = run_pair(q, k, v, L, heavy, recent, 0.9)
+    outs, kept_sets, evictions = brute_force_run(q.tolist(), k.tolist(), v.tolist(), L, heavy, recent, 0.9)
+    for t, (before, r, after) in enumerate(steps):
+        assert set(after.pos[after.pos >= 0].tolist()) == kept_sets[t]
+        ev_pos = None if r.evicted < 0 else int(before.pos[r.evicted])
+        assert ev_pos == evictions[t]
+        np.testing.assert_allclose(r.out, outs[t], atol=1e-12)
+
+
+def test_prefill_selection_brute_force():
+    """Heavy set = top-Hh of the key (score, position) by a full lexicographic
+    sort, which also equals Hh iterated lowest-key evictions."""
+    rng = np.random.default_rng(8)
+    for trial in range(20):
+        L = int(rng.integers(10, 200))
+        heavy = int(rng.integers(0, 12))
+        recent = int(rng.integers(1, 12))
+        colsum = rng.integers(0, 5, size=L).astype(np.float64) / 4  # many exact ties
+        keep = O.select_prefill(colsum, L, heavy, recent)
+        if L <= heavy + recent:
+            assert keep == list(range(L))
+            continue
+        n = L - recent
+        order = np.lexsort((np.arange(n), colsum[:n]))  # ascending (score, pos)
+        top = sorted(order[n - heavy:].tolist()) if heavy else []
+        assert keep == top + list(range(n, L))
+        cand = list(range(n))
+        while len(cand) > heavy:
+            cand.remove(min(cand, key=lambda j: (colsum[j], j)))
+        assert keep[:heavy] == cand
+
+
+def test_tie_evicts_lowest_position():
+    """Equal scores: the candidate with the lowest position is evicted."""
+    D = 2
+    C_heavy, recent = 3, 1
+    st = O.empty_pair(C_heavy + recent, recent, D)
+    st.count = 4
+    st.p = 10
+    st.pos[:] = [7, 2, 5, 9]
+    st.score[:] = [0.5, 0.5, 0.5, 0.1]
+    st.ring[:] = [3]
+    st.head = 0
+    q = np.zeros(D)  # uniform attention: every kept score rises by the same amount
+    r = O.decode_step_pair(st, q, np.zeros(D), np.zeros(D), 1.0, C_heavy, recent)
+    # candidates: pos <= 9 -> all four; slot 3 (pos 9, score 0.1 + 0.2) is lowest
+    assert r.evicted == 3
+    st2 = O.empty_pair(4, 1, D)
+    st2.count, st2.p, st2.head = 4, 10, 0
+    st2.pos[:] = [7, 2, 5, 9]
+    st2.score[:] = [0.5, 0.5, 0.5, 0.9]
+    st2.ring[:] = [3]
+    r2 = O.decode_step_pair(st2, q, np.zeros(D), np.zeros(D), 1.0, C_heavy, recent)
+    assert r2.evicted == 1  # equal lowest scores at pos 7, 2, 5 -> pos 2
+    assert st2.pos[1] == 10 and st2.ring[0] == 1
+
+
+def test_kv_cache_size_worked_example():
+    """The report's sizing example (section 1.1): a 30B model (OPT-30B: 48
+    layers, hidden 7168) at batch 128 and sequence 1024 holds ~180 GB of fp16
+    K and V.  Pins the byte accounting used by the benchmark."""
+    from kv_cache_eviction_03_gb300.accounting import kv_cache_bytes
+
+    with open(os.path.join(GOLDEN, "kv_size_opt30b.txt")) as f:
+        fields = {a.strip(): b.strip() for a, b in
+                  (l.split("=") for l in (x.split("#")[0].strip() for x in f) if l)}
+    b = kv_cache_bytes(int(fields["layers"]), int(fields["hidden"]), int(fields["batch"]),
+                       int(fields["seq"]), int(fields["bytes_per_elem"]))
+    assert round(b / 1e9) == int(fields["approx_gb"])
