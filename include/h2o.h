@@ -1,0 +1,147 @@
+/*
+ * h2o.h - C ABI of the GB300 (sm_103a) H2O heavy-hitter KV-cache library.
+ *
+ * H2O keeps, per (batch, head) pair, a fixed budget of C = heavy + recent
+ * cached tokens: the `recent` most recent ones plus the `heavy` tokens with the
+ * largest accumulated attention score ("H2O: Heavy-Hitter Oracle ... 深度解读报告",
+ * sections 3.1, 3.3 and 3.4; "H2O" inference-research notes, summary).
+ *
+ * Conventions shared by every call
+ *  - All tensor arguments are DEVICE pointers owned by the caller, borrowed
+ *    for the stream-ordered duration of the call, densely packed, row-major.
+ *    B = batch, H = heads, D = head_dim, L = prompt length, P = B*H pairs.
+ *  - q / k / v arguments have the cache's K/V dtype (h2o_dtype); outputs are
+ *    float32.  Device pointers must be 16-byte aligned.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and never synchronise the host, except the calls marked
+ *    "synchronous".  One cache must not be used from two streams at once.
+ *  - Return values are h2o_status codes; no exception crosses the ABI.
+ *    Argument errors are detected on the host before any launch.  Device-side
+ *    checks latch a flag that h2o_cache_check() reports as H2O_EDEVICE.
+ *  - h2o_last_error() returns a thread-local message for the last failure.
+ *  - The library owns the slot store (K, V), the float32 score buffer, the
+ *    int32 position tags, the recent ring and the per-pair counters; they are
+ *    allocated in h2o_cache_create and freed in h2o_cache_destroy.
+ */
+#ifndef H2O_GB300_H
+#define H2O_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define H2O_API __attribute__((visibility("default")))
+#else
+#define H2O_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { H2O_F16 = 0, H2O_F32 = 1 } h2o_dtype;
+
+typedef enum {
+  H2O_OK = 0,
+  H2O_EINVAL = -1,  /* bad argument (NULL pointer, size out of range, ...) */
+  H2O_ENOMEM = -2,  /* device allocation failed */
+  H2O_ECUDA = -3,   /* a CUDA runtime call failed (message has the CUDA error) */
+  H2O_ESTATE = -4,  /* call not valid in the cache's state (e.g. positions exhausted) */
+  H2O_EDEVICE = -5  /* a device-side check fired (see h2o_cache_check) */
+} h2o_status;
+
+typedef struct h2o_cache h2o_cache; /* opaque */
+
+/* Preallocate a cache for B x H pairs of `heavy_budget + recent_budget` slots
+ * ("... 深度解读报告", section 3.4: preallocated memory, overwrite in place,
+ * heavy-hitter region + recent region).  head_dim in {64, 128};
+ * heavy_budget >= 0; recent_budget >= 1 (the newest token is always recent);
+ * slots <= 65536.  kv_dtype is an h2o_dtype.  The cache starts empty (as after
+ * h2o_cache_reset).  Uses the current CUDA device.  *out = NULL on failure. */
+H2O_API int h2o_cache_create(int batch, int heads, int head_dim, int heavy_budget, int recent_budget,
+                     int kv_dtype, h2o_cache** out);
+
+/* Free every allocation of the cache.  NULL-safe.  The caller must ensure no
+ * call on the cache is still running on a stream. */
+H2O_API void h2o_cache_destroy(h2o_cache* cache);
+
+/* Prefill ("... 深度解读报告", section 3.4, prefill rule; section 3.3 for the
+ * score): for each pair, full causal attention over the prompt,
+ * column sums colsum_j = sum_{i>=j} softmax_i(scale * q_i . k_j), then
+ *   L <= C : keep every position (slot j = position j);
+ *   L >  C : keep positions L-R..L-1 (recent) and the `heavy` positions below
+ *            L-R with the largest (colsum, position) keys.
+ * Heavy hitters go to slots 0..heavy-1 in ascending position, the recent window
+ * to slots heavy..C-1; each kept slot's score = its colsum.  Replaces whatever
+ * the cache held.  q, k, v: [B, H, L, D] kv_dtype.  out_or_null: [B, H, L, D]
+ * float32 causal attention output, or NULL to skip it.  prompt_len = 0 empties
+ * the cache.  The first prefill at a new maximum prompt length allocates its
+ * column-sum workspace (cudaMalloc); later ones allocate nothing. */
+H2O_API int h2o_prefill(h2o_cache* cache, const void* q, const void* k, const void* v, int prompt_len,
+                float scale, float* out_or_null, void* stream);
+
+/* h2o_prefill plus optional float32 views of its intermediate results:
+ * colsum_or_null [B, H, L] (every position's column sum) and
+ * lse_or_null [B, H, L] (log-sum-exp of each causal row, natural log, of the
+ * scaled logits). */
+H2O_API int h2o_prefill_ex(h2o_cache* cache, const void* q, const void* k, const void* v, int prompt_len,
+                   float scale, float* out_or_null, float* colsum_or_null, float* lse_or_null,
+                   void* stream);
+
+/* One decode step for every pair ("... 深度解读报告", sections 3.1, 3.3, 3.4):
+ *   1. attend over the kept slots and the new token: softmax of
+ *      scale * q . k over kept + self only; out = sum_j p_j v_j;
+ *   2. score[j] += p_j for every kept slot;
+ *   3. if the cache is full, evict the kept slot with the lowest
+ *      (score, position) among positions <= p - recent; otherwise use the next
+ *      free slot;
+ *   4. overwrite that slot with k_new / v_new, score = p_self, position = p,
+ *      and append it to the recent ring.
+ * q, k_new, v_new: [B, H, D] kv_dtype.  out: [B, H, D] float32 (required).
+ * evicted_or_null: [B, H] int32, the slot freed this step or -1 while filling.
+ * Counters live on the device, so steps can be captured in a CUDA graph and
+ * replayed.  Returns H2O_ESTATE when the int32 position would overflow. */
+H2O_API int h2o_decode_step(h2o_cache* cache, const void* q, const void* k_new, const void* v_new,
+                    float scale, float* out, int32_t* evicted_or_null, void* stream);
+
+/* Empty the cache (count 0, position 0): a stream that starts without a
+ * prompt.  Asynchronous on `stream`. */
+H2O_API int h2o_cache_reset(h2o_cache* cache, void* stream);
+
+/* Size in bytes of the host image used by export/import. */
+H2O_API size_t h2o_cache_state_bytes(const h2o_cache* cache);
+
+/* Synchronous.  Copy the whole cache state into host memory `host_buf` of
+ * `bytes` >= h2o_cache_state_bytes().  Layout (little-endian, packed):
+ *   int32 header[16] = {magic 0x48324F31, version 1, B, H, D, heavy, recent,
+ *                       kv_dtype, 0...}
+ *   K      [P, C, D] kv_dtype     V [P, C, D] kv_dtype
+ *   score  [P, C]   float32       pos [P, C] int32 (-1 = empty slot)
+ *   ring   [P, R]   int32 (-1 = empty)
+ *   ctr    [P, 4]   int32 {next position p, count, ring head, 0} */
+H2O_API int h2o_cache_export_state(const h2o_cache* cache, void* host_buf, size_t bytes, void* stream);
+
+/* Synchronous.  Load a host image written by export (or built by a caller in
+ * the same layout).  The header must match the cache's shape and dtype. */
+H2O_API int h2o_cache_import_state(h2o_cache* cache, const void* host_buf, size_t bytes, void* stream);
+
+/* Synchronous.  Wait for the stream, then report H2O_EDEVICE if a device-side
+ * check has fired since the last h2o_cache_check (and clear it), or the
+ * pending CUDA error as H2O_ECUDA. */
+H2O_API int h2o_cache_check(h2o_cache* cache, void* stream);
+
+/* Tuning: number of CTAs (a thread-block cluster) that share one pair in the
+ * decode kernel, 0 = automatic.  Must be 1, 2, 4, 8 or 16. */
+H2O_API int h2o_cache_set_decode_splits(h2o_cache* cache, int splits);
+
+/* info[0..7] = {batch, heads, head_dim, heavy, recent, kv_dtype,
+ *               decode splits in use, decode threads per CTA}. */
+H2O_API int h2o_cache_info(const h2o_cache* cache, int32_t* info);
+
+/* Thread-local message describing the last error returned on this thread. */
+H2O_API const char* h2o_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* H2O_GB300_H */

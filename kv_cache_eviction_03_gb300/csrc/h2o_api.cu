@@ -1,0 +1,396 @@
+// C ABI of the H2O library: cache object, argument checks, error reporting and
+// stream-ordered launches of the decode / prefill kernels.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <map>
+#include <mutex>
+#include <utility>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "h2o.h"
+#include "h2o_internal.cuh"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(e == cudaErrorMemoryAllocation ? H2O_ENOMEM : H2O_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e),
+              cudaGetErrorString(e));
+}
+
+constexpr int kHeaderInts = 16;
+constexpr int kMagic = 0x48324F31;
+constexpr int kMaxSlots = 65536;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t kv_bytes(const h2o_cache* c) { return static_cast<size_t>(c->P) * c->C * c->D * c->elem; }
+
+int chunk_for(int C, int splits) {
+  const int ch = (C + splits - 1) / splits;
+  return (ch + 3) / 4 * 4;
+}
+
+// CTAs per pair: enough CTAs to give every SM about four, while each CTA keeps
+// at least 32 slots; more when one CTA's slot range would not fit on chip.
+int auto_splits(int pairs, int C, int sms) {
+  const long long target = 4LL * sms;
+  int s = 1;
+  while (s < 16 && static_cast<long long>(pairs) * s < target && chunk_for(C, 2 * s) >= 32) s *= 2;
+  while (s < 16 && chunk_for(C, s) > h2o::decode_max_chunk()) s *= 2;
+  return s;
+}
+
+int splits_in_use(const h2o_cache* c) { return c->splits_override > 0 ? c->splits_override : c->splits_auto; }
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+namespace h2o {
+cudaError_t kernel_attrs(const void* kern, size_t smem_bytes, bool nonportable_cluster) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, size_t> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  auto key = std::make_pair(kern, dev);
+  auto it = done.find(key);
+  if (it != done.end() && it->second >= smem_bytes) return cudaSuccess;
+  if (smem_bytes > 48 * 1024 &&
+      (e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes))) !=
+          cudaSuccess)
+    return e;
+  if (nonportable_cluster &&
+      (e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
+    return e;
+  done[key] = smem_bytes;
+  return cudaSuccess;
+}
+}  // namespace h2o
+
+extern "C" {
+
+const char* h2o_last_error(void) { return g_msg; }
+
+int h2o_cache_create(int batch, int heads, int head_dim, int heavy_budget, int recent_budget, int kv_dtype,
+                     h2o_cache** out) {
+  if (!out) return fail(H2O_EINVAL, "h2o_cache_create: out is NULL");
+  *out = nullptr;
+  if (batch < 1 || heads < 1) return fail(H2O_EINVAL, "h2o_cache_create: batch and heads must be >= 1");
+  if (head_dim != 64 && head_dim != 128) return fail(H2O_EINVAL, "h2o_cache_create: head_dim must be 64 or 128");
+  if (heavy_budget < 0) return fail(H2O_EINVAL, "h2o_cache_create: heavy_budget must be >= 0");
+  if (recent_budget < 1) return fail(H2O_EINVAL, "h2o_cache_create: recent_budget must be >= 1");
+  if (kv_dtype != H2O_F16 && kv_dtype != H2O_F32) return fail(H2O_EINVAL, "h2o_cache_create: bad kv_dtype");
+  const long long C = static_cast<long long>(heavy_budget) + recent_budget;
+  if (C > kMaxSlots) return fail(H2O_EINVAL, "h2o_cache_create: heavy+recent must be <= %d", kMaxSlots);
+  const long long P = static_cast<long long>(batch) * heads;
+  if (P > 65535) return fail(H2O_EINVAL, "h2o_cache_create: batch*heads must be <= 65535");
+
+  h2o_cache* c = new (std::nothrow) h2o_cache();
+  if (!c) return fail(H2O_ENOMEM, "h2o_cache_create: host allocation failed");
+  std::memset(c, 0, sizeof(*c));
+  c->B = batch;
+  c->H = heads;
+  c->D = head_dim;
+  c->heavy = heavy_budget;
+  c->recent = recent_budget;
+  c->C = static_cast<int>(C);
+  c->dtype = kv_dtype;
+  c->elem = kv_dtype == H2O_F16 ? 2 : 4;
+  c->P = static_cast<int>(P);
+  cudaError_t e = cudaGetDevice(&c->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+  if (e != cudaSuccess) {
+    delete c;
+    return cuda_fail(e, "h2o_cache_create: no CUDA device");
+  }
+  const size_t nslot = static_cast<size_t>(c->P) * c->C;
+  const size_t nring = static_cast<size_t>(c->P) * c->recent;
+  if ((e = cudaMalloc(&c->K, kv_bytes(c))) != cudaSuccess || (e = cudaMalloc(&c->V, kv_bytes(c))) != cudaSuccess ||
+      (e = cudaMalloc(&c->score, nslot * sizeof(float))) != cudaSuccess ||
+      (e = cudaMalloc(&c->pos, nslot * sizeof(int))) != cudaSuccess ||
+      (e = cudaMalloc(&c->ring, nring * sizeof(int))) != cudaSuccess ||
+      (e = cudaMalloc(&c->ctr, static_cast<size_t>(c->P) * sizeof(h2o::PairCtr))) != cudaSuccess ||
+      (e = cudaMalloc(&c->err, sizeof(int))) != cudaSuccess) {
+    h2o_cache_destroy(c);
+    return cuda_fail(e, "h2o_cache_create: cudaMalloc");
+  }
+  if ((e = cudaMemset(c->K, 0, kv_bytes(c))) != cudaSuccess || (e = cudaMemset(c->V, 0, kv_bytes(c))) != cudaSuccess ||
+      (e = cudaMemset(c->score, 0, nslot * sizeof(float))) != cudaSuccess ||
+      (e = cudaMemset(c->pos, 0xff, nslot * sizeof(int))) != cudaSuccess ||
+      (e = cudaMemset(c->ring, 0xff, nring * sizeof(int))) != cudaSuccess ||
+      (e = cudaMemset(c->ctr, 0, static_cast<size_t>(c->P) * sizeof(h2o::PairCtr))) != cudaSuccess ||
+      (e = cudaMemset(c->err, 0, sizeof(int))) != cudaSuccess || (e = cudaDeviceSynchronize()) != cudaSuccess) {
+    h2o_cache_destroy(c);
+    return cuda_fail(e, "h2o_cache_create: initialisation");
+  }
+  // pick the cluster size; fall back to smaller clusters if the device
+  // cannot co-schedule the preferred one
+  c->splits_auto = auto_splits(c->P, c->C, c->num_sms);
+  while (c->splits_auto > 1 &&
+         h2o::decode_max_active_clusters(c->dtype, c->D, c->splits_auto, chunk_for(c->C, c->splits_auto), c->P) < 1 &&
+         chunk_for(c->C, c->splits_auto / 2) <= h2o::decode_max_chunk())
+    c->splits_auto /= 2;
+  *out = c;
+  return H2O_OK;
+}
+
+void h2o_cache_destroy(h2o_cache* c) {
+  if (!c) return;
+  cudaFree(c->K);
+  cudaFree(c->V);
+  cudaFree(c->score);
+  cudaFree(c->pos);
+  cudaFree(c->ring);
+  cudaFree(c->ctr);
+  cudaFree(c->err);
+  cudaFree(c->ws);
+  delete c;
+}
+
+int h2o_cache_reset(h2o_cache* c, void* stream) {
+  if (!c) return fail(H2O_EINVAL, "h2o_cache_reset: cache is NULL");
+  cudaError_t e = h2o::launch_reset(c->ctr, c->pos, c->score, c->ring, c->P, c->C, c->recent, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "h2o_cache_reset");
+  c->host_next_p = 0;
+  return H2O_OK;
+}
+
+int h2o_prefill_ex(h2o_cache* c, const void* q, const void* k, const void* v, int prompt_len, float scale,
+                   float* out_or_null, float* colsum_or_null, float* lse_or_null, void* stream) {
+  if (!c) return fail(H2O_EINVAL, "h2o_prefill: cache is NULL");
+  if (prompt_len < 0) return fail(H2O_EINVAL, "h2o_prefill: prompt_len must be >= 0");
+  if (prompt_len == 0) return h2o_cache_reset(c, stream);
+  if (!q || !k || !v) return fail(H2O_EINVAL, "h2o_prefill: q, k and v are required");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (out_or_null && !aligned16(out_or_null)))
+    return fail(H2O_EINVAL, "h2o_prefill: device pointers must be 16-byte aligned");
+  if (!(scale > 0.f) || scale != scale) return fail(H2O_EINVAL, "h2o_prefill: scale must be positive");
+  const size_t need = static_cast<size_t>(prompt_len);
+  cudaError_t e;
+  if (need > c->ws_len) {
+    // grow the workspace: [P, L] log2-domain lse + [P, L] column sums
+    if (c->ws) {
+      if ((e = cudaStreamSynchronize(as_stream(stream))) != cudaSuccess) return cuda_fail(e, "h2o_prefill: sync");
+      cudaFree(c->ws);
+      c->ws = nullptr;
+      c->ws_len = 0;
+    }
+    if ((e = cudaMalloc(&c->ws, 2 * need * c->P * sizeof(float))) != cudaSuccess)
+      return cuda_fail(e, "h2o_prefill: workspace cudaMalloc");
+    c->ws_len = need;
+  }
+  const size_t plen = static_cast<size_t>(c->P) * prompt_len;
+  h2o::PrefillParams pp;
+  pp.q = q;
+  pp.k = k;
+  pp.v = v;
+  pp.out = out_or_null;
+  pp.lse2 = c->ws;
+  pp.colsum = colsum_or_null ? colsum_or_null : c->ws + plen;
+  pp.L = prompt_len;
+  pp.qscale = scale * 1.4426950408889634f;
+  cudaStream_t s = as_stream(stream);
+  if ((e = h2o::launch_prefill_stats(pp, c->dtype, c->D, c->P, s)) != cudaSuccess)
+    return cuda_fail(e, "h2o_prefill: row statistics launch");
+  if ((e = h2o::launch_prefill_colsum(pp, c->dtype, c->D, c->P, s)) != cudaSuccess)
+    return cuda_fail(e, "h2o_prefill: column sum launch");
+  h2o::SelectParams sp;
+  sp.k = k;
+  sp.v = v;
+  sp.colsum = pp.colsum;
+  sp.K = c->K;
+  sp.V = c->V;
+  sp.score = c->score;
+  sp.pos = c->pos;
+  sp.ring = c->ring;
+  sp.ctr = c->ctr;
+  sp.err = c->err;
+  sp.L = prompt_len;
+  sp.heavy = c->heavy;
+  sp.recent = c->recent;
+  sp.C = c->C;
+  if ((e = h2o::launch_prefill_select(sp, c->dtype, c->D, c->P, s)) != cudaSuccess)
+    return cuda_fail(e, "h2o_prefill: select launch");
+  if (lse_or_null && (e = h2o::launch_lse_export(pp.lse2, lse_or_null, plen, s)) != cudaSuccess)
+    return cuda_fail(e, "h2o_prefill: lse export");
+  c->host_next_p = prompt_len;
+  return H2O_OK;
+}
+
+int h2o_prefill(h2o_cache* c, const void* q, const void* k, const void* v, int prompt_len, float scale,
+                float* out_or_null, void* stream) {
+  return h2o_prefill_ex(c, q, k, v, prompt_len, scale, out_or_null, nullptr, nullptr, stream);
+}
+
+int h2o_decode_step(h2o_cache* c, const void* q, const void* k_new, const void* v_new, float scale, float* out,
+                    int32_t* evicted_or_null, void* stream) {
+  if (!c) return fail(H2O_EINVAL, "h2o_decode_step: cache is NULL");
+  if (!q || !k_new || !v_new || !out) return fail(H2O_EINVAL, "h2o_decode_step: q, k_new, v_new and out are required");
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out))
+    return fail(H2O_EINVAL, "h2o_decode_step: device pointers must be 16-byte aligned");
+  if (!(scale > 0.f) || scale != scale) return fail(H2O_EINVAL, "h2o_decode_step: scale must be positive");
+  if (c->host_next_p >= INT_MAX) return fail(H2O_ESTATE, "h2o_decode_step: int32 positions exhausted");
+  const int splits = splits_in_use(c);
+  h2o::DecodeParams dp;
+  dp.K = c->K;
+  dp.V = c->V;
+  dp.score = c->score;
+  dp.pos = c->pos;
+  dp.ring = c->ring;
+  dp.ctr = c->ctr;
+  dp.q = q;
+  dp.k_new = k_new;
+  dp.v_new = v_new;
+  dp.out = out;
+  dp.evicted = evicted_or_null;
+  dp.err = c->err;
+  dp.C = c->C;
+  dp.R = c->recent;
+  dp.chunk = chunk_for(c->C, splits);
+  dp.qscale = scale * 1.4426950408889634f;
+  cudaError_t e = h2o::launch_decode(dp, c->dtype, c->D, c->P, splits, 128, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "h2o_decode_step: launch");
+  c->host_next_p += 1;
+  return H2O_OK;
+}
+
+size_t h2o_cache_state_bytes(const h2o_cache* c) {
+  if (!c) return 0;
+  const size_t nslot = static_cast<size_t>(c->P) * c->C;
+  return kHeaderInts * sizeof(int) + 2 * kv_bytes(c) + nslot * (sizeof(float) + sizeof(int)) +
+         static_cast<size_t>(c->P) * c->recent * sizeof(int) + static_cast<size_t>(c->P) * sizeof(h2o::PairCtr);
+}
+
+int h2o_cache_export_state(const h2o_cache* c, void* host_buf, size_t bytes, void* stream) {
+  if (!c || !host_buf) return fail(H2O_EINVAL, "h2o_cache_export_state: NULL argument");
+  if (bytes < h2o_cache_state_bytes(c)) return fail(H2O_EINVAL, "h2o_cache_export_state: buffer too small");
+  int* hdr = static_cast<int*>(host_buf);
+  std::memset(hdr, 0, kHeaderInts * sizeof(int));
+  hdr[0] = kMagic;
+  hdr[1] = 1;
+  hdr[2] = c->B;
+  hdr[3] = c->H;
+  hdr[4] = c->D;
+  hdr[5] = c->heavy;
+  hdr[6] = c->recent;
+  hdr[7] = c->dtype;
+  unsigned char* p = static_cast<unsigned char*>(host_buf) + kHeaderInts * sizeof(int);
+  const size_t nslot = static_cast<size_t>(c->P) * c->C;
+  cudaStream_t s = as_stream(stream);
+  cudaError_t e;
+  struct {
+    const void* src;
+    size_t n;
+  } parts[] = {{c->K, kv_bytes(c)},
+               {c->V, kv_bytes(c)},
+               {c->score, nslot * sizeof(float)},
+               {c->pos, nslot * sizeof(int)},
+               {c->ring, static_cast<size_t>(c->P) * c->recent * sizeof(int)},
+               {c->ctr, static_cast<size_t>(c->P) * sizeof(h2o::PairCtr)}};
+  for (auto& part : parts) {
+    if ((e = cudaMemcpyAsync(p, part.src, part.n, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+      return cuda_fail(e, "h2o_cache_export_state: copy");
+    p += part.n;
+  }
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "h2o_cache_export_state: sync");
+  return H2O_OK;
+}
+
+int h2o_cache_import_state(h2o_cache* c, const void* host_buf, size_t bytes, void* stream) {
+  if (!c || !host_buf) return fail(H2O_EINVAL, "h2o_cache_import_state: NULL argument");
+  if (bytes < h2o_cache_state_bytes(c)) return fail(H2O_EINVAL, "h2o_cache_import_state: buffer too small");
+  const int* hdr = static_cast<const int*>(host_buf);
+  if (hdr[0] != kMagic || hdr[1] != 1 || hdr[2] != c->B || hdr[3] != c->H || hdr[4] != c->D ||
+      hdr[5] != c->heavy || hdr[6] != c->recent || hdr[7] != c->dtype)
+    return fail(H2O_EINVAL, "h2o_cache_import_state: header does not match this cache");
+  const unsigned char* p = static_cast<const unsigned char*>(host_buf) + kHeaderInts * sizeof(int);
+  const size_t nslot = static_cast<size_t>(c->P) * c->C;
+  const size_t nring = static_cast<size_t>(c->P) * c->recent;
+  // validate counters before they reach the device
+  const h2o::PairCtr* ctr =
+      reinterpret_cast<const h2o::PairCtr*>(p + 2 * kv_bytes(c) + nslot * 8 + nring * sizeof(int));
+  long long maxp = 0;
+  for (int i = 0; i < c->P; ++i) {
+    if (ctr[i].count < 0 || ctr[i].count > c->C || ctr[i].head < 0 || ctr[i].head >= c->recent || ctr[i].p < 0 ||
+        ctr[i].count > ctr[i].p)
+      return fail(H2O_EINVAL, "h2o_cache_import_state: counters of pair %d out of range", i);
+    if (ctr[i].p > maxp) maxp = ctr[i].p;
+  }
+  cudaStream_t s = as_stream(stream);
+  cudaError_t e;
+  struct {
+    void* dst;
+    size_t n;
+  } parts[] = {{c->K, kv_bytes(c)},         {c->V, kv_bytes(c)},
+               {c->score, nslot * sizeof(float)}, {c->pos, nslot * sizeof(int)},
+               {c->ring, nring * sizeof(int)},    {c->ctr, static_cast<size_t>(c->P) * sizeof(h2o::PairCtr)}};
+  for (auto& part : parts) {
+    if ((e = cudaMemcpyAsync(part.dst, p, part.n, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+      return cuda_fail(e, "h2o_cache_import_state: copy");
+    p += part.n;
+  }
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "h2o_cache_import_state: sync");
+  c->host_next_p = maxp;
+  return H2O_OK;
+}
+
+int h2o_cache_check(h2o_cache* c, void* stream) {
+  if (!c) return fail(H2O_EINVAL, "h2o_cache_check: cache is NULL");
+  cudaError_t e = cudaStreamSynchronize(as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "h2o_cache_check: stream");
+  int flags = 0;
+  if ((e = cudaMemcpy(&flags, c->err, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "h2o_cache_check: read flag");
+  if (flags) {
+    cudaMemset(c->err, 0, sizeof(int));
+    cudaDeviceSynchronize();
+    return fail(H2O_EDEVICE, "h2o_cache_check: device check fired (flags 0x%x:%s%s%s)", flags,
+                (flags & h2o::ERR_MBAR_TIMEOUT) ? " copy-wait-timeout" : "",
+                (flags & h2o::ERR_NO_CANDIDATE) ? " no-eviction-candidate" : "",
+                (flags & h2o::ERR_SELECT) ? " prefill-select" : "");
+  }
+  return H2O_OK;
+}
+
+int h2o_cache_set_decode_splits(h2o_cache* c, int splits) {
+  if (!c) return fail(H2O_EINVAL, "h2o_cache_set_decode_splits: cache is NULL");
+  if (splits != 0 && splits != 1 && splits != 2 && splits != 4 && splits != 8 && splits != 16)
+    return fail(H2O_EINVAL, "h2o_cache_set_decode_splits: splits must be 0, 1, 2, 4, 8 or 16");
+  if (splits > 0 && chunk_for(c->C, splits) > h2o::decode_max_chunk())
+    return fail(H2O_EINVAL, "h2o_cache_set_decode_splits: %d splits leave more than %d slots per CTA", splits,
+                h2o::decode_max_chunk());
+  if (splits > 0 && h2o::decode_max_active_clusters(c->dtype, c->D, splits, chunk_for(c->C, splits), c->P) < 1)
+    return fail(H2O_EINVAL, "h2o_cache_set_decode_splits: clusters of %d CTAs cannot be scheduled", splits);
+  c->splits_override = splits;
+  return H2O_OK;
+}
+
+int h2o_cache_info(const h2o_cache* c, int32_t* info) {
+  if (!c || !info) return fail(H2O_EINVAL, "h2o_cache_info: NULL argument");
+  info[0] = c->B;
+  info[1] = c->H;
+  info[2] = c->D;
+  info[3] = c->heavy;
+  info[4] = c->recent;
+  info[5] = c->dtype;
+  info[6] = splits_in_use(c);
+  info[7] = 128;
+  return H2O_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,108 @@
+// Internal definitions shared by the C-ABI layer and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace h2o {
+
+// Device error bits latched in h2o_cache::err (reported by h2o_cache_check).
+enum : int {
+  ERR_MBAR_TIMEOUT = 1,  // a bulk-copy barrier wait gave up
+  ERR_NO_CANDIDATE = 2,  // full cache but no slot outside the recent window
+  ERR_SELECT = 4,        // prefill selection did not find `heavy` keys
+};
+
+// Per-pair counters kept on the device so decode steps can be replayed from
+// a CUDA graph: next absolute position, occupied slots, ring head.
+struct PairCtr {
+  int p;
+  int count;
+  int head;
+  int pad;
+};
+
+struct DecodeParams {
+  void* K;            // [P, C, D] slot store, kv dtype
+  void* V;            // [P, C, D]
+  float* score;       // [P, C] accumulated attention
+  int* pos;           // [P, C] absolute position per slot, -1 = empty
+  int* ring;          // [P, R] slot ids of the recent window
+  PairCtr* ctr;       // [P]
+  const void* q;      // [P, D]
+  const void* k_new;  // [P, D]
+  const void* v_new;  // [P, D]
+  float* out;         // [P, D]
+  int* evicted;       // [P] or nullptr
+  int* err;
+  int C, R;
+  int chunk;          // slots per CTA of a pair's cluster (multiple of 4)
+  float qscale;       // scale * log2(e): logits kept in the base-2 domain
+};
+
+struct PrefillParams {
+  const void* q;  // [P, L, D]
+  const void* k;
+  const void* v;
+  float* out;     // [P, L, D] or nullptr
+  float* lse2;    // [P, L] log2-domain row log-sum-exp of the scaled logits
+  float* colsum;  // [P, L]
+  int L;
+  float qscale;   // scale * log2(e)
+};
+
+struct SelectParams {
+  const void* k;         // prompt keys   [P, L, D]
+  const void* v;         // prompt values [P, L, D]
+  const float* colsum;   // [P, L]
+  void* K;               // slot store [P, C, D]
+  void* V;
+  float* score;
+  int* pos;
+  int* ring;
+  PairCtr* ctr;
+  int* err;
+  int L, heavy, recent, C;
+};
+
+// Raise a kernel's dynamic shared-memory limit (and optionally allow
+// non-portable cluster sizes) once per process and device; later calls with
+// a smaller or equal size do nothing, so launches inside stream capture make
+// no attribute calls.
+cudaError_t kernel_attrs(const void* kern, size_t smem_bytes, bool nonportable_cluster);
+
+// Launchers (return the launch error; they do not synchronise).
+cudaError_t launch_decode(const DecodeParams& prm, int dtype, int D, int pairs, int splits, int threads,
+                          cudaStream_t s);
+int decode_max_active_clusters(int dtype, int D, int splits, int chunk, int pairs);
+int decode_max_chunk();
+
+cudaError_t launch_prefill_stats(const PrefillParams& prm, int dtype, int D, int pairs, cudaStream_t s);
+cudaError_t launch_prefill_colsum(const PrefillParams& prm, int dtype, int D, int pairs, cudaStream_t s);
+cudaError_t launch_prefill_select(const SelectParams& prm, int dtype, int D, int pairs, cudaStream_t s);
+cudaError_t launch_reset(PairCtr* ctr, int* pos, float* score, int* ring, int pairs, int C, int R,
+                         cudaStream_t s);
+// lse (natural log) from the log2-domain buffer, for callers that ask for it
+cudaError_t launch_lse_export(const float* lse2, float* lse, size_t n, cudaStream_t s);
+
+}  // namespace h2o
+
+// The opaque cache object behind the C ABI.
+struct h2o_cache {
+  int B, H, D, heavy, recent, C, dtype, elem, P;
+  void* K;
+  void* V;
+  float* score;
+  int* pos;
+  int* ring;
+  h2o::PairCtr* ctr;
+  int* err;
+  // prefill workspace, grown on demand: lse2 and colsum, [P, ws_len] each
+  float* ws;
+  size_t ws_len;
+  int device, num_sms;
+  int splits_override;
+  int splits_auto;
+  long long host_next_p;  // host mirror of the next position (overflow check)
+};

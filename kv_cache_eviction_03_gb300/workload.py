@@ -156,34 +156,41 @@ def _round(x: np.ndarray, dtype) -> np.ndarray:
     return x.astype(np.float32).astype(dtype)
 
 
-def _keys(w: Workload, seed: int, ids: np.ndarray, noise: np.ndarray) -> np.ndarray:
-    """k = 0.5*E[h][id] + noise; ids [B, T]; noise [B, H, T, D] float64."""
-    k = noise.copy()
+def _key_means(w: Workload, seed: int, ids: np.ndarray) -> np.ndarray:
+    """0.5 * E[h][id] for every head: float64 [H, *ids.shape, D]."""
+    uniq, inv = np.unique(ids, return_inverse=True)
+    out = np.empty((w.heads,) + ids.shape + (w.head_dim,))
     for h in range(w.heads):
-        k[:, h] += KEY_MEAN_WEIGHT * embedding_rows(seed, h, ids, w.head_dim)
-    return k
+        rows = KEY_MEAN_WEIGHT * embedding_rows(seed, h, uniq, w.head_dim)
+        out[h] = rows[inv.reshape(ids.shape)]
+    return out
 
 
 def prefill_inputs(w: Workload, seed: int | None = None, layer: int = 0):
     """q, k, v for the prompt: arrays [B, H, L, D] in the K/V dtype."""
     seed = seed_for(w.name) if seed is None else seed
     B, H, L, D = w.batch, w.heads, w.prompt, w.head_dim
-    ids = token_ids(w, seed, layer, np.arange(L))
-    q = _rng(seed, _KIND["q"], layer).standard_normal((B, H, L, D))
-    k = _keys(w, seed, ids, _rng(seed, _KIND["k"], layer).standard_normal((B, H, L, D)))
-    v = _rng(seed, _KIND["v"], layer).standard_normal((B, H, L, D))
     t = w.np_dtype
-    return _round(q, t), _round(k, t), _round(v, t)
+    ids = token_ids(w, seed, layer, np.arange(L))
+    q, k, v = (np.empty((B, H, L, D), dtype=t) for _ in range(3))
+    gq, gk, gv = (_rng(seed, _KIND[x], layer) for x in ("q", "k", "v"))
+    # drawn one batch row at a time (same stream order as one [B,H,L,D] draw)
+    for b in range(B):
+        q[b] = _round(gq.standard_normal((H, L, D)), t)
+        mean = _key_means(w, seed, ids[b])  # [H, L, D]
+        k[b] = _round(gk.standard_normal((H, L, D)) + mean, t)
+        v[b] = _round(gv.standard_normal((H, L, D)), t)
+    return q, k, v
 
 
 def decode_inputs(w: Workload, position: int, seed: int | None = None, layer: int = 0):
     """q, k_new, v_new for the token at absolute `position`: arrays [B, H, D]."""
     seed = seed_for(w.name) if seed is None else seed
     B, H, D = w.batch, w.heads, w.head_dim
-    ids = token_ids(w, seed, layer, np.array([position]))
+    ids = token_ids(w, seed, layer, np.array([position]))[:, 0]  # [B]
     q = _rng(seed, _KIND["qd"], layer, position).standard_normal((B, H, D))
-    kn = _rng(seed, _KIND["kd"], layer, position).standard_normal((B, H, 1, D))
-    k = _keys(w, seed, ids, kn)[:, :, 0]
+    k = _rng(seed, _KIND["kd"], layer, position).standard_normal((B, H, D))
+    k += np.moveaxis(_key_means(w, seed, ids), 0, 1)  # [B, H, D]
     v = _rng(seed, _KIND["vd"], layer, position).standard_normal((B, H, D))
     t = w.np_dtype
     return _round(q, t), _round(k, t), _round(v, t)

@@ -59,13 +59,14 @@ def causal_attention_stats(q, k, v, scale):
     attention token j has received after the prompt), O_i = sum_j p_ij v_j.
     """
     L = q.shape[0]
-    s = scale * (q @ k.T)
-    future = np.triu(np.ones((L, L), dtype=bool), k=1)
-    s[future] = -np.inf
+    s = q @ k.T
+    s *= scale
+    s[np.triu_indices(L, k=1)] = -np.inf  # token i sees positions j <= i only
     m = s.max(axis=1, keepdims=True)
-    e = np.exp(s - m)
-    z = e.sum(axis=1, keepdims=True)
-    p = e / z
+    s -= m
+    p = np.exp(s, out=s)  # in place: the [L, L] matrix is the large one
+    z = p.sum(axis=1, keepdims=True)
+    p /= z
     lse = (m + np.log(z))[:, 0]
     colsum = p.sum(axis=0)
     out = p @ v
@@ -84,11 +85,11 @@ def select_prefill(colsum, L, heavy, recent):
     C = heavy + recent
     if L <= C:
         return list(range(L))
-    cand = list(range(L - recent))
-    score = to_f32(colsum)
-    ranked = sorted(cand, key=lambda j: (score[j], j), reverse=True)
-    heavy_pos = sorted(ranked[:heavy])
-    return heavy_pos + list(range(L - recent, L))
+    n = L - recent
+    score = to_f32(colsum[:n])
+    ascending = np.lexsort((np.arange(n), score))  # by score, then position
+    heavy_pos = sorted(ascending[n - heavy:].tolist()) if heavy else []
+    return heavy_pos + list(range(n, L))
 
 
 @dataclass
@@ -183,11 +184,11 @@ def decode_step_pair(st: PairState, q, k_new, v_new, scale, heavy, recent) -> St
         evicted = -1
         st.count = n + 1
     else:
-        cand = [j for j in range(C) if st.pos[j] <= p - recent]
-        ranked = sorted(cand, key=lambda j: (st.score[j], st.pos[j]))
-        u = ranked[0]
+        cand = np.nonzero(st.pos[:C] <= p - recent)[0]
+        ranked = cand[np.lexsort((st.pos[cand], st.score[cand]))]  # by score, then position
+        u = int(ranked[0])
         evicted = u
-        if len(ranked) > 1:
+        if ranked.size > 1:
             gap = st.score[ranked[1]] - st.score[ranked[0]]
 
     st.K[u] = k_new

@@ -1,0 +1,221 @@
+"""GPU parity of the fused decode step against the fp64 oracle.
+
+Step-wise protocol: before each checked step the oracle's own state is
+imported into the CUDA cache, both sides run one step on the same inputs, and
+outputs, evicted slots, scores, positions, ring and counters are compared
+(out within 2e-3 for fp16 K/V, 1e-5 for fp32; scores within 1e-5 relative;
+slots and positions bit-exact unless the oracle's two lowest candidate scores
+are within 1e-6).  Free-run protocol: both sides run a whole prefill + decode
+trajectory on their own and are compared step by step.
+"""
+import numpy as np
+import pytest
+
+from harness import StepReport, compare_decode_step, oracle_image, out_tol, NEAR_TIE
+from kv_cache_eviction_03_gb300 import binding as B
+from kv_cache_eviction_03_gb300 import workload as W
+from oracle import h2o_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def dtype_code(w):
+    return B.H2O_F16 if w.dtype == "f16" else B.H2O_F32
+
+
+def flat(a):
+    a = np.asarray(a, dtype=np.float64)
+    return a.reshape((-1,) + a.shape[2:])
+
+
+def oracle_start(w, seed):
+    if w.prompt:
+        q, k, v = W.prefill_inputs(w, seed)
+        st, _, _ = O.prefill(q, k, v, w.heavy, w.recent, w.scale)
+        return st
+    return O.empty_cache(w.pairs, w.heavy, w.recent, w.head_dim)
+
+
+def run_stepwise(w, seed, check=None, splits=None):
+    cache = B.h2o_cache_create(w.batch, w.heads, w.head_dim, w.heavy, w.recent, dtype_code(w))
+    if splits:
+        B.h2o_cache_set_decode_splits(cache, splits)
+    st = oracle_start(w, seed)
+    out = torch.empty((w.batch, w.heads, w.head_dim), dtype=torch.float32, device="cuda")
+    ev = torch.empty((w.batch, w.heads), dtype=torch.int32, device="cuda")
+    rep = StepReport()
+    P, D = w.pairs, w.head_dim
+    for t in range(w.decode):
+        qd, kd, vd = W.decode_inputs(w, w.prompt + t, seed)
+        nxt, r_out, r_ev, gap = O.decode_step(st, qd, kd, vd, w.heavy, w.recent, w.scale)
+        if check is None or t in check:
+            B.h2o_cache_import_state(cache, oracle_image(cache, st))
+            B.h2o_decode_step(cache, torch.from_numpy(qd).cuda(), torch.from_numpy(kd).cuda(),
+                              torch.from_numpy(vd).cuda(), w.scale, out, ev)
+            B.h2o_cache_check(cache)
+            after = B.unpack_state(cache, B.h2o_cache_export_state(cache))
+            compare_decode_step(cache, after, out.cpu().numpy().reshape(P, D), ev.cpu().numpy().reshape(P),
+                                st, nxt, r_out, r_ev, gap, rep, inputs=(flat(qd), flat(kd), flat(vd)),
+                                scale=w.scale)
+        st = nxt
+    B.h2o_cache_destroy(cache)
+    return rep
+
+
+def run_free(w, seed, splits=None):
+    """Both sides run prefill + every decode step on their own."""
+    cache = B.h2o_cache_create(w.batch, w.heads, w.head_dim, w.heavy, w.recent, dtype_code(w))
+    if splits:
+        B.h2o_cache_set_decode_splits(cache, splits)
+    P, D = w.pairs, w.head_dim
+    st = oracle_start(w, seed)
+    if w.prompt:
+        q, k, v = W.prefill_inputs(w, seed)
+        B.h2o_prefill(cache, torch.from_numpy(q).cuda(), torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(),
+                      w.scale)
+        g0 = B.unpack_state(cache, B.h2o_cache_export_state(cache))
+        alive = np.array([np.array_equal(g0["pos"][i], st.pos[i]) for i in range(P)])
+    else:
+        B.h2o_cache_reset(cache)
+        alive = np.ones(P, dtype=bool)
+    tol = out_tol(cache.kv_dtype)
+    out = torch.empty((w.batch, w.heads, D), dtype=torch.float32, device="cuda")
+    ev = torch.empty((w.batch, w.heads), dtype=torch.int32, device="cuda")
+    worst = 0.0
+    for t in range(w.decode):
+        qd, kd, vd = W.decode_inputs(w, w.prompt + t, seed)
+        B.h2o_decode_step(cache, torch.from_numpy(qd).cuda(), torch.from_numpy(kd).cuda(),
+                          torch.from_numpy(vd).cuda(), w.scale, out, ev)
+        st, r_out, r_ev, gap = O.decode_step(st, qd, kd, vd, w.heavy, w.recent, w.scale)
+        g_out = out.cpu().numpy().reshape(P, D)
+        g_ev = ev.cpu().numpy().reshape(P)
+        for i in np.nonzero(alive)[0]:
+            err = float(np.max(np.abs(g_out[i] - r_out[i])))
+            worst = max(worst, err)
+            assert err <= tol, f"step {t} pair {i}: out err {err}"
+            if g_ev[i] != r_ev[i]:
+                assert gap[i] <= NEAR_TIE, f"step {t} pair {i}: evicted {g_ev[i]} != {r_ev[i]}"
+                alive[i] = False  # trajectories legitimately part at a near tie
+    B.h2o_cache_check(cache)
+    g = B.unpack_state(cache, B.h2o_cache_export_state(cache))
+    for i in np.nonzero(alive)[0]:
+        assert np.array_equal(g["pos"][i], st.pos[i])
+        used = st.pos[i] >= 0
+        rel = np.abs(g["score"][i][used] - st.score[i][used]) / st.score[i][used]
+        assert rel.max() <= 1e-5
+    B.h2o_cache_destroy(cache)
+    return worst, int(alive.sum())
+
+
+TINY = W.WORKLOADS["tiny-ref"]
+
+
+def test_tiny_reference_workload_every_step():
+    """The 4-head fp32 workload (prompt 256 + 64 steps, 26+26 slots), all steps."""
+    rep = run_stepwise(TINY, W.seed_for("tiny-ref"))
+    assert rep.pairs == TINY.pairs * TINY.decode
+    assert rep.max_out_err <= 1e-5
+
+
+def test_tiny_reference_free_run():
+    worst, alive = run_free(TINY, W.seed_for("tiny-ref"))
+    assert alive >= TINY.pairs - 1
+
+
+SMALL = [
+    # name, batch, heads, D, dtype, prompt, decode, heavy, recent
+    ("f16-d128-ragged", 2, 3, 128, "f16", 100, 40, 20, 17),
+    ("f16-d64", 1, 5, 64, "f16", 90, 30, 13, 11),
+    ("f32-d128", 2, 2, 128, "f32", 70, 30, 9, 14),
+    ("fill-then-evict", 1, 4, 128, "f16", 10, 60, 25, 12),
+    ("no-prompt", 2, 2, 128, "f16", 0, 50, 20, 10),
+    ("no-heavy", 1, 3, 128, "f16", 60, 30, 0, 9),
+    ("recent-1", 1, 3, 64, "f32", 40, 30, 7, 1),
+    ("prompt-equals-cache", 1, 2, 128, "f16", 29, 20, 17, 12),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_small_shapes_every_step(case):
+    name, b, h, d, dt, L, T, hv, rc = case
+    w = W.Workload(name, b, h, d, dt, L, T, hv, rc, 1.1)
+    rep = run_stepwise(w, 7)
+    assert rep.pairs == w.pairs * T
+
+
+@pytest.mark.parametrize("splits", [1, 2, 4, 8, 16])
+def test_cluster_splits_agree(splits):
+    """Every cluster size gives the oracle's result, including ragged last CTAs
+    (301 slots) and CTAs whose slot range is still empty while filling."""
+    w = W.Workload("splits", 1, 4, 128, "f16", 280, 40, 150, 151, 1.1)
+    rep = run_stepwise(w, 11, check=set(range(0, 40, 3)) | {21, 22}, splits=splits)
+    assert rep.pairs > 0
+
+
+@pytest.mark.parametrize("splits", [1, 4, 16])
+def test_free_run_fp16(splits):
+    w = W.Workload("free", 2, 4, 128, "f16", 300, 80, 40, 30, 1.1)
+    worst, alive = run_free(w, 5, splits=splits)
+    assert alive >= w.pairs - 2
+
+
+def test_decode_rejects_wrong_shapes_and_devices():
+    w = W.Workload("x", 1, 2, 64, "f16", 0, 1, 4, 4, 1.1)
+    cache = B.h2o_cache_create(1, 2, 64, 4, 4, B.H2O_F16)
+    q = torch.zeros((1, 2, 64), dtype=torch.float16, device="cuda")
+    out = torch.empty((1, 2, 64), dtype=torch.float32, device="cuda")
+    with pytest.raises(ValueError):
+        B.h2o_decode_step(cache, q.float(), q, q, 0.1, out)
+    with pytest.raises(ValueError):
+        B.h2o_decode_step(cache, q.cpu(), q, q, 0.1, out)
+    with pytest.raises(B.H2OError):
+        B._check(B.lib().h2o_decode_step(cache.handle, q.data_ptr(), q.data_ptr(), q.data_ptr(), -1.0,
+                                         out.data_ptr(), None, None))
+    with pytest.raises(B.H2OError):
+        B.h2o_cache_set_decode_splits(cache, 3)
+    B.h2o_cache_destroy(cache)
+
+
+def test_import_rejects_bad_counters():
+    cache = B.h2o_cache_create(1, 2, 64, 4, 4, B.H2O_F16)
+    img = B.h2o_cache_export_state(cache)
+    st = B.unpack_state(cache, img)
+    st["count"][0] = 99
+    with pytest.raises(B.H2OError):
+        B.h2o_cache_import_state(cache, img)
+    B.h2o_cache_destroy(cache)
+
+
+def test_graph_replay_matches_eager():
+    """Counters live on the device, so a captured step replays correctly."""
+    w = W.Workload("graph", 2, 4, 128, "f16", 64, 24, 16, 16, 1.1)
+    q, k, v = (torch.from_numpy(a).cuda() for a in W.prefill_inputs(w, 3))
+    seq = [tuple(torch.from_numpy(a).cuda() for a in W.decode_inputs(w, w.prompt + t, 3)) for t in range(w.decode)]
+    res = []
+    for use_graph in (False, True):
+        cache = B.h2o_cache_create(w.batch, w.heads, w.head_dim, w.heavy, w.recent, B.H2O_F16)
+        B.h2o_prefill(cache, q, k, v, w.scale)
+        xq, xk, xv = (torch.empty_like(seq[0][0]) for _ in range(3))
+        out = torch.empty((w.batch, w.heads, w.head_dim), dtype=torch.float32, device="cuda")
+        outs = []
+        if use_graph:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                B.h2o_decode_step(cache, xq, xk, xv, w.scale, out, stream=s)
+            torch.cuda.current_stream().wait_stream(s)
+        for t in range(w.decode):
+            xq.copy_(seq[t][0]); xk.copy_(seq[t][1]); xv.copy_(seq[t][2])
+            if use_graph:
+                g.replay()
+            else:
+                B.h2o_decode_step(cache, xq, xk, xv, w.scale, out)
+            outs.append(out.clone())
+        torch.cuda.synchronize()
+        res.append((torch.stack(outs).cpu(), B.h2o_cache_export_state(cache)))
+        B.h2o_cache_destroy(cache)
+    assert torch.equal(res[0][0], res[1][0])
+    assert np.array_equal(res[0][1], res[1][1])

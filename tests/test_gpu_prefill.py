@@ -1,0 +1,127 @@
+"""GPU parity of the prefill (row statistics, column sums, keep rule, slot
+layout) against the fp64 oracle."""
+import math
+
+import numpy as np
+import pytest
+
+from harness import NEAR_TIE, heavy_boundary_gap, out_tol
+from kv_cache_eviction_03_gb300 import binding as B
+from kv_cache_eviction_03_gb300 import workload as W
+from oracle import h2o_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def check_prefill(w, seed, pairs=None, with_out=True):
+    """Run the GPU prefill on the full shape, compare `pairs` (default all)."""
+    dt = B.H2O_F16 if w.dtype == "f16" else B.H2O_F32
+    cache = B.h2o_cache_create(w.batch, w.heads, w.head_dim, w.heavy, w.recent, dt)
+    q, k, v = W.prefill_inputs(w, seed)
+    L, P, D = w.prompt, w.pairs, w.head_dim
+    dev = lambda a: torch.from_numpy(a).cuda()
+    out = torch.empty((w.batch, w.heads, L, D), dtype=torch.float32, device="cuda") if with_out else None
+    colsum = torch.empty((w.batch, w.heads, L), dtype=torch.float32, device="cuda")
+    lse = torch.empty((w.batch, w.heads, L), dtype=torch.float32, device="cuda")
+    B.h2o_prefill_ex(cache, dev(q), dev(k), dev(v), w.scale, out=out, colsum=colsum, lse=lse)
+    B.h2o_cache_check(cache)
+    g = B.unpack_state(cache, B.h2o_cache_export_state(cache))
+    g_cs = colsum.cpu().numpy().reshape(P, L).astype(np.float64)
+    g_lse = lse.cpu().numpy().reshape(P, L).astype(np.float64)
+    g_out = out.cpu().numpy().reshape(P, L, D) if with_out else None
+    qf, kf, vf = (a.reshape(P, L, D).astype(np.float64) for a in (q, k, v))
+    tol = out_tol(dt)
+    stats = {"colsum_rel": 0.0, "out_err": 0.0, "lse_err": 0.0, "ties": 0}
+    for i in (range(P) if pairs is None else pairs):
+        st, cs, o = O.prefill_pair(qf[i], kf[i], vf[i], w.heavy, w.recent, w.scale)
+        lse_ref, _, _ = O.causal_attention_stats(qf[i], kf[i], vf[i], w.scale) if L <= 4096 else (None, 0, 0)
+        rel = float(np.max(np.abs(g_cs[i] - cs) / cs))
+        stats["colsum_rel"] = max(stats["colsum_rel"], rel)
+        assert rel <= 1e-5, f"pair {i}: colsum rel err {rel}"
+        assert abs(g_cs[i].sum() - L) <= 1e-5 * L
+        if lse_ref is not None:
+            e = float(np.max(np.abs(g_lse[i] - lse_ref)))
+            stats["lse_err"] = max(stats["lse_err"], e)
+            assert e <= 5e-5, f"pair {i}: lse err {e}"
+        if with_out:
+            e = float(np.max(np.abs(g_out[i] - o)))
+            stats["out_err"] = max(stats["out_err"], e)
+            assert e <= tol, f"pair {i}: out err {e}"
+        gap = heavy_boundary_gap(O.to_f32(cs), L, w.heavy, w.recent)
+        if not np.array_equal(g["pos"][i], st.pos):
+            assert gap <= NEAR_TIE, f"pair {i}: kept positions differ (boundary gap {gap})"
+            stats["ties"] += 1
+            continue
+        used = st.pos >= 0
+        assert np.array_equal(g["score"][i][used], st.score[used].astype(np.float32)) or \
+            np.max(np.abs(g["score"][i][used] - st.score[used]) / st.score[used]) <= 1e-5
+        kd = np.float16 if w.dtype == "f16" else np.float32
+        assert np.array_equal(g["K"][i][used], st.K[used].astype(kd))
+        assert np.array_equal(g["V"][i][used], st.V[used].astype(kd))
+        assert np.array_equal(g["ring"][i], st.ring)
+        assert (g["p"][i], g["count"][i], g["head"][i]) == (st.p, st.count, st.head)
+    B.h2o_cache_destroy(cache)
+    return stats
+
+
+CASES = [
+    # name, batch, heads, D, dtype, L, heavy, recent
+    ("f16-d128-L200", 1, 3, 128, "f16", 200, 30, 20),
+    ("f16-d128-L64", 2, 2, 128, "f16", 64, 10, 10),
+    ("f16-d128-L65", 2, 2, 128, "f16", 65, 10, 10),
+    ("f16-d128-L1", 1, 2, 128, "f16", 1, 4, 3),
+    ("f16-d64-L257", 1, 3, 64, "f16", 257, 40, 33),
+    ("f16-keep-all", 1, 2, 128, "f16", 50, 40, 30),
+    ("f16-keep-all-short", 1, 2, 128, "f16", 7, 40, 30),
+    ("f16-no-heavy", 1, 2, 128, "f16", 130, 0, 17),
+    ("f16-L-eq-C", 1, 2, 64, "f16", 48, 24, 24),
+    ("f16-L-eq-C+1", 1, 2, 64, "f16", 49, 24, 24),
+    ("f32-d64-L300", 1, 2, 64, "f32", 300, 30, 30),
+    ("f32-d128-L97", 2, 1, 128, "f32", 97, 11, 9),
+    ("f16-large-heavy", 1, 1, 128, "f16", 1500, 700, 100),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_prefill_parity(case):
+    name, b, h, d, dt, L, hv, rc = case
+    w = W.Workload(name, b, h, d, dt, L, 0, hv, rc, 1.1)
+    check_prefill(w, 13)
+
+
+def test_prefill_without_output():
+    w = W.Workload("noout", 1, 2, 128, "f16", 180, 0, 20, 20, 1.1)
+    check_prefill(w, 17, with_out=False)
+
+
+def test_tiny_reference_prefill():
+    w = W.WORKLOADS["tiny-ref"]
+    s = check_prefill(w, W.seed_for("tiny-ref"))
+    assert s["out_err"] <= 1e-5
+
+
+def test_constant_keys_harmonic_colsum_on_gpu():
+    """Equal keys: colsum_j = H_L - H_j exactly in real arithmetic."""
+    L, D = 300, 128
+    cache = B.h2o_cache_create(1, 1, D, 20, 20, B.H2O_F16)
+    rng = np.random.default_rng(0)
+    q = torch.from_numpy(rng.standard_normal((1, 1, L, D)).astype(np.float16)).cuda()
+    k = torch.from_numpy(np.tile(rng.standard_normal(D).astype(np.float16), (1, 1, L, 1))).cuda()
+    v = torch.from_numpy(rng.standard_normal((1, 1, L, D)).astype(np.float16)).cuda()
+    cs = torch.empty((1, 1, L), dtype=torch.float32, device="cuda")
+    B.h2o_prefill_ex(cache, q, k, v, 1 / math.sqrt(D), colsum=cs)
+    Hn = np.concatenate([[0.0], np.cumsum(1.0 / np.arange(1, L + 1))])
+    np.testing.assert_allclose(cs.cpu().numpy()[0, 0], Hn[L] - Hn[:L], rtol=1e-5)
+    B.h2o_cache_destroy(cache)
+
+
+def test_prefill_zero_length_empties_cache():
+    cache = B.h2o_cache_create(1, 2, 64, 4, 4, B.H2O_F16)
+    B.h2o_prefill(cache, torch.zeros((1, 2, 0, 64), dtype=torch.float16, device="cuda"),
+                  torch.zeros((1, 2, 0, 64), dtype=torch.float16, device="cuda"),
+                  torch.zeros((1, 2, 0, 64), dtype=torch.float16, device="cuda"), 0.125)
+    g = B.unpack_state(cache, B.h2o_cache_export_state(cache))
+    assert (g["pos"] == -1).all() and (g["count"] == 0).all() and (g["p"] == 0).all()
+    B.h2o_cache_destroy(cache)
