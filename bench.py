@@ -91,17 +91,19 @@ def oracle_sample(w, seed, batch_rows=1, decode_steps=None):
     return ws, (q, k, v, dq, dk, dv), T
 
 
-def time_oracle(w, seed, workers=None, batch_rows=1):
+def time_oracle(w, seed, workers=None, batch_rows=4):
     """fp64 oracle on the host cores over a sample of the workload; returns
     (tokens/s/layer scaled to the whole workload, cores, sample text, seconds)."""
     import multiprocessing as mp
 
     ws, (q, k, v, dq, dk, dv), T = oracle_sample(w, seed, batch_rows)
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    workers = workers or min(cores, ws.heads)
-    # one task per head (pairs are independent); single-threaded BLAS per worker
-    tasks = [(q[:, h:h + 1], k[:, h:h + 1], v[:, h:h + 1], dq[:, :, h:h + 1], dk[:, :, h:h + 1], dv[:, :, h:h + 1],
-              w.heavy, w.recent, w.scale) for h in range(ws.heads)]
+    workers = workers or min(cores, ws.pairs)
+    # one task per (batch row, head) pair (pairs are independent);
+    # single-threaded BLAS per worker
+    tasks = [(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1], dq[:, b:b + 1, h:h + 1],
+              dk[:, b:b + 1, h:h + 1], dv[:, b:b + 1, h:h + 1], w.heavy, w.recent, w.scale)
+             for b in range(ws.batch) for h in range(ws.heads)]
     env_keep = {x: os.environ.get(x) for x in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
     for x in env_keep:
         os.environ[x] = "1"
