@@ -138,6 +138,28 @@ H2O_API int h2o_cache_set_decode_splits(h2o_cache* cache, int splits);
  *               decode splits in use, decode threads per CTA}. */
 H2O_API int h2o_cache_info(const h2o_cache* cache, int32_t* info);
 
+/* Column sums of the prefill without any device allocation.  The paper has
+ * no counterpart: this exists for callers that cannot call cudaMalloc, such
+ * as engines that hand out all device memory from their own pools and forbid
+ * allocation after start-up, or loops that cannot afford the device-wide
+ * synchronisation a cudaMalloc implies.  It computes exactly what
+ * h2o_prefill_ex returns in colsum_or_null (same kernels, same order):
+ *   colsum[b,h,j] = sum_{i>=j} softmax_i(scale * q_i . k_j)    (causal rows)
+ * q, k: [B, H, L, D] device pointers in kv_dtype (16-byte aligned); colsum:
+ * [B, H, L] float32 device output.  No cache is involved and nothing is kept.
+ * The per-row log-sum-exp scratch lives in a fixed array inside the library
+ * (8 MiB, held on every GPU that loads the library until the process exits),
+ * so B*H*L must be <= 2,097,152; larger sizes return H2O_EINVAL before any
+ * launch.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call shares the one array: calls whose
+ * kernels overlap on the GPU (different streams, or several host threads)
+ * race and corrupt each other's results, so serialise them.  Each call
+ * writes every scratch entry it reads, so stale contents from a previous
+ * call do no harm.  Asynchronous on `stream`. */
+H2O_API int h2o_prefill_colsum_static(const void* q, const void* k, int batch, int heads, int head_dim,
+                                      int prompt_len, int kv_dtype, float scale, float* colsum, void* stream);
+
 /* Thread-local message describing the last error returned on this thread. */
 H2O_API const char* h2o_last_error(void);
 

@@ -40,6 +40,8 @@ SIGNATURES = {
     "h2o_cache_check": (_c_int, [_c_void_p, _c_void_p]),
     "h2o_cache_set_decode_splits": (_c_int, [_c_void_p, _c_int]),
     "h2o_cache_info": (_c_int, [_c_void_p, ctypes.POINTER(ctypes.c_int32)]),
+    "h2o_prefill_colsum_static": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
+                                           _c_void_p, _c_void_p]),
     "h2o_last_error": (ctypes.c_char_p, []),
 }
 
@@ -215,6 +217,21 @@ def h2o_cache_info(cache: Cache) -> list[int]:
     info = (ctypes.c_int32 * 8)()
     _check(lib().h2o_cache_info(cache.handle, info))
     return list(info)
+
+
+def h2o_prefill_colsum_static(q, k, scale, colsum, kv_dtype=None, stream=None):
+    """Column sums of a prompt with no device allocation (fixed library
+    scratch; see include/h2o.h for the size limit and the no-overlap rule)."""
+    import torch
+
+    B, H, L, D = q.shape
+    dt = q.dtype
+    code = H2O_F16 if dt == torch.float16 else H2O_F32
+    if kv_dtype is not None and kv_dtype != code:
+        raise ValueError("kv_dtype does not match the tensors")
+    _check(lib().h2o_prefill_colsum_static(
+        _ptr(q, dt, (B, H, L, D), "q"), _ptr(k, dt, (B, H, L, D), "k"), B, H, D, L, code, float(scale),
+        _ptr(colsum, torch.float32, (B, H, L), "colsum"), _stream(stream)))
 
 
 def h2o_last_error() -> str:

@@ -61,6 +61,14 @@ cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 }  // namespace
 
 namespace h2o {
+int set_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
 cudaError_t kernel_attrs(const void* kern, size_t smem_bytes, bool nonportable_cluster) {
   static std::mutex mu;
   static std::map<std::pair<const void*, int>, size_t> done;

@@ -66,6 +66,9 @@ struct SelectParams {
   int L, heavy, recent, C;
 };
 
+// Record the thread-local message returned by h2o_last_error(); returns code.
+int set_error(int code, const char* fmt, ...);
+
 // Raise a kernel's dynamic shared-memory limit (and optionally allow
 // non-portable cluster sizes) once per process and device; later calls with
 // a smaller or equal size do nothing, so launches inside stream capture make
