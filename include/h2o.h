@@ -130,12 +130,16 @@ H2O_API int h2o_cache_import_state(h2o_cache* cache, const void* host_buf, size_
  * pending CUDA error as H2O_ECUDA. */
 H2O_API int h2o_cache_check(h2o_cache* cache, void* stream);
 
-/* Tuning: number of CTAs (a thread-block cluster) that share one pair in the
- * decode kernel, 0 = automatic.  Must be 1, 2, 4, 8 or 16. */
-H2O_API int h2o_cache_set_decode_splits(h2o_cache* cache, int splits);
+/* Tuning of the decode kernel's launch shape: `splits` CTAs (one thread-block
+ * cluster) share a pair, each streaming its slots through a ring of `stages`
+ * 16-row shared-memory stages.  0 = automatic for either value.  splits must
+ * be 1, 2, 4, 8 or 16, stages 1..16; H2O_EINVAL if the shape cannot be
+ * scheduled on the current device. */
+H2O_API int h2o_cache_set_decode_shape(h2o_cache* cache, int splits, int stages);
 
-/* info[0..7] = {batch, heads, head_dim, heavy, recent, kv_dtype,
- *               decode splits in use, decode threads per CTA}. */
+/* info[0..9] = {batch, heads, head_dim, heavy, recent, kv_dtype,
+ *               decode splits in use, decode stages in use, decode threads
+ *               per CTA, 0}. */
 H2O_API int h2o_cache_info(const h2o_cache* cache, int32_t* info);
 
 /* Column sums of the prefill without any device allocation.  The paper has

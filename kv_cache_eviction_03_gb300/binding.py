@@ -38,7 +38,7 @@ SIGNATURES = {
     "h2o_cache_export_state": (_c_int, [_c_void_p, _c_void_p, _c_size_t, _c_void_p]),
     "h2o_cache_import_state": (_c_int, [_c_void_p, _c_void_p, _c_size_t, _c_void_p]),
     "h2o_cache_check": (_c_int, [_c_void_p, _c_void_p]),
-    "h2o_cache_set_decode_splits": (_c_int, [_c_void_p, _c_int]),
+    "h2o_cache_set_decode_shape": (_c_int, [_c_void_p, _c_int, _c_int]),
     "h2o_cache_info": (_c_int, [_c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     "h2o_prefill_colsum_static": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
                                            _c_void_p, _c_void_p]),
@@ -209,12 +209,12 @@ def h2o_cache_check(cache: Cache, stream=None):
     _check(lib().h2o_cache_check(cache.handle, _stream(stream)))
 
 
-def h2o_cache_set_decode_splits(cache: Cache, splits: int):
-    _check(lib().h2o_cache_set_decode_splits(cache.handle, splits))
+def h2o_cache_set_decode_shape(cache: Cache, splits: int = 0, stages: int = 0):
+    _check(lib().h2o_cache_set_decode_shape(cache.handle, splits, stages))
 
 
 def h2o_cache_info(cache: Cache) -> list[int]:
-    info = (ctypes.c_int32 * 8)()
+    info = (ctypes.c_int32 * 10)()
     _check(lib().h2o_cache_info(cache.handle, info))
     return list(info)
 

@@ -11,18 +11,29 @@
 // GB300 design.  Decode reads every kept K and V row once per step: about
 // 1 FLOP per byte, so the kernel is bound by HBM bandwidth and uses no tensor
 // cores.  One pair (batch row, head) is handled by a thread-block cluster of S
-// CTAs; CTA r owns the contiguous slot range [r*chunk, (r+1)*chunk).  Each CTA
-// streams its K and V rows through a ring of shared-memory stages filled by
-// 1-D bulk async copies (cp.async.bulk, mbarrier completion) and keeps a
-// base-2 online softmax (m, l, o) per row group.  The CTAs then exchange their
-// partial (m, l, o) through distributed shared memory, so every CTA knows the
-// pair's global max and normaliser without a second pass over K: each turns
-// its own logits (kept in shared memory) into probabilities, adds them to its
-// slots' scores, and proposes its lowest candidate key (score bits, position)
-// packed in 64 bits (non-negative float bits order like the floats).  The
-// cluster's minimum is the victim; the CTA that owns it writes the new row.
-// Cluster barriers are hardware barriers of co-scheduled CTAs: no CTA spins
-// on another.
+// CTAs; CTA r owns the contiguous slot range [r*chunk, (r+1)*chunk), and S is
+// chosen so that every CTA of the grid is resident at once.
+//
+// Inside a CTA one producer warp streams the CTA's K and V rows, 16 rows per
+// stage, through a ring of shared-memory stages with 1-D bulk async copies
+// (cp.async.bulk, full/empty mbarriers, L2 evict-first), after one bulk L2
+// prefetch of the CTA's whole K and V range; four consumer warps
+// compute the logits and a base-2 online softmax (m, l, o) per row group and
+// release each stage with an mbarrier arrive, so the streaming loop has no
+// block-wide barrier.  When the previous kernel on the stream worked on a
+// different cache, the producer starts streaming before the programmatic
+// grid-dependency wait, overlapping this step's loads with the tail of the
+// previous kernel; only reads of the step's inputs (q, k_new, v_new) and all
+// writes wait for it.
+//
+// The cluster's CTAs then exchange partial (m, l, o) through distributed
+// shared memory, so every CTA knows the pair's global max and normaliser
+// without a second pass over K: each turns its own logits (kept in shared
+// memory) into probabilities, adds them to its slots' scores, and proposes its
+// lowest candidate key (score bits, position) packed in 64 bits (non-negative
+// float bits order like the floats).  The cluster minimum is the victim; the
+// CTA that owns it writes the new row.  Cluster barriers are hardware barriers
+// of co-scheduled CTAs: no CTA spins on another.
 #include <cooperative_groups.h>
 #include <cuda_fp16.h>
 
@@ -38,21 +49,23 @@ constexpr float kNeg = -3.0e38f;  // finite "minus infinity" for running maxima
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr int kMaxChunk = 4096;
 
-template <typename T, int D, int NT, int TILE, int NSTAGE>
+template <typename T, int D, int NCW, int TILE>
 struct DecodeCfg {
   static constexpr int E = sizeof(T);
-  static constexpr int ROWB = D * E;    // bytes per K or V row
-  static constexpr int EPV = 16 / E;    // elements per 16-byte vector
-  static constexpr int LPR = ROWB / 16; // lanes per row
-  static constexpr int RPI = 32 / LPR;  // rows per warp-wide load
-  static constexpr int NW = NT / 32;
-  static constexpr int RPW = TILE / NW; // rows per warp per tile
-  static constexpr int IPW = RPW / RPI; // warp-wide loads per tile, per operand
+  static constexpr int ROWB = D * E;     // bytes per K or V row
+  static constexpr int EPV = 16 / E;     // elements per 16-byte vector
+  static constexpr int LPR = ROWB / 16;  // lanes per row
+  static constexpr int RPI = 32 / LPR;   // rows per warp-wide load
+  static constexpr int NW = NCW + 1;     // consumer warps + one producer warp
+  static constexpr int NT = NW * 32;
   static constexpr int STAGE = 2 * TILE * ROWB;
   static_assert(LPR >= 1 && LPR <= 32, "row must be 16..512 bytes");
-  static_assert(RPW % RPI == 0 && IPW >= 1, "tile must cover whole warp loads");
-  static_assert(NT >= D, "one thread per output dimension in the merge");
+  static_assert(TILE % RPI == 0, "a stage holds whole row groups");
+  static_assert(NCW * 32 >= D, "one consumer thread per output dimension in the merge");
+  static_assert(TILE <= 64, "per-warp weight buffer holds 64 rows");
 };
+
+constexpr int kMaxStages = 16;
 
 struct __align__(16) Xch {
   float m, l, s_self, pad;
@@ -60,40 +73,63 @@ struct __align__(16) Xch {
   int slot, pad2;
 };
 
-// Shared-memory layout; identical on host and device.
-template <int D, int NW, int STAGE, int NSTAGE>
+// Shared-memory layout (bytes); identical on host and device.  The stage ring
+// depth and the CTA's slot count are launch parameters.
+template <int D, int NCW, int STAGE>
 struct Layout {
-  static constexpr size_t bars = 0;
-  static constexpr size_t xch = 128;
-  static constexpr size_t xo = xch + sizeof(Xch);  // cluster-visible partial o[D]
+  static constexpr size_t full = 0;                            // kMaxStages mbarriers
+  static constexpr size_t empty = 8 * kMaxStages;              // kMaxStages mbarriers
+  static constexpr size_t xch = 16 * kMaxStages;
+  static constexpr size_t xo = xch + sizeof(Xch);              // cluster-visible partial o[D]
   static constexpr size_t red = (xo + D * 4 + 127) / 128 * 128;
-  static constexpr size_t gm = red + NW * (D + 4) * 4;     // per-rank m / l / key / slot copies
-  static constexpr size_t stages = (gm + 16 * 24 + 127) / 128 * 128;
-  static constexpr size_t tail = stages + (size_t)NSTAGE * STAGE;  // then lg, sc, ps [chunk]
-  static size_t bytes(int chunk) { return tail + (size_t)chunk * 12; }
+  static constexpr size_t gm = red + NCW * (D + 4) * 4;        // per-rank m / l / self / key / slot
+  static constexpr size_t blk = gm + 16 * 24;                  // block argmin scratch + counters
+  static constexpr size_t wbuf = (blk + 8 * (NCW + 1) + 32 + 15) / 16 * 16;  // per-warp row weights
+  static constexpr size_t stages = (wbuf + NCW * 64 * 4 + 127) / 128 * 128;
+  __host__ __device__ static size_t tail(int nstage) { return stages + static_cast<size_t>(nstage) * STAGE; }
+  __host__ __device__ static size_t bytes(int nstage, int chunk) {
+    return tail(nstage) + static_cast<size_t>(chunk) * 12;  // logits, scores, positions
+  }
 };
 
-template <typename T, int D, int NT, int TILE, int NSTAGE>
-__global__ void __launch_bounds__(NT) decode_kernel(const DecodeParams prm) {
-  using Cfg = DecodeCfg<T, D, NT, TILE, NSTAGE>;
-  using Lay = Layout<D, Cfg::NW, Cfg::STAGE, NSTAGE>;
-  constexpr int EPV = Cfg::EPV, LPR = Cfg::LPR, RPI = Cfg::RPI, IPW = Cfg::IPW, ROWB = Cfg::ROWB;
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+template <typename T, int D, int NCW, int TILE>
+__global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeParams prm) {
+  using Cfg = DecodeCfg<T, D, NCW, TILE>;
+  using Lay = Layout<D, NCW, Cfg::STAGE>;
+  const int NSTAGE = prm.nstage;
+  constexpr int EPV = Cfg::EPV, LPR = Cfg::LPR, RPI = Cfg::RPI, ROWB = Cfg::ROWB;
+  constexpr int NT = Cfg::NT, NW = Cfg::NW;
   extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::bars);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + Lay::full);
+  uint64_t* empty_bar = reinterpret_cast<uint64_t*>(smem + Lay::empty);
   Xch* xch = reinterpret_cast<Xch*>(smem + Lay::xch);
   float* xo = reinterpret_cast<float*>(smem + Lay::xo);
   float* red = reinterpret_cast<float*>(smem + Lay::red);
   float* g_m = reinterpret_cast<float*>(smem + Lay::gm);
   float* g_l = g_m + 16;
-  float* g_self = g_l + 16;  // [1] (padded to 16)
+  float* g_self = g_l + 16;
   unsigned long long* g_key = reinterpret_cast<unsigned long long*>(g_self + 16);
   int* g_slot = reinterpret_cast<int*>(g_key + 16);
+  unsigned long long* blk_key = reinterpret_cast<unsigned long long*>(smem + Lay::blk);
+  int* blk_int = reinterpret_cast<int*>(blk_key + NW);  // [0] slot, [1..3] p, count, head
+  float* wbuf = reinterpret_cast<float*>(smem + Lay::wbuf);
   unsigned char* stage_base = smem + Lay::stages;
-  float* lg = reinterpret_cast<float*>(smem + Lay::tail);
+  float* lg = reinterpret_cast<float*>(smem + Lay::tail(NSTAGE));
   float* sc = lg + prm.chunk;
   int* ps = reinterpret_cast<int*>(sc + prm.chunk);
-  __shared__ unsigned long long blk_key[Cfg::NW];
-  __shared__ int blk_slot;
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
@@ -101,176 +137,231 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeParams prm) {
   const int pair = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grp = lane / LPR, lig = lane % LPR;
-
-  griddep_wait();  // the previous step on this cache must be complete
-
-  const PairCtr ctr = prm.ctr[pair];
   const int C = prm.C, R = prm.R;
-  const int p = ctr.p, count = ctr.count, head = ctr.head;
-  const bool full = count >= C;
   const int lo = rank * prm.chunk;
-  const int hi = min(lo + prm.chunk, count);
-  const int nrows = max(hi - lo, 0);
-  const int ntiles = (nrows + TILE - 1) / TILE;
   const size_t slot0 = static_cast<size_t>(pair) * C + lo;
-  const unsigned char* gK = static_cast<const unsigned char*>(prm.K) + slot0 * ROWB;
-  const unsigned char* gV = static_cast<const unsigned char*>(prm.V) + slot0 * ROWB;
 
   if (tid == 0) {
-    for (int s = 0; s < NSTAGE; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
     fence_mbar_init();
   }
   __syncthreads();
-  uint64_t policy = 0;
-  if (tid == 0) {
-    policy = policy_evict_first();
-    const int first = ntiles < NSTAGE ? ntiles : NSTAGE;
-    for (int t = 0; t < first; ++t) {
-      const int rows = min(TILE, nrows - t * TILE);
-      const uint32_t bytes = static_cast<uint32_t>(rows * ROWB);
-      unsigned char* st = stage_base + static_cast<size_t>(t) * Cfg::STAGE;
-      mbar_arrive_expect_tx(&bars[t], 2 * bytes);
-      bulk_g2s_stream(st, gK + static_cast<size_t>(t) * TILE * ROWB, bytes, &bars[t], policy);
-      bulk_g2s_stream(st + TILE * ROWB, gV + static_cast<size_t>(t) * TILE * ROWB, bytes, &bars[t], policy);
-    }
-  }
-
-  // q, pre-scaled so that exp2(logit) is the softmax numerator
-  float qv[EPV];
-  {
-    const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(prm.q) +
-                                                    static_cast<size_t>(pair) * ROWB + lig * 16);
-    Vec16<T>::unpack(u, qv);
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) qv[e] *= prm.qscale;
-  }
-  // scores and positions of this CTA's slots (needed after the softmax)
-  for (int j = tid; j < nrows; j += NT) {
-    sc[j] = prm.score[slot0 + j];
-    ps[j] = prm.pos[slot0 + j];
-  }
 
   float m = kNeg, l = 0.f, o[EPV];
 #pragma unroll
   for (int e = 0; e < EPV; ++e) o[e] = 0.f;
   float s_self = 0.f;
-  if (rank == 0 && warp == 0) {
-    // the new token attends to itself: row group 0 of warp 0 starts from it
-    float kf[EPV];
-    const uint4 ku = *reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(prm.k_new) +
-                                                     static_cast<size_t>(pair) * ROWB + lig * 16);
-    Vec16<T>::unpack(ku, kf);
-    float acc = 0.f;
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) acc = fmaf(qv[e], kf[e], acc);
-#pragma unroll
-    for (int off = LPR / 2; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    s_self = acc;
-    if (grp == 0) {
-      const uint4 vu = *reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(prm.v_new) +
-                                                       static_cast<size_t>(pair) * ROWB + lig * 16);
-      Vec16<T>::unpack(vu, o);
-      m = s_self;
-      l = 1.f;
-    }
-  }
+  int p = 0, count = 0, head = 0;
 
-  bool ok = true;
-  for (int t = 0; t < ntiles; ++t) {
-    const int s = t % NSTAGE;
-    if (ok && !mbar_wait_bounded(&bars[s], static_cast<uint32_t>((t / NSTAGE) & 1), kWaitLimit)) {
-      ok = false;
-      atomicOr(prm.err, ERR_MBAR_TIMEOUT);
-    }
-    const unsigned char* sK = stage_base + static_cast<size_t>(s) * Cfg::STAGE;
-    const unsigned char* sV = sK + TILE * ROWB;
-    const int rows = min(TILE, nrows - t * TILE);
-    float lgi[IPW];
-    int rowi[IPW];
-#pragma unroll
-    for (int i = 0; i < IPW; ++i) {
-      const int row = warp * Cfg::RPW + i * RPI + grp;
-      rowi[i] = row;
-      float acc = 0.f;
-      if (ok && row < rows) {
-        float kf[EPV];
-        Vec16<T>::unpack(*reinterpret_cast<const uint4*>(sK + row * ROWB + lig * 16), kf);
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) acc = fmaf(qv[e], kf[e], acc);
+  if (warp == NCW) {
+    // ---------------------------------------------------------- producer warp
+    if (lane == 0) {
+      // The slot store is read before the grid-dependency wait only when the
+      // previous kernel on this stream did not touch this cache.
+      if (!prm.prefetch) griddep_wait();
+      const int cnt = prm.ctr[pair].count;
+      const int nrows = max(min(lo + prm.chunk, cnt) - lo, 0);
+      const int ntiles = (nrows + TILE - 1) / TILE;
+      const unsigned char* gK = static_cast<const unsigned char*>(prm.K) + slot0 * ROWB;
+      const unsigned char* gV = static_cast<const unsigned char*>(prm.V) + slot0 * ROWB;
+      // the whole slot range goes to L2 at once, so HBM streams it while the
+      // ring below (and, before the wait, the previous kernel) catches up
+      if (nrows > 0) {
+        bulk_prefetch_l2(gK, static_cast<uint32_t>(nrows * ROWB));
+        bulk_prefetch_l2(gV, static_cast<uint32_t>(nrows * ROWB));
       }
+      const uint64_t policy = policy_evict_first();
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % NSTAGE, k = t / NSTAGE;
+        if (k > 0 && !mbar_wait_bounded(&empty_bar[s], static_cast<uint32_t>((k - 1) & 1), kWaitLimit)) {
+          atomicOr(prm.err, ERR_MBAR_TIMEOUT);
+          break;
+        }
+        const int rows = min(TILE, nrows - t * TILE);
+        const uint32_t bytes = static_cast<uint32_t>(rows * ROWB);
+        unsigned char* st = stage_base + static_cast<size_t>(s) * Cfg::STAGE;
+        mbar_arrive_expect_tx(&full_bar[s], 2 * bytes);
+        bulk_g2s_stream(st, gK + static_cast<size_t>(t) * TILE * ROWB, bytes, &full_bar[s], policy);
+        bulk_g2s_stream(st + TILE * ROWB, gV + static_cast<size_t>(t) * TILE * ROWB, bytes, &full_bar[s], policy);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------- consumer warps
+    // Cache-owned state (counters, scores, positions) may be read before the
+    // grid-dependency wait under the same rule as the producer's prefetch;
+    // the step's inputs (q, k_new, v_new) only after it.
+    int4 ctr = make_int4(0, 0, 0, 0);
+    int nrows = 0;
+    auto load_state = [&]() {
+      ctr = *reinterpret_cast<const int4*>(prm.ctr + pair);  // {p, count, head, -}
+      nrows = max(min(lo + prm.chunk, ctr.y) - lo, 0);
+      for (int j = tid; j < nrows; j += NCW * 32) {
+        sc[j] = prm.score[slot0 + j];
+        ps[j] = prm.pos[slot0 + j];
+      }
+    };
+    if (prm.prefetch) load_state();
+    griddep_wait();    // every earlier kernel on the stream has completed
+    griddep_launch();  // so the next step may start its own prefetch now
+    if (!prm.prefetch) load_state();
+    p = ctr.x;
+    count = ctr.y;
+    head = ctr.z;
+    const int ntiles = (nrows + TILE - 1) / TILE;
+    if (tid == 0) {
+      blk_int[1] = p;
+      blk_int[2] = count;
+      blk_int[3] = head;
+    }
+    float qv[EPV];
+    Vec16<T>::unpack(*reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(prm.q) +
+                                                     static_cast<size_t>(pair) * ROWB + lig * 16),
+                     qv);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) qv[e] *= prm.qscale;  // exp2(logit) is the softmax numerator
+    if (rank == 0 && warp == 0) {
+      // the new token attends to itself: row group 0 of warp 0 starts from it
+      float kf[EPV];
+      Vec16<T>::unpack(*reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(prm.k_new) +
+                                                       static_cast<size_t>(pair) * ROWB + lig * 16),
+                       kf);
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) acc = fmaf(qv[e], kf[e], acc);
 #pragma unroll
       for (int off = LPR / 2; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      lgi[i] = (ok && row < rows) ? acc : kNeg;
-    }
-    float mt = m;
-#pragma unroll
-    for (int i = 0; i < IPW; ++i) mt = fmaxf(mt, lgi[i]);
-    const float corr = exp2f(m - mt);
-    l *= corr;
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) o[e] *= corr;
-    m = mt;
-#pragma unroll
-    for (int i = 0; i < IPW; ++i) {
-      if (ok && rowi[i] < rows) {
-        const float w = exp2f(lgi[i] - m);
-        l += w;
-        float vf[EPV];
-        Vec16<T>::unpack(*reinterpret_cast<const uint4*>(sV + rowi[i] * ROWB + lig * 16), vf);
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) o[e] = fmaf(w, vf[e], o[e]);
-        if (lig == 0) lg[t * TILE + rowi[i]] = lgi[i];
+      s_self = acc;
+      if (grp == 0) {
+        Vec16<T>::unpack(*reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(prm.v_new) +
+                                                         static_cast<size_t>(pair) * ROWB + lig * 16),
+                         o);
+        m = s_self;
+        l = 1.f;
       }
     }
-    __syncthreads();  // every warp is done with stage s
-    if (tid == 0 && ok && t + NSTAGE < ntiles) {
-      const int tn = t + NSTAGE;
-      const int rn = min(TILE, nrows - tn * TILE);
-      const uint32_t bytes = static_cast<uint32_t>(rn * ROWB);
-      unsigned char* st = stage_base + static_cast<size_t>(s) * Cfg::STAGE;
-      mbar_arrive_expect_tx(&bars[s], 2 * bytes);
-      bulk_g2s_stream(st, gK + static_cast<size_t>(tn) * TILE * ROWB, bytes, &bars[s], policy);
-      bulk_g2s_stream(st + TILE * ROWB, gV + static_cast<size_t>(tn) * TILE * ROWB, bytes, &bars[s], policy);
+    // Each consumer warp takes whole stages in turn (warp w: stages w, w+NCW,
+    // ...).  Within a stage, row group g of the warp (LPR lanes) owns RG rows;
+    // every lane accumulates partial dot products of those rows over its 16
+    // bytes of the row, a butterfly exchange sums them so that lane group
+    // members end up holding whole-row logits (DUP copies of each), and the
+    // probabilities go through shared memory to the lanes that weight V.
+    constexpr int G = RPI;          // row groups per warp
+    constexpr int RG = TILE / G;    // rows per group per stage
+    constexpr int DUP = LPR / RG;   // lanes holding each row's total
+    static_assert(RG >= 1 && RG <= LPR && LPR % RG == 0, "butterfly shape");
+    float* wb = wbuf + warp * TILE;
+    bool ok = true;
+    for (int t = warp; t < ntiles; t += NCW) {
+      const int s = t % NSTAGE;
+      if (ok && !mbar_wait_bounded(&full_bar[s], static_cast<uint32_t>((t / NSTAGE) & 1), kWaitLimit)) {
+        ok = false;
+        atomicOr(prm.err, ERR_MBAR_TIMEOUT);
+      }
+      const unsigned char* sK = stage_base + static_cast<size_t>(s) * Cfg::STAGE;
+      const unsigned char* sV = sK + TILE * ROWB;
+      const int rows = ok ? min(TILE, nrows - t * TILE) : 0;
+      float acc[RG];
+#pragma unroll
+      for (int r = 0; r < RG; ++r) {
+        const int row = grp * RG + r;
+        float kf[EPV];
+        Vec16<T>::unpack(*reinterpret_cast<const uint4*>(sK + row * ROWB + lig * 16), kf);
+        float a = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) a = fmaf(qv[e], kf[e], a);
+        acc[r] = row < rows ? a : 0.f;
+      }
+      // butterfly: halve the rows held per lane at each step
+#pragma unroll
+      for (int off = LPR / 2, n = RG; off >= 1; off >>= 1) {
+        if (n > 1) {
+          const int half = n / 2;
+          const bool hi = (lig & off) != 0;
+#pragma unroll
+          for (int i = 0; i < half; ++i) {
+            const float keep = hi ? acc[half + i] : acc[i];
+            const float send = hi ? acc[i] : acc[half + i];
+            acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+          }
+          n = half;
+        } else {
+          acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], off);
+        }
+      }
+      const int rown = grp * RG + lig / DUP;  // the row whose logit this lane holds
+      const bool valid = rown < rows;
+      const float x = valid ? acc[0] : kNeg;
+      float mx = x;
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float mn = fmaxf(m, mx);
+      const float corr = exp2f(m - mn);
+      m = mn;
+      if (lig % DUP == 0) {
+        wb[rown] = valid ? exp2f(x - mn) : 0.f;
+        if (valid) lg[t * TILE + rown] = x;
+      }
+      __syncwarp();
+      l *= corr;
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) o[e] *= corr;
+#pragma unroll
+      for (int r = 0; r < RG; ++r) {
+        const int row = grp * RG + r;
+        if (row < rows) {
+          const float w = wb[row];
+          l += w;
+          float vf[EPV];
+          Vec16<T>::unpack(*reinterpret_cast<const uint4*>(sV + row * ROWB + lig * 16), vf);
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) o[e] = fmaf(w, vf[e], o[e]);
+        }
+      }
+      __syncwarp();  // wb is rewritten by the next stage
+      if (lane == 0) mbar_arrive(&empty_bar[s]);  // stage s may be refilled
     }
-  }
-  griddep_launch();
 
-  // merge the row groups of this warp (identical result in every lane group)
+    // merge the row groups of this warp (identical result in every group)
 #pragma unroll
-  for (int off = LPR; off < 32; off <<= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-    const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
-    const float M = fmaxf(m, m2);
-    const float a = exp2f(m - M), b = exp2f(m2 - M);
-    l = l * a + l2 * b;
+    for (int off = LPR; off < 32; off <<= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+      const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
+      const float M = fmaxf(m, m2);
+      const float a = exp2f(m - M), b = exp2f(m2 - M);
+      l = l * a + l2 * b;
 #pragma unroll
-    for (int e = 0; e < EPV; ++e) o[e] = o[e] * a + __shfl_xor_sync(0xffffffffu, o[e], off) * b;
-    m = M;
-  }
-  float* myred = red + warp * (D + 4);
-  if (lane == 0) {
-    myred[0] = m;
-    myred[1] = l;
-  }
-  if (grp == 0) {
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) myred[4 + lig * EPV + e] = o[e];
-  }
-  __syncthreads();
-  if (tid < D) {
-    float M = kNeg;
-    for (int w = 0; w < Cfg::NW; ++w) M = fmaxf(M, red[w * (D + 4)]);
-    float Ls = 0.f, Od = 0.f;
-    for (int w = 0; w < Cfg::NW; ++w) {
-      const float a = exp2f(red[w * (D + 4)] - M);
-      Ls = fmaf(red[w * (D + 4) + 1], a, Ls);
-      Od = fmaf(red[w * (D + 4) + 4 + tid], a, Od);
+      for (int e = 0; e < EPV; ++e) o[e] = o[e] * a + __shfl_xor_sync(0xffffffffu, o[e], off) * b;
+      m = M;
     }
-    xo[tid] = Od;
-    if (tid == 0) {
-      xch->m = M;
-      xch->l = Ls;
-      xch->s_self = s_self;
+    float* myred = red + warp * (D + 4);
+    if (lane == 0) {
+      myred[0] = m;
+      myred[1] = l;
+    }
+    if (grp == 0) {
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) myred[4 + lig * EPV + e] = o[e];
+    }
+    consumer_sync(NCW * 32);
+    if (tid < D) {
+      float M = kNeg;
+      for (int w = 0; w < NCW; ++w) M = fmaxf(M, red[w * (D + 4)]);
+      float Ls = 0.f, Od = 0.f;
+      for (int w = 0; w < NCW; ++w) {
+        const float a = exp2f(red[w * (D + 4)] - M);
+        Ls = fmaf(red[w * (D + 4) + 1], a, Ls);
+        Od = fmaf(red[w * (D + 4) + 4 + tid], a, Od);
+      }
+      xo[tid] = Od;
+      if (tid == 0) {
+        xch->m = M;
+        xch->l = Ls;
+        xch->s_self = s_self;
+      }
     }
   }
   cluster.sync();  // (1) every CTA's partial softmax is published
@@ -282,6 +373,11 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeParams prm) {
     if (tid == 0) g_self[0] = rx->s_self;
   }
   __syncthreads();
+  p = blk_int[1];
+  count = blk_int[2];
+  head = blk_int[3];
+  const bool full = count >= C;
+  const int nrows = max(min(lo + prm.chunk, count) - lo, 0);
   float M = kNeg;
   for (int r = 0; r < S; ++r) M = fmaxf(M, g_m[r]);
   float Ls = 0.f;
@@ -318,16 +414,15 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeParams prm) {
     wk = other < wk ? other : wk;
   }
   if (lane == 0) blk_key[warp] = wk;
+  if (tid == 0) blk_int[0] = -1;
   __syncthreads();
   unsigned long long bk = blk_key[0];
-  for (int w = 1; w < Cfg::NW; ++w) bk = blk_key[w] < bk ? blk_key[w] : bk;
-  if (tid == 0) blk_slot = -1;
-  __syncthreads();
-  if (kmin == bk && kmin != ~0ull) blk_slot = smin;  // keys are unique (positions are)
+  for (int w = 1; w < NW; ++w) bk = blk_key[w] < bk ? blk_key[w] : bk;
+  if (kmin == bk && kmin != ~0ull) blk_int[0] = smin;  // keys are unique (positions are)
   __syncthreads();
   if (tid == 0) {
     xch->key = bk;
-    xch->slot = blk_slot;
+    xch->slot = blk_int[0];
   }
   cluster.sync();  // (2) every CTA's candidate is published
 
@@ -350,6 +445,7 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeParams prm) {
   } else {
     u = count;
   }
+  cluster_arrive_release();  // this CTA reads no more remote shared memory
 
   // write back: scores of this CTA's slots, the new token into slot u
   for (int j = tid; j < nrows; j += NT) prm.score[slot0 + j] = (lo + j == u) ? p_self : sc[j];
@@ -364,105 +460,147 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeParams prm) {
     }
     if (tid == 0) {
       prm.pos[us] = p;
-      if (u >= hi) prm.score[us] = p_self;  // fill phase: slot was empty
+      if (u >= lo + nrows) prm.score[us] = p_self;  // fill phase: slot was empty
     }
   }
   if (rank == 0 && tid == 0) {
     if (u >= 0) prm.ring[static_cast<size_t>(pair) * R + head] = u;
-    PairCtr nc;
-    nc.p = p + 1;
-    nc.count = full ? C : count + 1;
-    nc.head = (head + 1) % R;
-    nc.pad = 0;
-    prm.ctr[pair] = nc;
+    *reinterpret_cast<int4*>(prm.ctr + pair) = make_int4(p + 1, full ? C : count + 1, (head + 1) % R, 0);
     if (prm.evicted) prm.evicted[pair] = full ? u : -1;
   }
-  cluster.sync();  // (3) no CTA leaves while its shared memory may be read
+  cluster_wait_acquire();  // (3) peers are done reading this CTA's shared memory
 }
 
-template <typename T, int D, int NT, int TILE, int NSTAGE>
-cudaError_t launch_t(const DecodeParams& prm, int pairs, int splits, cudaStream_t s) {
-  using Cfg = DecodeCfg<T, D, NT, TILE, NSTAGE>;
-  using Lay = Layout<D, Cfg::NW, Cfg::STAGE, NSTAGE>;
-  auto kern = decode_kernel<T, D, NT, TILE, NSTAGE>;
-  const size_t smem = Lay::bytes(prm.chunk);
-  // the limit is set for the largest chunk once, so later launches (also
-  // inside graph capture) make no attribute calls
-  cudaError_t e = kernel_attrs(reinterpret_cast<const void*>(kern), Lay::bytes(kMaxChunk), true);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(splits, pairs, 1);
-  cfg.blockDim = dim3(NT, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = splits;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, prm);
+template <typename T, int D>
+struct Kern {
+  static constexpr int NCW = 4, TILE = 16;
+  using Cfg = DecodeCfg<T, D, NCW, TILE>;
+  using Lay = Layout<D, NCW, Cfg::STAGE>;
+  static constexpr auto fn = decode_kernel<T, D, NCW, TILE>;
+
+  static size_t smem(int nstage, int chunk) { return Lay::bytes(nstage, chunk); }
+
+  static cudaError_t attrs() {
+    // raised once for the largest configuration, so later launches (also
+    // inside stream capture) make no attribute calls
+    size_t most = Lay::bytes(kMaxStages, kMaxChunk);
+    if (most > 227 * 1024) most = 227 * 1024;
+    return kernel_attrs(reinterpret_cast<const void*>(fn), most, true);
+  }
+
+  static cudaError_t launch(const DecodeParams& prm, int pairs, int splits, cudaStream_t s) {
+    cudaError_t e = attrs();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(splits, pairs, 1);
+    cfg.blockDim = dim3(Cfg::NT, 1, 1);
+    cfg.dynamicSmemBytes = smem(prm.nstage, prm.chunk);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, fn, prm);
+  }
+
+  // CTAs that can be resident at once for this shape (0 = cannot launch)
+  static int resident(int splits, int nstage, int chunk, int pairs, int sms) {
+    if (attrs() != cudaSuccess) return 0;
+    const size_t bytes = smem(nstage, chunk);
+    if (bytes > 227 * 1024) return 0;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, Cfg::NT, bytes) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(splits, pairs, 1);
+    cfg.blockDim = dim3(Cfg::NT, 1, 1);
+    cfg.dynamicSmemBytes = bytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess) return 0;
+    const long long by_sm = static_cast<long long>(per_sm) * sms;
+    const long long by_cluster = static_cast<long long>(clusters) * splits;
+    return static_cast<int>(by_sm < by_cluster ? by_sm : by_cluster);
+  }
+};
+
+int chunk_for(int C, int splits) {
+  const int ch = (C + splits - 1) / splits;
+  return (ch + 3) / 4 * 4;
 }
 
-constexpr int kThreads = 128;
-constexpr int kTile = 16;
-constexpr int kStages = 4;
+template <typename F>
+auto dispatch(int dtype, int D, F&& f) -> decltype(f(Kern<__half, 128>{})) {
+  if (dtype == 0 && D == 128) return f(Kern<__half, 128>{});
+  if (dtype == 0 && D == 64) return f(Kern<__half, 64>{});
+  if (dtype == 1 && D == 128) return f(Kern<float, 128>{});
+  return f(Kern<float, 64>{});
+}
 
 }  // namespace
 
 int decode_max_chunk() { return kMaxChunk; }
 
-namespace {
-template <typename T, int D>
-cudaError_t feasible_t(int splits, int chunk, int pairs, int* clusters) {
-  using Cfg = DecodeCfg<T, D, kThreads, kTile, kStages>;
-  using Lay = Layout<D, Cfg::NW, Cfg::STAGE, kStages>;
-  auto kern = decode_kernel<T, D, kThreads, kTile, kStages>;
-  const size_t smem = Lay::bytes(chunk);
-  cudaError_t e = kernel_attrs(reinterpret_cast<const void*>(kern), Lay::bytes(kMaxChunk), true);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(splits, pairs, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = splits;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(clusters, kern, &cfg);
-}
-}  // namespace
+int decode_chunk(int C, int splits) { return chunk_for(C, splits); }
 
-// Number of clusters of `splits` CTAs the device can hold at once (0 = the
-// cluster shape cannot be scheduled).
-int decode_max_active_clusters(int dtype, int D, int splits, int chunk, int pairs) {
-  int n = 0;
-  cudaError_t e = cudaErrorInvalidValue;
-  if (dtype == 0 && D == 128) e = feasible_t<__half, 128>(splits, chunk, pairs, &n);
-  if (dtype == 0 && D == 64) e = feasible_t<__half, 64>(splits, chunk, pairs, &n);
-  if (dtype == 1 && D == 128) e = feasible_t<float, 128>(splits, chunk, pairs, &n);
-  if (dtype == 1 && D == 64) e = feasible_t<float, 64>(splits, chunk, pairs, &n);
-  if (e != cudaSuccess) {
+int decode_max_stages() { return kMaxStages; }
+
+int device_sms() {
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
-  return n;
+  return sms;
+}
+
+int decode_resident(int dtype, int D, int splits, int nstage, int chunk, int pairs) {
+  const int sms = device_sms();
+  const int r = dispatch(dtype, D, [&](auto k) { return decltype(k)::resident(splits, nstage, chunk, pairs, sms); });
+  cudaGetLastError();
+  return r;
+}
+
+// Default launch shape.  Consecutive decode steps of different layers
+// overlap (the next kernel prefetches while this one finishes), so a step
+// should fill about half of the GPU: the largest cluster size whose CTAs fit
+// in half the resident capacity, each CTA keeping at least 32 slots; one CTA
+// per pair when pairs alone exceed that.  Eight 16-row stages per CTA.
+DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C) {
+  DecodeShape sh;
+  sh.stages = 8;
+  sh.splits = 1;
+  for (int s = 16; s >= 2; s /= 2) {
+    const int ch = chunk_for(C, s);
+    if (ch < 32 || ch > kMaxChunk) continue;
+    const int res = decode_resident(dtype, D, s, sh.stages, ch, pairs);
+    if (res > 0 && 2LL * pairs * s <= res) {
+      sh.splits = s;
+      return sh;
+    }
+  }
+  while (sh.splits < 16 && chunk_for(C, sh.splits) > kMaxChunk) sh.splits *= 2;
+  return sh;
 }
 
 cudaError_t launch_decode(const DecodeParams& prm, int dtype, int D, int pairs, int splits, int threads,
                           cudaStream_t s) {
   (void)threads;
-  if (dtype == 0 && D == 128) return launch_t<__half, 128, kThreads, kTile, kStages>(prm, pairs, splits, s);
-  if (dtype == 0 && D == 64) return launch_t<__half, 64, kThreads, kTile, kStages>(prm, pairs, splits, s);
-  if (dtype == 1 && D == 128) return launch_t<float, 128, kThreads, kTile, kStages>(prm, pairs, splits, s);
-  if (dtype == 1 && D == 64) return launch_t<float, 64, kThreads, kTile, kStages>(prm, pairs, splits, s);
-  return cudaErrorInvalidValue;
+  if ((dtype != 0 && dtype != 1) || (D != 64 && D != 128)) return cudaErrorInvalidValue;
+  return dispatch(dtype, D, [&](auto k) { return decltype(k)::launch(prm, pairs, splits, s); });
 }
+
+int decode_threads() { return 160; }
 
 }  // namespace h2o

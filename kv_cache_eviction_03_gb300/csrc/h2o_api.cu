@@ -39,22 +39,36 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t kv_bytes(const h2o_cache* c) { return static_cast<size_t>(c->P) * c->C * c->D * c->elem; }
 
-int chunk_for(int C, int splits) {
-  const int ch = (C + splits - 1) / splits;
-  return (ch + 3) / 4 * 4;
+int chunk_for(int C, int splits) { return h2o::decode_chunk(C, splits); }
+
+// Which cache the last library kernel issued on each stream worked on.  A
+// decode step may read its slot store before the programmatic
+// grid-dependency wait only if the kernel just before it on the stream did not
+// touch the same cache (every library kernel issues its launch-dependents
+// trigger after its own wait, so all earlier kernels are complete by then).
+std::mutex g_stream_mu;
+std::map<const void*, const h2o_cache*> g_last_on_stream;
+
+bool touch_stream(const h2o_cache* c, void* stream) {
+  std::lock_guard<std::mutex> lock(g_stream_mu);
+  auto it = g_last_on_stream.find(stream);
+  const bool other = it == g_last_on_stream.end() || it->second != c;
+  g_last_on_stream[stream] = c;
+  return other;
 }
 
-// CTAs per pair: enough CTAs to give every SM about four, while each CTA keeps
-// at least 32 slots; more when one CTA's slot range would not fit on chip.
-int auto_splits(int pairs, int C, int sms) {
-  const long long target = 4LL * sms;
-  int s = 1;
-  while (s < 16 && static_cast<long long>(pairs) * s < target && chunk_for(C, 2 * s) >= 32) s *= 2;
-  while (s < 16 && chunk_for(C, s) > h2o::decode_max_chunk()) s *= 2;
-  return s;
+void forget_cache(const h2o_cache* c) {
+  std::lock_guard<std::mutex> lock(g_stream_mu);
+  for (auto it = g_last_on_stream.begin(); it != g_last_on_stream.end();)
+    it = it->second == c ? g_last_on_stream.erase(it) : std::next(it);
 }
 
-int splits_in_use(const h2o_cache* c) { return c->splits_override > 0 ? c->splits_override : c->splits_auto; }
+int splits_in_use(const h2o_cache* c) {
+  return c->splits_override > 0 ? c->splits_override : c->shape_auto.splits;
+}
+int stages_in_use(const h2o_cache* c) {
+  return c->stages_override > 0 ? c->stages_override : c->shape_auto.stages;
+}
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
@@ -147,19 +161,15 @@ int h2o_cache_create(int batch, int heads, int head_dim, int heavy_budget, int r
     h2o_cache_destroy(c);
     return cuda_fail(e, "h2o_cache_create: initialisation");
   }
-  // pick the cluster size; fall back to smaller clusters if the device
-  // cannot co-schedule the preferred one
-  c->splits_auto = auto_splits(c->P, c->C, c->num_sms);
-  while (c->splits_auto > 1 &&
-         h2o::decode_max_active_clusters(c->dtype, c->D, c->splits_auto, chunk_for(c->C, c->splits_auto), c->P) < 1 &&
-         chunk_for(c->C, c->splits_auto / 2) <= h2o::decode_max_chunk())
-    c->splits_auto /= 2;
+  // cluster size: the largest that keeps every CTA of the grid resident
+  c->shape_auto = h2o::decode_pick_shape(c->dtype, c->D, c->P, c->C);
   *out = c;
   return H2O_OK;
 }
 
 void h2o_cache_destroy(h2o_cache* c) {
   if (!c) return;
+  forget_cache(c);
   cudaFree(c->K);
   cudaFree(c->V);
   cudaFree(c->score);
@@ -173,6 +183,7 @@ void h2o_cache_destroy(h2o_cache* c) {
 
 int h2o_cache_reset(h2o_cache* c, void* stream) {
   if (!c) return fail(H2O_EINVAL, "h2o_cache_reset: cache is NULL");
+  touch_stream(c, stream);
   cudaError_t e = h2o::launch_reset(c->ctr, c->pos, c->score, c->ring, c->P, c->C, c->recent, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "h2o_cache_reset");
   c->host_next_p = 0;
@@ -213,6 +224,7 @@ int h2o_prefill_ex(h2o_cache* c, const void* q, const void* k, const void* v, in
   pp.L = prompt_len;
   pp.qscale = scale * 1.4426950408889634f;
   cudaStream_t s = as_stream(stream);
+  touch_stream(c, stream);
   if ((e = h2o::launch_prefill_stats(pp, c->dtype, c->D, c->P, s)) != cudaSuccess)
     return cuda_fail(e, "h2o_prefill: row statistics launch");
   if ((e = h2o::launch_prefill_colsum(pp, c->dtype, c->D, c->P, s)) != cudaSuccess)
@@ -270,7 +282,9 @@ int h2o_decode_step(h2o_cache* c, const void* q, const void* k_new, const void* 
   dp.C = c->C;
   dp.R = c->recent;
   dp.chunk = chunk_for(c->C, splits);
+  dp.nstage = stages_in_use(c);
   dp.qscale = scale * 1.4426950408889634f;
+  dp.prefetch = touch_stream(c, stream) ? 1 : 0;
   cudaError_t e = h2o::launch_decode(dp, c->dtype, c->D, c->P, splits, 128, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "h2o_decode_step: launch");
   c->host_next_p += 1;
@@ -340,6 +354,7 @@ int h2o_cache_import_state(h2o_cache* c, const void* host_buf, size_t bytes, voi
     if (ctr[i].p > maxp) maxp = ctr[i].p;
   }
   cudaStream_t s = as_stream(stream);
+  touch_stream(c, stream);
   cudaError_t e;
   struct {
     void* dst;
@@ -375,16 +390,21 @@ int h2o_cache_check(h2o_cache* c, void* stream) {
   return H2O_OK;
 }
 
-int h2o_cache_set_decode_splits(h2o_cache* c, int splits) {
-  if (!c) return fail(H2O_EINVAL, "h2o_cache_set_decode_splits: cache is NULL");
+int h2o_cache_set_decode_shape(h2o_cache* c, int splits, int stages) {
+  if (!c) return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: cache is NULL");
   if (splits != 0 && splits != 1 && splits != 2 && splits != 4 && splits != 8 && splits != 16)
-    return fail(H2O_EINVAL, "h2o_cache_set_decode_splits: splits must be 0, 1, 2, 4, 8 or 16");
-  if (splits > 0 && chunk_for(c->C, splits) > h2o::decode_max_chunk())
-    return fail(H2O_EINVAL, "h2o_cache_set_decode_splits: %d splits leave more than %d slots per CTA", splits,
+    return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: splits must be 0, 1, 2, 4, 8 or 16");
+  if (stages < 0 || stages > h2o::decode_max_stages())
+    return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: stages must be 0..%d", h2o::decode_max_stages());
+  const int s = splits > 0 ? splits : c->shape_auto.splits;
+  const int n = stages > 0 ? stages : c->shape_auto.stages;
+  if (chunk_for(c->C, s) > h2o::decode_max_chunk())
+    return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: %d splits leave more than %d slots per CTA", s,
                 h2o::decode_max_chunk());
-  if (splits > 0 && h2o::decode_max_active_clusters(c->dtype, c->D, splits, chunk_for(c->C, splits), c->P) < 1)
-    return fail(H2O_EINVAL, "h2o_cache_set_decode_splits: clusters of %d CTAs cannot be scheduled", splits);
+  if (h2o::decode_resident(c->dtype, c->D, s, n, chunk_for(c->C, s), c->P) < s)
+    return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: %d CTAs per pair with %d stages cannot be scheduled", s, n);
   c->splits_override = splits;
+  c->stages_override = stages;
   return H2O_OK;
 }
 
@@ -397,7 +417,9 @@ int h2o_cache_info(const h2o_cache* c, int32_t* info) {
   info[4] = c->recent;
   info[5] = c->dtype;
   info[6] = splits_in_use(c);
-  info[7] = 128;
+  info[7] = stages_in_use(c);
+  info[8] = h2o::decode_threads();
+  info[9] = 0;
   return H2O_OK;
 }
 

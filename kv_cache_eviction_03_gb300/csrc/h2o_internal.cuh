@@ -39,6 +39,10 @@ struct DecodeParams {
   int C, R;
   int chunk;          // slots per CTA of a pair's cluster (multiple of 4)
   float qscale;       // scale * log2(e): logits kept in the base-2 domain
+  int nstage;         // depth of the shared-memory stage ring (1..16)
+  int prefetch;       // 1: the previous kernel on the stream did not touch
+                      // this cache, so its slot store may be read before the
+                      // grid-dependency wait
 };
 
 struct PrefillParams {
@@ -78,8 +82,17 @@ cudaError_t kernel_attrs(const void* kern, size_t smem_bytes, bool nonportable_c
 // Launchers (return the launch error; they do not synchronise).
 cudaError_t launch_decode(const DecodeParams& prm, int dtype, int D, int pairs, int splits, int threads,
                           cudaStream_t s);
-int decode_max_active_clusters(int dtype, int D, int splits, int chunk, int pairs);
+struct DecodeShape {
+  int splits;  // CTAs (one cluster) per pair
+  int stages;  // shared-memory ring depth per CTA
+};
+DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C);
+// CTAs of this shape that fit on the device at once (0: cannot launch)
+int decode_resident(int dtype, int D, int splits, int nstage, int chunk, int pairs);
+int decode_chunk(int C, int splits);
+int decode_max_stages();
 int decode_max_chunk();
+int decode_threads();
 
 cudaError_t launch_prefill_stats(const PrefillParams& prm, int dtype, int D, int pairs, cudaStream_t s);
 cudaError_t launch_prefill_colsum(const PrefillParams& prm, int dtype, int D, int pairs, cudaStream_t s);
@@ -105,7 +118,7 @@ struct h2o_cache {
   float* ws;
   size_t ws_len;
   int device, num_sms;
-  int splits_override;
-  int splits_auto;
+  int splits_override, stages_override;
+  h2o::DecodeShape shape_auto;
   long long host_next_p;  // host mirror of the next position (overflow check)
 };

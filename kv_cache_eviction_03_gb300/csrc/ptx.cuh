@@ -71,6 +71,11 @@ __device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+// Bulk prefetch of a global range into L2 (no completion tracking).  src
+// 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -130,15 +135,23 @@ struct Vec16<float> {
 template <>
 struct Vec16<__half> {
   static constexpr int N = 8;
+  __device__ __forceinline__ static float2 pair(uint32_t w) {
+    float2 f;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+        : "=f"(f.x), "=f"(f.y)
+        : "r"(w));
+    return f;
+  }
   __device__ __forceinline__ static void unpack(const uint4& u, float (&f)[8]) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
-      float2 t = __half22float2(h);
-      f[2 * i] = t.x;
-      f[2 * i + 1] = t.y;
-    }
+    const float2 a = pair(u.x), b = pair(u.y), c = pair(u.z), d = pair(u.w);
+    f[0] = a.x;
+    f[1] = a.y;
+    f[2] = b.x;
+    f[3] = b.y;
+    f[4] = c.x;
+    f[5] = c.y;
+    f[6] = d.x;
+    f[7] = d.y;
   }
 };
 

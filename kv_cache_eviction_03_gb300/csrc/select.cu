@@ -71,7 +71,7 @@ __device__ __forceinline__ void copy_rows(const unsigned char* srcK, const unsig
 }
 
 template <int ROWB>
-__global__ void __launch_bounds__(NT) select_kernel(const SelectParams prm) {
+__global__ void __launch_bounds__(NT, 1) select_kernel(const SelectParams prm) {
   __shared__ unsigned hist[256];
   __shared__ Scan scan;
   __shared__ int list_pos[NT];

@@ -60,7 +60,7 @@ def test_null_cache_is_rejected_everywhere():
     assert lib.h2o_cache_export_state(None, None, 0, None) == -1
     assert lib.h2o_cache_import_state(None, None, 0, None) == -1
     assert lib.h2o_cache_check(None, None) == -1
-    assert lib.h2o_cache_set_decode_splits(None, 2) == -1
+    assert lib.h2o_cache_set_decode_shape(None, 2, 0) == -1
     assert lib.h2o_cache_info(None, None) == -1
     assert lib.h2o_cache_state_bytes(None) == 0
     lib.h2o_cache_destroy(None)  # NULL-safe

@@ -41,7 +41,7 @@ def oracle_start(w, seed):
 def run_stepwise(w, seed, check=None, splits=None):
     cache = B.h2o_cache_create(w.batch, w.heads, w.head_dim, w.heavy, w.recent, dtype_code(w))
     if splits:
-        B.h2o_cache_set_decode_splits(cache, splits)
+        B.h2o_cache_set_decode_shape(cache, splits)
     st = oracle_start(w, seed)
     out = torch.empty((w.batch, w.heads, w.head_dim), dtype=torch.float32, device="cuda")
     ev = torch.empty((w.batch, w.heads), dtype=torch.int32, device="cuda")
@@ -68,7 +68,7 @@ def run_free(w, seed, splits=None):
     """Both sides run prefill + every decode step on their own."""
     cache = B.h2o_cache_create(w.batch, w.heads, w.head_dim, w.heavy, w.recent, dtype_code(w))
     if splits:
-        B.h2o_cache_set_decode_splits(cache, splits)
+        B.h2o_cache_set_decode_shape(cache, splits)
     P, D = w.pairs, w.head_dim
     st = oracle_start(w, seed)
     if w.prompt:
@@ -174,7 +174,7 @@ def test_decode_rejects_wrong_shapes_and_devices():
         B._check(B.lib().h2o_decode_step(cache.handle, q.data_ptr(), q.data_ptr(), q.data_ptr(), -1.0,
                                          out.data_ptr(), None, None))
     with pytest.raises(B.H2OError):
-        B.h2o_cache_set_decode_splits(cache, 3)
+        B.h2o_cache_set_decode_shape(cache, 3)
     B.h2o_cache_destroy(cache)
 
 
