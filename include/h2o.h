@@ -133,8 +133,9 @@ H2O_API int h2o_cache_check(h2o_cache* cache, void* stream);
 /* Tuning of the decode kernel's launch shape: `splits` CTAs (one thread-block
  * cluster) share a pair, each streaming its slots through a ring of `stages`
  * 16-row shared-memory stages.  0 = automatic for either value.  splits must
- * be 1, 2, 4, 8 or 16, stages 1..16; H2O_EINVAL if the shape cannot be
- * scheduled on the current device. */
+ * be 1, 2, 4, 8 or 16, stages 4, 8, 12 or 16 (a multiple of the kernel's four
+ * consumer warps); H2O_EINVAL otherwise or if the shape cannot be scheduled
+ * on the current device. */
 H2O_API int h2o_cache_set_decode_shape(h2o_cache* cache, int splits, int stages);
 
 /* info[0..9] = {batch, heads, head_dim, heavy, recent, kv_dtype,

@@ -46,7 +46,10 @@ namespace h2o {
 namespace {
 
 constexpr float kNeg = -3.0e38f;  // finite "minus infinity" for running maxima
-constexpr uint32_t kWaitLimit = 1u << 22;
+// Every wait in this kernel is on work of this same grid (bulk copies it
+// issued, stages its own warps release), so it completes within microseconds;
+// 200k polls of <= 1 us each is a generous bound.
+constexpr uint32_t kWaitLimit = 200000u;
 constexpr int kMaxChunk = 4096;
 
 template <typename T, int D, int NCW, int TILE>
@@ -109,7 +112,12 @@ template <typename T, int D, int NCW, int TILE>
 __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeParams prm) {
   using Cfg = DecodeCfg<T, D, NCW, TILE>;
   using Lay = Layout<D, NCW, Cfg::STAGE>;
+  // Stage s is always consumed by warp s % NCW: with a ring depth that is a
+  // multiple of NCW a warp never waits two phases ahead on a stage another
+  // warp still owns, so mbarrier parity waits cannot alias.  Other depths
+  // are rejected on the host; a kernel given one does no streaming.
   const int NSTAGE = prm.nstage;
+  const bool ring_ok = NSTAGE >= NCW && NSTAGE % NCW == 0 && NSTAGE <= kMaxStages;
   constexpr int EPV = Cfg::EPV, LPR = Cfg::LPR, RPI = Cfg::RPI, ROWB = Cfg::ROWB;
   constexpr int NT = Cfg::NT, NW = Cfg::NW;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -142,7 +150,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
   const size_t slot0 = static_cast<size_t>(pair) * C + lo;
 
   if (tid == 0) {
-    for (int s = 0; s < NSTAGE; ++s) {
+    if (!ring_ok) atomicOr(prm.err, ERR_RING_TIMEOUT);
+    for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
@@ -163,7 +172,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
       // previous kernel on this stream did not touch this cache.
       if (!prm.prefetch) griddep_wait();
       const int cnt = prm.ctr[pair].count;
-      const int nrows = max(min(lo + prm.chunk, cnt) - lo, 0);
+      const int nrows = ring_ok ? max(min(lo + prm.chunk, cnt) - lo, 0) : 0;
       const int ntiles = (nrows + TILE - 1) / TILE;
       const unsigned char* gK = static_cast<const unsigned char*>(prm.K) + slot0 * ROWB;
       const unsigned char* gV = static_cast<const unsigned char*>(prm.V) + slot0 * ROWB;
@@ -174,10 +183,15 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
         bulk_prefetch_l2(gV, static_cast<uint32_t>(nrows * ROWB));
       }
       const uint64_t policy = policy_evict_first();
+      int issued = 0;
       for (int t = 0; t < ntiles; ++t) {
         const int s = t % NSTAGE, k = t / NSTAGE;
+        // stages are only released once the consumers are past the
+        // grid-dependency wait, whose length depends on earlier kernels: wait
+        // for the dependency here too before waiting on a stage
+        if (k == 1 && s == 0 && prm.prefetch) griddep_wait();
         if (k > 0 && !mbar_wait_bounded(&empty_bar[s], static_cast<uint32_t>((k - 1) & 1), kWaitLimit)) {
-          atomicOr(prm.err, ERR_MBAR_TIMEOUT);
+          atomicOr(prm.err, ERR_RING_TIMEOUT);
           break;
         }
         const int rows = min(TILE, nrows - t * TILE);
@@ -186,7 +200,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
         mbar_arrive_expect_tx(&full_bar[s], 2 * bytes);
         bulk_g2s_stream(st, gK + static_cast<size_t>(t) * TILE * ROWB, bytes, &full_bar[s], policy);
         bulk_g2s_stream(st + TILE * ROWB, gV + static_cast<size_t>(t) * TILE * ROWB, bytes, &full_bar[s], policy);
+        issued = t + 1;
       }
+      // no copy may still be landing in shared memory when the CTA exits: the
+      // last phase of every stage used has completed (immediately true once
+      // the consumers have read it)
+      for (int t = max(issued - NSTAGE, 0); t < issued; ++t)
+        if (!mbar_wait_bounded(&full_bar[t % NSTAGE], static_cast<uint32_t>((t / NSTAGE) & 1), kWaitLimit))
+          atomicOr(prm.err, ERR_RING_TIMEOUT);
     }
     __syncwarp();
   } else {
@@ -198,7 +219,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
     int nrows = 0;
     auto load_state = [&]() {
       ctr = *reinterpret_cast<const int4*>(prm.ctr + pair);  // {p, count, head, -}
-      nrows = max(min(lo + prm.chunk, ctr.y) - lo, 0);
+      nrows = ring_ok ? max(min(lo + prm.chunk, ctr.y) - lo, 0) : 0;
       for (int j = tid; j < nrows; j += NCW * 32) {
         sc[j] = prm.score[slot0 + j];
         ps[j] = prm.pos[slot0 + j];
@@ -322,7 +343,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
         }
       }
       __syncwarp();  // wb is rewritten by the next stage
-      if (lane == 0) mbar_arrive(&empty_bar[s]);  // stage s may be refilled
+      // stage s may be refilled; after a timeout the stage is not released,
+      // so no new copy can target memory an unfinished copy still writes
+      if (lane == 0 && ok) mbar_arrive(&empty_bar[s]);
     }
 
     // merge the row groups of this warp (identical result in every group)
@@ -364,10 +387,16 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
       }
     }
   }
-  cluster.sync();  // (1) every CTA's partial softmax is published
+  // A pair handled by one CTA needs no cluster barrier or distributed shared
+  // memory: plain block barriers and local shared memory do.
+  const bool clustered = S > 1;
+  if (clustered)
+    cluster.sync();  // (1) every CTA's partial softmax is published
+  else
+    __syncthreads();
 
   if (tid < S) {
-    const Xch* rx = cluster.map_shared_rank(xch, tid);
+    const Xch* rx = clustered ? cluster.map_shared_rank(xch, tid) : xch;
     g_m[tid] = rx->m;
     g_l[tid] = rx->l;
     if (tid == 0) g_self[0] = rx->s_self;
@@ -387,7 +416,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
 
   if (rank == 0 && tid < D) {
     float acc = 0.f;
-    for (int r = 0; r < S; ++r) acc = fmaf(cluster.map_shared_rank(xo, r)[tid], exp2f(g_m[r] - M), acc);
+    for (int r = 0; r < S; ++r)
+      acc = fmaf((clustered ? cluster.map_shared_rank(xo, r) : xo)[tid], exp2f(g_m[r] - M), acc);
     prm.out[static_cast<size_t>(pair) * D + tid] = acc * inv;
   }
 
@@ -424,12 +454,15 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
     xch->key = bk;
     xch->slot = blk_int[0];
   }
-  cluster.sync();  // (2) every CTA's candidate is published
+  if (clustered)
+    cluster.sync();  // (2) every CTA's candidate is published
+  else
+    __syncthreads();
 
   int u;
   if (full) {
     if (tid < S) {
-      const Xch* rx = cluster.map_shared_rank(xch, tid);
+      const Xch* rx = clustered ? cluster.map_shared_rank(xch, tid) : xch;
       g_key[tid] = rx->key;
       g_slot[tid] = rx->slot;
     }
@@ -445,7 +478,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
   } else {
     u = count;
   }
-  cluster_arrive_release();  // this CTA reads no more remote shared memory
+  if (clustered) cluster_arrive_release();  // this CTA reads no more remote shared memory
 
   // write back: scores of this CTA's slots, the new token into slot u
   for (int j = tid; j < nrows; j += NT) prm.score[slot0 + j] = (lo + j == u) ? p_self : sc[j];
@@ -468,7 +501,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
     *reinterpret_cast<int4*>(prm.ctr + pair) = make_int4(p + 1, full ? C : count + 1, (head + 1) % R, 0);
     if (prm.evicted) prm.evicted[pair] = full ? u : -1;
   }
-  cluster_wait_acquire();  // (3) peers are done reading this CTA's shared memory
+  if (clustered) cluster_wait_acquire();  // (3) peers are done reading this CTA's shared memory
 }
 
 template <typename T, int D>
@@ -497,14 +530,14 @@ struct Kern {
     cfg.dynamicSmemBytes = smem(prm.nstage, prm.chunk);
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = splits;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = splits > 1 ? 2 : 1;  // one CTA per pair: no cluster
     return cudaLaunchKernelEx(&cfg, fn, prm);
   }
 
@@ -554,6 +587,7 @@ int decode_max_chunk() { return kMaxChunk; }
 int decode_chunk(int C, int splits) { return chunk_for(C, splits); }
 
 int decode_max_stages() { return kMaxStages; }
+int decode_stage_multiple() { return Kern<__half, 128>::NCW; }
 
 int device_sms() {
   int sms = 0, dev = 0;

@@ -382,10 +382,11 @@ int h2o_cache_check(h2o_cache* c, void* stream) {
   if (flags) {
     cudaMemset(c->err, 0, sizeof(int));
     cudaDeviceSynchronize();
-    return fail(H2O_EDEVICE, "h2o_cache_check: device check fired (flags 0x%x:%s%s%s)", flags,
+    return fail(H2O_EDEVICE, "h2o_cache_check: device check fired (flags 0x%x:%s%s%s%s)", flags,
                 (flags & h2o::ERR_MBAR_TIMEOUT) ? " copy-wait-timeout" : "",
                 (flags & h2o::ERR_NO_CANDIDATE) ? " no-eviction-candidate" : "",
-                (flags & h2o::ERR_SELECT) ? " prefill-select" : "");
+                (flags & h2o::ERR_SELECT) ? " prefill-select" : "",
+                (flags & h2o::ERR_RING_TIMEOUT) ? " ring-wait-timeout" : "");
   }
   return H2O_OK;
 }
@@ -394,8 +395,9 @@ int h2o_cache_set_decode_shape(h2o_cache* c, int splits, int stages) {
   if (!c) return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: cache is NULL");
   if (splits != 0 && splits != 1 && splits != 2 && splits != 4 && splits != 8 && splits != 16)
     return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: splits must be 0, 1, 2, 4, 8 or 16");
-  if (stages < 0 || stages > h2o::decode_max_stages())
-    return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: stages must be 0..%d", h2o::decode_max_stages());
+  if (stages < 0 || stages > h2o::decode_max_stages() || stages % h2o::decode_stage_multiple() != 0)
+    return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: stages must be a multiple of %d in 0..%d",
+                h2o::decode_stage_multiple(), h2o::decode_max_stages());
   const int s = splits > 0 ? splits : c->shape_auto.splits;
   const int n = stages > 0 ? stages : c->shape_auto.stages;
   if (chunk_for(c->C, s) > h2o::decode_max_chunk())

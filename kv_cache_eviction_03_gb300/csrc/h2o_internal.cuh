@@ -9,9 +9,10 @@ namespace h2o {
 
 // Device error bits latched in h2o_cache::err (reported by h2o_cache_check).
 enum : int {
-  ERR_MBAR_TIMEOUT = 1,  // a bulk-copy barrier wait gave up
+  ERR_MBAR_TIMEOUT = 1,  // a consumer's wait for a filled stage gave up
   ERR_NO_CANDIDATE = 2,  // full cache but no slot outside the recent window
   ERR_SELECT = 4,        // prefill selection did not find `heavy` keys
+  ERR_RING_TIMEOUT = 8,  // the producer's wait for a free stage gave up
 };
 
 // Per-pair counters kept on the device so decode steps can be replayed from
@@ -91,6 +92,7 @@ DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C);
 int decode_resident(int dtype, int D, int splits, int nstage, int chunk, int pairs);
 int decode_chunk(int C, int splits);
 int decode_max_stages();
+int decode_stage_multiple();  // ring depths must be multiples of this
 int decode_max_chunk();
 int decode_threads();
 

@@ -38,10 +38,10 @@ def oracle_start(w, seed):
     return O.empty_cache(w.pairs, w.heavy, w.recent, w.head_dim)
 
 
-def run_stepwise(w, seed, check=None, splits=None):
+def run_stepwise(w, seed, check=None, splits=None, stages=0):
     cache = B.h2o_cache_create(w.batch, w.heads, w.head_dim, w.heavy, w.recent, dtype_code(w))
-    if splits:
-        B.h2o_cache_set_decode_shape(cache, splits)
+    if splits or stages:
+        B.h2o_cache_set_decode_shape(cache, splits or 0, stages)
     st = oracle_start(w, seed)
     out = torch.empty((w.batch, w.heads, w.head_dim), dtype=torch.float32, device="cuda")
     ev = torch.empty((w.batch, w.heads), dtype=torch.int32, device="cuda")
@@ -152,6 +152,26 @@ def test_cluster_splits_agree(splits):
     w = W.Workload("splits", 1, 4, 128, "f16", 280, 40, 150, 151, 1.1)
     rep = run_stepwise(w, 11, check=set(range(0, 40, 3)) | {21, 22}, splits=splits)
     assert rep.pairs > 0
+
+
+@pytest.mark.parametrize("splits,stages", [(1, 4), (1, 12), (1, 16), (2, 4), (4, 16)])
+def test_ring_depths_agree(splits, stages):
+    """Every legal ring depth (a multiple of the four consumer warps) gives
+    the oracle's result, with more tiles than stages so stages are reused."""
+    w = W.Workload("ring", 1, 3, 128, "f16", 600, 12, 300, 200, 1.1)
+    cache_check = set(range(12))
+    rep = run_stepwise(w, 23, check=cache_check, splits=splits, stages=stages)
+    assert rep.pairs == w.pairs * 12
+
+
+def test_ring_depth_must_be_a_multiple_of_four():
+    cache = B.h2o_cache_create(1, 2, 128, 40, 40, B.H2O_F16)
+    for bad in (1, 3, 6, 10, 20):
+        with pytest.raises(B.H2OError):
+            B.h2o_cache_set_decode_shape(cache, 1, bad)
+    B.h2o_cache_set_decode_shape(cache, 1, 12)
+    assert B.h2o_cache_info(cache)[6:8] == [1, 12]
+    B.h2o_cache_destroy(cache)
 
 
 @pytest.mark.parametrize("splits", [1, 4, 16])
