@@ -187,17 +187,26 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+DECODE_SOURCES = ("decode.cu", "ptx.cuh", "h2o_internal.cuh")
+
+
+def decode_source_digest():
+    """sha256 over the sources the decode kernel is compiled from."""
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "kv_cache_eviction_03_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def decode_traffic_record():
     """DRAM bytes per decode launch from the committed ncu summary, if the
-    kernel source has not changed since it was captured."""
+    kernel's sources have not changed since it was captured."""
     path = os.path.join(ROOT, "profiles", "decode_traffic.json")
-    src = os.path.join(ROOT, "kv_cache_eviction_03_gb300", "csrc", "decode.cu")
     try:
         with open(path) as f:
             rec = json.load(f)
-        with open(src, "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()
-        if rec.get("decode_cu_sha256") == digest and rec.get("workload") == WORKLOAD:
+        if rec.get("decode_sources_sha256") == decode_source_digest() and rec.get("workload") == WORKLOAD:
             return rec.get("dram_bytes_per_launch")
     except (OSError, ValueError):
         pass

@@ -16,8 +16,7 @@
 //
 // Inside a CTA one producer warp streams the CTA's K and V rows, 16 rows per
 // stage, through a ring of shared-memory stages with 1-D bulk async copies
-// (cp.async.bulk, full/empty mbarriers, L2 evict-first), after one bulk L2
-// prefetch of the CTA's whole K and V range; four consumer warps
+// (cp.async.bulk, full/empty mbarriers, L2 evict-first); four consumer warps
 // compute the logits and a base-2 online softmax (m, l, o) per row group and
 // release each stage with an mbarrier arrive, so the streaming loop has no
 // block-wide barrier.  When the previous kernel on the stream worked on a
@@ -176,12 +175,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
       const int ntiles = (nrows + TILE - 1) / TILE;
       const unsigned char* gK = static_cast<const unsigned char*>(prm.K) + slot0 * ROWB;
       const unsigned char* gV = static_cast<const unsigned char*>(prm.V) + slot0 * ROWB;
-      // the whole slot range goes to L2 at once, so HBM streams it while the
-      // ring below (and, before the wait, the previous kernel) catches up
-      if (nrows > 0) {
-        bulk_prefetch_l2(gK, static_cast<uint32_t>(nrows * ROWB));
-        bulk_prefetch_l2(gV, static_cast<uint32_t>(nrows * ROWB));
-      }
       const uint64_t policy = policy_evict_first();
       int issued = 0;
       for (int t = 0; t < ntiles; ++t) {
@@ -607,24 +600,38 @@ int decode_resident(int dtype, int D, int splits, int nstage, int chunk, int pai
 }
 
 // Default launch shape.  Consecutive decode steps of different layers
-// overlap (the next kernel prefetches while this one finishes), so a step
-// should fill about half of the GPU: the largest cluster size whose CTAs fit
-// in half the resident capacity, each CTA keeping at least 32 slots; one CTA
-// per pair when pairs alone exceed that.  Eight 16-row stages per CTA.
+// overlap: the next kernel's CTAs start filling their rings while this one
+// finishes, so one step should take about 1.7 CTAs per SM (the largest
+// cluster size whose grid stays within that, each CTA keeping at least 32
+// slots), with a 12-stage ring (three stages in flight per consumer warp)
+// when two such CTAs fit on an SM.  Grids that need several waves anyway
+// (many pairs) use 4-stage rings so that more CTAs are resident.
 DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C) {
+  const int sms = device_sms();
+  const long long target = sms > 0 ? (17LL * sms) / 10 : 256;
   DecodeShape sh;
-  sh.stages = 8;
   sh.splits = 1;
   for (int s = 16; s >= 2; s /= 2) {
     const int ch = chunk_for(C, s);
     if (ch < 32 || ch > kMaxChunk) continue;
-    const int res = decode_resident(dtype, D, s, sh.stages, ch, pairs);
-    if (res > 0 && 2LL * pairs * s <= res) {
+    if (static_cast<long long>(pairs) * s <= target) {
       sh.splits = s;
-      return sh;
+      break;
     }
   }
   while (sh.splits < 16 && chunk_for(C, sh.splits) > kMaxChunk) sh.splits *= 2;
+  const long long ctas = static_cast<long long>(pairs) * sh.splits;
+  sh.stages = 4;
+  if (ctas <= 2LL * sms) {
+    const int ch = chunk_for(C, sh.splits);
+    for (int st : {12, 8}) {
+      const int res = decode_resident(dtype, D, sh.splits, st, ch, pairs);
+      if (res >= 2 * sms || static_cast<long long>(res) >= ctas) {
+        sh.stages = st;
+        break;
+      }
+    }
+  }
   return sh;
 }
 
