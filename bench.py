@@ -34,6 +34,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 
 from kv_cache_eviction_03_gb300 import accounting as A  # noqa: E402
+from kv_cache_eviction_03_gb300 import sharding  # noqa: E402
 from kv_cache_eviction_03_gb300 import workload as W  # noqa: E402
 
 METRIC = "H2O decode tokens/s per attention layer; achieved HBM GB/s vs GB300 peak"
@@ -296,10 +297,7 @@ def run_ours(args, rank, world, local_rank):
     elapsed = t_begin.elapsed_time(t_end) / 1e3
     decode_s = sum(mid[i].elapsed_time(ends[i]) for i in range(args.steps)) / 1e3
     prefill_s = sum(starts[i].elapsed_time(mid[i]) for i in range(args.steps)) / 1e3
-    if dist:
-        t = torch.tensor([elapsed, decode_s, prefill_s], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed, decode_s, prefill_s = t.tolist()
+    elapsed, decode_s, prefill_s = sharding.max_over_ranks([elapsed, decode_s, prefill_s], dist, device="cuda")
     for c in caches:
         B.h2o_cache_check(c, stream=stream)
 
@@ -386,10 +384,7 @@ def run_e2e(args, w, NL, inp, caches, stream, pout, dout, dev_ev, g_pre, g_dec, 
     b.record(stream)
     torch.cuda.synchronize()
     el = a.elapsed_time(b) / 1e3
-    if dist:
-        t = torch.tensor([el], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        el = t.item()
+    el = sharding.max_over_ranks([el], dist, device="cuda")[0]
     return {"value": w.batch * w.decode * world * NL * args.steps / el, "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
