@@ -86,7 +86,7 @@ struct Layout {
   static constexpr size_t red = (xo + D * 4 + 127) / 128 * 128;
   static constexpr size_t gm = red + NCW * (D + 4) * 4;        // per-rank m / l / self / key / slot
   static constexpr size_t blk = gm + 16 * 24;                  // block argmin scratch + counters
-  static constexpr size_t wbuf = (blk + 8 * (NCW + 1) + 32 + 15) / 16 * 16;  // per-warp row weights
+  static constexpr size_t wbuf = (blk + 12 * (NCW + 1) + 16 + 15) / 16 * 16;  // per-warp row weights
   static constexpr size_t stages = (wbuf + NCW * 64 * 4 + 127) / 128 * 128;
   __host__ __device__ static size_t tail(int nstage) { return stages + static_cast<size_t>(nstage) * STAGE; }
   __host__ __device__ static size_t bytes(int nstage, int chunk) {
@@ -131,7 +131,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
   unsigned long long* g_key = reinterpret_cast<unsigned long long*>(g_self + 16);
   int* g_slot = reinterpret_cast<int*>(g_key + 16);
   unsigned long long* blk_key = reinterpret_cast<unsigned long long*>(smem + Lay::blk);
-  int* blk_int = reinterpret_cast<int*>(blk_key + NW);  // [0] slot, [1..3] p, count, head
+  int* blk_slot = reinterpret_cast<int*>(blk_key + NW);  // per-warp candidate slot
+  int* blk_int = blk_slot + NW;                           // [1..3] p, count, head
   float* wbuf = reinterpret_cast<float*>(smem + Lay::wbuf);
   unsigned char* stage_base = smem + Lay::stages;
   float* lg = reinterpret_cast<float*>(smem + Lay::tail(NSTAGE));
@@ -220,7 +221,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
     };
     if (prm.prefetch) load_state();
     griddep_wait();    // every earlier kernel on the stream has completed
-    griddep_launch();  // so the next step may start its own prefetch now
     if (!prm.prefetch) load_state();
     p = ctr.x;
     count = ctr.y;
@@ -268,6 +268,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
     constexpr int DUP = LPR / RG;   // lanes holding each row's total
     static_assert(RG >= 1 && RG <= LPR && LPR % RG == 0, "butterfly shape");
     float* wb = wbuf + warp * TILE;
+    // Every earlier kernel has completed, so the next step may start its own
+    // prefetch now; triggering only after this step's inputs are loaded keeps
+    // those small loads ahead of the next step's bulk traffic.
+    griddep_launch();
     bool ok = true;
     for (int t = warp; t < ntiles; t += NCW) {
       const int s = t % NSTAGE;
@@ -430,47 +434,57 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
       }
     }
   }
+  // warp minimum, and the slot of the lane that holds it (keys are unique:
+  // positions are)
   unsigned long long wk = kmin;
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) {
     const unsigned long long other = __shfl_xor_sync(0xffffffffu, wk, off);
     wk = other < wk ? other : wk;
   }
-  if (lane == 0) blk_key[warp] = wk;
-  if (tid == 0) blk_int[0] = -1;
-  __syncthreads();
-  unsigned long long bk = blk_key[0];
-  for (int w = 1; w < NW; ++w) bk = blk_key[w] < bk ? blk_key[w] : bk;
-  if (kmin == bk && kmin != ~0ull) blk_int[0] = smin;  // keys are unique (positions are)
-  __syncthreads();
-  if (tid == 0) {
-    xch->key = bk;
-    xch->slot = blk_int[0];
+  const unsigned holder = __ballot_sync(0xffffffffu, kmin == wk && kmin != ~0ull);
+  const int wslot = __shfl_sync(0xffffffffu, smin, holder ? __ffs(holder) - 1 : 0);
+  if (lane == 0) {
+    blk_key[warp] = wk;
+    blk_slot[warp] = holder ? wslot : -1;
   }
-  if (clustered)
-    cluster.sync();  // (2) every CTA's candidate is published
-  else
-    __syncthreads();
+  __syncthreads();
+  unsigned long long bk = ~0ull;
+  int bslot = -1;
+  for (int w = 0; w < NW; ++w)
+    if (blk_key[w] < bk) {
+      bk = blk_key[w];
+      bslot = blk_slot[w];
+    }
 
   int u;
-  if (full) {
-    if (tid < S) {
-      const Xch* rx = clustered ? cluster.map_shared_rank(xch, tid) : xch;
-      g_key[tid] = rx->key;
-      g_slot[tid] = rx->slot;
+  if (clustered) {
+    if (tid == 0) {
+      xch->key = bk;
+      xch->slot = bslot;
     }
-    __syncthreads();
-    unsigned long long best = ~0ull;
-    u = -1;
-    for (int r = 0; r < S; ++r)
-      if (g_key[r] < best) {
-        best = g_key[r];
-        u = g_slot[r];
+    cluster.sync();  // (2) every CTA's candidate is published
+    if (full) {
+      if (tid < S) {
+        const Xch* rx = cluster.map_shared_rank(xch, tid);
+        g_key[tid] = rx->key;
+        g_slot[tid] = rx->slot;
       }
-    if (u < 0 && tid == 0) atomicOr(prm.err, ERR_NO_CANDIDATE);
+      __syncthreads();
+      unsigned long long best = ~0ull;
+      u = -1;
+      for (int r = 0; r < S; ++r)
+        if (g_key[r] < best) {
+          best = g_key[r];
+          u = g_slot[r];
+        }
+    } else {
+      u = count;
+    }
   } else {
-    u = count;
+    u = full ? bslot : count;
   }
+  if (full && u < 0 && tid == 0) atomicOr(prm.err, ERR_NO_CANDIDATE);
   if (clustered) cluster_arrive_release();  // this CTA reads no more remote shared memory
 
   // write back: scores of this CTA's slots, the new token into slot u
