@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libh2o_gb300.so")
-SOURCES = ["h2o_api.cu", "decode.cu", "prefill.cu", "select.cu", "noalloc.cu"]
+SOURCES = ["h2o_api.cu", "decode.cu", "prefill.cu", "select.cu", "noalloc.cu", "prefill_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]

@@ -223,6 +223,7 @@ int h2o_prefill_ex(h2o_cache* c, const void* q, const void* k, const void* v, in
   pp.colsum = colsum_or_null ? colsum_or_null : c->ws + plen;
   pp.L = prompt_len;
   pp.qscale = scale * 1.4426950408889634f;
+  pp.err = c->err;
   cudaStream_t s = as_stream(stream);
   touch_stream(c, stream);
   if ((e = h2o::launch_prefill_stats(pp, c->dtype, c->D, c->P, s)) != cudaSuccess)
@@ -382,11 +383,12 @@ int h2o_cache_check(h2o_cache* c, void* stream) {
   if (flags) {
     cudaMemset(c->err, 0, sizeof(int));
     cudaDeviceSynchronize();
-    return fail(H2O_EDEVICE, "h2o_cache_check: device check fired (flags 0x%x:%s%s%s%s)", flags,
+    return fail(H2O_EDEVICE, "h2o_cache_check: device check fired (flags 0x%x:%s%s%s%s%s)", flags,
                 (flags & h2o::ERR_MBAR_TIMEOUT) ? " copy-wait-timeout" : "",
                 (flags & h2o::ERR_NO_CANDIDATE) ? " no-eviction-candidate" : "",
                 (flags & h2o::ERR_SELECT) ? " prefill-select" : "",
-                (flags & h2o::ERR_RING_TIMEOUT) ? " ring-wait-timeout" : "");
+                (flags & h2o::ERR_RING_TIMEOUT) ? " ring-wait-timeout" : "",
+                (flags & h2o::ERR_MMA_TIMEOUT) ? " tensor-core-wait-timeout" : "");
   }
   return H2O_OK;
 }

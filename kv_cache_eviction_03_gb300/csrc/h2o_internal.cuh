@@ -13,6 +13,7 @@ enum : int {
   ERR_NO_CANDIDATE = 2,  // full cache but no slot outside the recent window
   ERR_SELECT = 4,        // prefill selection did not find `heavy` keys
   ERR_RING_TIMEOUT = 8,  // the producer's wait for a free stage gave up
+  ERR_MMA_TIMEOUT = 16,  // a prefill wait for tensor-core results gave up
 };
 
 // Per-pair counters kept on the device so decode steps can be replayed from
@@ -55,6 +56,7 @@ struct PrefillParams {
   float* colsum;  // [P, L]
   int L;
   float qscale;   // scale * log2(e)
+  int* err = nullptr;  // device error bits, or nullptr
 };
 
 struct SelectParams {
@@ -98,6 +100,9 @@ int decode_threads();
 
 cudaError_t launch_prefill_stats(const PrefillParams& prm, int dtype, int D, int pairs, cudaStream_t s);
 cudaError_t launch_prefill_colsum(const PrefillParams& prm, int dtype, int D, int pairs, cudaStream_t s);
+// fp16 passes on tcgen05 (row statistics without the attention output)
+cudaError_t launch_prefill_stats_tc(const PrefillParams& prm, int D, int pairs, cudaStream_t s);
+cudaError_t launch_prefill_colsum_tc(const PrefillParams& prm, int D, int pairs, cudaStream_t s);
 cudaError_t launch_prefill_select(const SelectParams& prm, int dtype, int D, int pairs, cudaStream_t s);
 cudaError_t launch_reset(PairCtr* ctr, int* pos, float* score, int* ring, int pairs, int C, int R,
                          cudaStream_t s);

@@ -146,9 +146,10 @@ def test_small_shapes_every_step(case):
 
 
 @pytest.mark.parametrize("splits", [1, 2, 4, 8, 16])
-def test_cluster_splits_agree(splits):
-    """Every cluster size gives the oracle's result, including ragged last CTAs
-    (301 slots) and CTAs whose slot range is still empty while filling."""
+def test_splits_agree(splits):
+    """Every cluster size (CTAs per pair) gives the oracle's result, including
+    ragged last CTAs (301 slots) and CTAs whose slot range is still empty
+    while filling."""
     w = W.Workload("splits", 1, 4, 128, "f16", 280, 40, 150, 151, 1.1)
     rep = run_stepwise(w, 11, check=set(range(0, 40, 3)) | {21, 22}, splits=splits)
     assert rep.pairs > 0

@@ -81,7 +81,13 @@ CASES = [
     ("f32-d64-L300", 1, 2, 64, "f32", 300, 30, 30),
     ("f32-d128-L97", 2, 1, 128, "f32", 97, 11, 9),
     ("f16-large-heavy", 1, 1, 128, "f16", 1500, 700, 100),
+    # 128-row tensor-core blocks: exact multiples, one past, several + ragged tail
+    ("f16-d128-L128", 1, 2, 128, "f16", 128, 20, 20),
+    ("f16-d64-L129", 1, 2, 64, "f16", 129, 20, 20),
+    ("f16-d128-L256", 1, 1, 128, "f16", 256, 40, 40),
+    ("f16-d128-L643", 2, 2, 128, "f16", 643, 60, 50),
 ]
+F16_CASES = [c for c in CASES if c[4] == "f16"]
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
@@ -89,6 +95,14 @@ def test_prefill_parity(case):
     name, b, h, d, dt, L, hv, rc = case
     w = W.Workload(name, b, h, d, dt, L, 0, hv, rc, 1.1)
     check_prefill(w, 13)
+
+
+@pytest.mark.parametrize("case", F16_CASES, ids=[c[0] for c in F16_CASES])
+def test_prefill_parity_lse_only(case):
+    """Without the attention output the fp16 row pass runs on tcgen05."""
+    name, b, h, d, dt, L, hv, rc = case
+    w = W.Workload(name, b, h, d, dt, L, 0, hv, rc, 1.1)
+    check_prefill(w, 29, with_out=False)
 
 
 def test_prefill_without_output():
