@@ -441,8 +441,7 @@ cudaError_t launch_pdl(K kern, dim3 grid, dim3 block, size_t smem, cudaStream_t 
 }  // namespace
 
 // fp16 prefill engine: the tcgen05 kernels unless H2O_PREFILL_ENGINE=mma
-// selects the mma.sync ones (kept for comparison).  The attention output O
-// is only produced by the mma.sync row pass.
+// selects the mma.sync ones (kept for comparison).
 bool prefill_use_tc() {
   static const bool tc = [] {
     const char* v = std::getenv("H2O_PREFILL_ENGINE");
@@ -453,7 +452,7 @@ bool prefill_use_tc() {
 
 cudaError_t launch_prefill_stats(const PrefillParams& prm, int dtype, int D, int pairs, cudaStream_t s) {
   if (prm.L <= 0) return cudaSuccess;
-  if (dtype == 0 && prm.out == nullptr && prefill_use_tc()) return launch_prefill_stats_tc(prm, D, pairs, s);
+  if (dtype == 0 && prefill_use_tc()) return launch_prefill_stats_tc(prm, D, pairs, s);
   if (dtype == 0) {
     const dim3 grid((prm.L + BM - 1) / BM, pairs);
     const bool wo = prm.out != nullptr;

@@ -64,10 +64,12 @@ __device__ __forceinline__ void load_tile(unsigned char* tile, const __half* src
   }
 }
 
-// Entry row0 + t of a length-L vector (0 beyond the end); a plain load, since
-// the vector's rows need not be 16-byte aligned.
-__device__ __forceinline__ float vec_at(const float* src, int row0, int t, int L) {
-  return row0 + t < L ? src[row0 + t] : 0.f;
+// Log2-domain lse of query row row0 + t; rows past the prompt get a huge
+// value so that their probabilities exp2(s - lse) vanish without a mask.  A
+// plain load: the rows of the vector need not be 16-byte aligned.
+constexpr float kHugeLse = 3.0e38f;
+__device__ __forceinline__ float lse_at(const float* src, int row0, int t, int L) {
+  return row0 + t < L ? src[row0 + t] : kHugeLse;
 }
 
 // D[tmem] = A[128 x D] * B[128 x D]^T over the head dimension.
@@ -90,7 +92,7 @@ __device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(NT, 1) colsum_tc(const PrefillParams prm) {
+__global__ void __launch_bounds__(NT, 2) colsum_tc(const PrefillParams prm) {
   using Cfg = TcCfg<D>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = align1024(smem_raw);
@@ -119,8 +121,8 @@ __global__ void __launch_bounds__(NT, 1) colsum_tc(const PrefillParams prm) {
   load_tile<D>(sQ0, Q, kb * BLK, L, tid);
   if (n > 1) load_tile<D>(sQ0 + Cfg::TILE, Q, (kb + 1) * BLK, L, tid);
   if (tid < BLK) {
-    sL[tid] = vec_at(lse2, kb * BLK, tid, L);
-    sL[BLK + tid] = vec_at(lse2, (kb + 1) * BLK, tid, L);
+    sL[tid] = lse_at(lse2, kb * BLK, tid, L);
+    sL[BLK + tid] = lse_at(lse2, (kb + 1) * BLK, tid, L);
   }
   cp_async_commit();
   cp_async_wait<0>();
@@ -153,27 +155,46 @@ __global__ void __launch_bounds__(NT, 1) colsum_tc(const PrefillParams prm) {
     tc::fence_after_sync();
     // the tensor core is done with stage b: bring in query block i + 2
     // (its lse row is loaded now and stored after the exponentials)
-    float next_lse = 0.f;
+    float next_lse = kHugeLse;
     if (i + 2 < n) {
       load_tile<D>(sQ0 + b * Cfg::TILE, Q, (qb + 2) * BLK, L, tid);
-      if (tid < BLK) next_lse = vec_at(lse2, (qb + 2) * BLK, tid, L);
+      if (tid < BLK) next_lse = lse_at(lse2, (qb + 2) * BLK, tid, L);
     }
     cp_async_commit();
-    float acc = 0.f;
+    float acc0 = 0.f, acc1 = 0.f;
     const float* lse = sL + (i % 3) * BLK;
     if (ok) {
+      const int kl = quarter * 32 + lane;  // key within the block
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         float v[32];
         const int col0 = half * 64 + c * 32;
         tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + col0), v);
+        const float4* l4 = reinterpret_cast<const float4*>(lse + col0);
+        if (i == 0) {  // diagonal block: query col0 + e sees key kl only if kl <= col0 + e
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int q = qb * BLK + col0 + e;
-          acc += (key <= q && q < L) ? exp2f(fmaf(v[e], prm.qscale, -lse[col0 + e])) : 0.f;
+          for (int j = 0; j < 8; ++j) {
+            const float4 t = l4[j];
+            const int e = 4 * j;
+            acc0 += kl <= col0 + e ? ex2(fmaf(v[e], prm.qscale, -t.x)) : 0.f;
+            acc1 += kl <= col0 + e + 1 ? ex2(fmaf(v[e + 1], prm.qscale, -t.y)) : 0.f;
+            acc0 += kl <= col0 + e + 2 ? ex2(fmaf(v[e + 2], prm.qscale, -t.z)) : 0.f;
+            acc1 += kl <= col0 + e + 3 ? ex2(fmaf(v[e + 3], prm.qscale, -t.w)) : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 t = l4[j];
+            const int e = 4 * j;
+            acc0 += ex2(fmaf(v[e], prm.qscale, -t.x));
+            acc1 += ex2(fmaf(v[e + 1], prm.qscale, -t.y));
+            acc0 += ex2(fmaf(v[e + 2], prm.qscale, -t.z));
+            acc1 += ex2(fmaf(v[e + 3], prm.qscale, -t.w));
+          }
         }
       }
     }
+    const float acc = acc0 + acc1;
     dacc += static_cast<double>(acc);
     if (i + 2 < n && tid < BLK) sL[((i + 2) % 3) * BLK + tid] = next_lse;
     tc::fence_before_sync();
@@ -204,7 +225,7 @@ __global__ void __launch_bounds__(NT, 1) colsum_tc(const PrefillParams prm) {
 
 // ------------------------------------------------------- row log-sum-exp only
 template <int D>
-__global__ void __launch_bounds__(NT, 1) stats_tc(const PrefillParams prm) {
+__global__ void __launch_bounds__(NT, 2) stats_tc(const PrefillParams prm) {
   using Cfg = TcCfg<D>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = align1024(smem_raw);
@@ -263,25 +284,31 @@ __global__ void __launch_bounds__(NT, 1) stats_tc(const PrefillParams prm) {
     if (i + 2 < n) load_tile<D>(sK0 + b * Cfg::TILE, K, (i + 2) * BLK, L, tid);
     cp_async_commit();
     if (ok) {
+      float v[64];
+      tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + half * 64), *reinterpret_cast<float(*)[32]>(v));
+      tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + half * 64 + 32),
+                    *reinterpret_cast<float(*)[32]>(v + 32));
+      if (i == qb) {  // diagonal block: key half * 64 + e is visible to row rl if it is <= rl
+        const int rl = quarter * 32 + lane;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float v[32];
-        const int col0 = half * 64 + c * 32;
-        tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + col0), v);
-        float cm = kNeg;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int key = i * BLK + col0 + e;
-          v[e] = (key <= row && key < L) ? v[e] * prm.qscale : -INFINITY;
-          cm = fmaxf(cm, v[e]);
-        }
-        const float mn = fmaxf(m, cm);
-        float s = 0.f;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) s += exp2f(v[e] - mn);
-        l = l * exp2f(m - mn) + s;
-        m = mn;
+        for (int e = 0; e < 64; ++e) v[e] = half * 64 + e <= rl ? v[e] : -INFINITY;
       }
+      // the max of the raw logits (scale > 0 commutes with max)
+      float c0 = v[0], c1 = v[1];
+#pragma unroll
+      for (int e = 2; e < 64; e += 2) {
+        c0 = fmaxf(c0, v[e]);
+        c1 = fmaxf(c1, v[e + 1]);
+      }
+      const float mn = fmaxf(m, fmaxf(c0, c1) * prm.qscale);
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int e = 0; e < 64; e += 2) {
+        s0 += ex2(fmaf(v[e], prm.qscale, -mn));
+        s1 += ex2(fmaf(v[e + 1], prm.qscale, -mn));
+      }
+      l = l * ex2(m - mn) + (s0 + s1);
+      m = mn;
     }
     tc::fence_before_sync();
     cp_async_wait<0>();
@@ -307,10 +334,180 @@ __global__ void __launch_bounds__(NT, 1) stats_tc(const PrefillParams prm) {
   if (half == 0 && row < L) {
     const float m2 = red[2 * (quarter * 32 + lane)], l2 = red[2 * (quarter * 32 + lane) + 1];
     const float M = fmaxf(m, m2);
-    prm.lse2[static_cast<size_t>(pair) * L + row] = M + log2f(l * exp2f(m - M) + l2 * exp2f(m2 - M));
+    prm.lse2[static_cast<size_t>(pair) * L + row] = M + log2f(l * ex2(m - M) + l2 * ex2(m2 - M));
   }
   __syncwarp();
   if (warp == 0) tc::tmem_free(tbase, kTmemCols);
+}
+
+// ------------------------------------------------------- attention output O
+// With every row's lse known, O_i = sum_j exp2(s_ij - lse_i) v_j needs no
+// online rescaling: per key block, S = Q K^T goes to TMEM, the threads turn
+// it into fp16 probabilities in a K-major shared tile, and O += P V
+// accumulates in TMEM across all key blocks (V as stored, [key][d], is the
+// MN-major B operand: same swizzled byte layout as load_tile gives).
+template <int D>
+struct OutCfg {
+  static constexpr int TILE = BLK * D * 2;
+  static constexpr int PT = BLK * BLK * 2;  // fp16 probabilities of one block
+  static constexpr size_t k = TILE;                              // 2 key stages
+  static constexpr size_t v = 3 * static_cast<size_t>(TILE);     // 2 value stages
+  static constexpr size_t p = 5 * static_cast<size_t>(TILE);     // 2 probability tiles
+  static constexpr size_t bars = p + 2 * static_cast<size_t>(PT);  // S[2], O, drain
+  static constexpr size_t tslot = bars + 32;
+  static constexpr size_t bytes = tslot + 16 + 1024;
+};
+constexpr uint32_t kOutTmemCols = 512;  // two 128-column logit blocks + O (D <= 128 columns)
+
+// D[tmem] (+)= P[128 x 128 keys] * V[128 keys x D].
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, const unsigned char* p, const unsigned char* v, bool acc) {
+  constexpr uint32_t idesc = tc::idesc_f16_f32_bmn(BLK, D);
+  const uint32_t sp = smem_u32(p), sv = smem_u32(v);
+#pragma unroll
+  for (int ks = 0; ks < BLK / 16; ++ks) {
+    const uint32_t aoff = static_cast<uint32_t>((ks >> 2) * (BLK * 128) + (ks & 3) * 32);
+    tc::mma_f16(d_tmem, tc::desc_k_sw128(sp + aoff), tc::desc_mn_sw128(sv + ks * 2048u, BLK * 128), idesc,
+                acc || ks > 0);
+  }
+}
+
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int lane, int* err) {
+  const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, kWaitLimit));
+  if (!ok && lane == 0 && err) atomicOr(err, ERR_MMA_TIMEOUT);
+  return ok;
+}
+
+template <int D>
+__global__ void __launch_bounds__(NT, 1) out_tc(const PrefillParams prm) {
+  using Cfg = OutCfg<D>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = align1024(smem_raw);
+  unsigned char* sQ = smem;
+  unsigned char* sK = smem + Cfg::k;
+  unsigned char* sV = smem + Cfg::v;
+  unsigned char* sP = smem + Cfg::p;
+  uint64_t* mbS = reinterpret_cast<uint64_t*>(smem + Cfg::bars);
+  uint64_t* mbO = mbS + 2;
+  uint64_t* mbD = mbS + 3;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Cfg::tslot);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int L = prm.L, pair = blockIdx.y;
+  const int qb = gridDim.x - 1 - blockIdx.x;  // longest rows first
+  const size_t base = static_cast<size_t>(pair) * L * D;
+  const __half* Q = static_cast<const __half*>(prm.q) + base;
+  const __half* K = static_cast<const __half*>(prm.k) + base;
+  const __half* V = static_cast<const __half*>(prm.v) + base;
+  const int n = qb + 1;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int rl = quarter * 32 + lane, row = qb * BLK + rl;  // this thread's TMEM lane / query row
+
+  griddep_wait();
+  if (warp == 0) tc::tmem_alloc(tslot, kOutTmemCols);
+  if (tid == 0) {
+    for (int i = 0; i < 4; ++i) mbar_init(&mbS[i], 1);
+    fence_mbar_init();
+  }
+  const float lse = lse_at(prm.lse2 + static_cast<size_t>(pair) * L, qb * BLK, rl, L);
+  load_tile<D>(sQ, Q, qb * BLK, L, tid);
+  load_tile<D>(sK, K, 0, L, tid);
+  if (n > 1) load_tile<D>(sK + Cfg::TILE, K, BLK, L, tid);
+  load_tile<D>(sV, V, 0, L, tid);
+  cp_async_commit();
+  cp_async_wait<0>();
+  fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = *tslot;
+  const uint32_t o_tmem = tbase + 2 * BLK;
+  if (tid == 0) {
+    issue_block<D>(tbase, sQ, sK);
+    tc::mma_commit(&mbS[0]);
+    if (n > 1) {
+      issue_block<D>(tbase + BLK, sQ, sK + Cfg::TILE);
+      tc::mma_commit(&mbS[1]);
+    }
+  }
+  const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+  bool ok = true;
+  for (int j = 0; j < n; ++j) {
+    const int b = j & 1;
+    if (ok) ok = wait_all(&mbS[b], static_cast<uint32_t>((j >> 1) & 1), lane, prm.err);
+    tc::fence_after_sync();
+    if (j + 2 < n) load_tile<D>(sK + b * Cfg::TILE, K, (j + 2) * BLK, L, tid);  // S(j) has read stage b
+    cp_async_commit();
+    uint32_t ph[32];  // this thread's 64 probabilities as fp16 pairs
+    if (ok) {
+      float v[64];
+      tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + half * 64), *reinterpret_cast<float(*)[32]>(v));
+      tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + half * 64 + 32),
+                    *reinterpret_cast<float(*)[32]>(v + 32));
+      if (j == qb) {  // diagonal block: key half * 64 + e is visible to row rl if it is <= rl
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = half * 64 + 2 * e <= rl ? ex2(fmaf(v[2 * e], prm.qscale, -lse)) : 0.f;
+          const float p1 = half * 64 + 2 * e + 1 <= rl ? ex2(fmaf(v[2 * e + 1], prm.qscale, -lse)) : 0.f;
+          ph[e] = tc::cvt_half2(p0, p1);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          ph[e] = tc::cvt_half2(ex2(fmaf(v[2 * e], prm.qscale, -lse)), ex2(fmaf(v[2 * e + 1], prm.qscale, -lse)));
+      }
+    }
+    // O(j-1) complete: probability tile b (last read by O(j-2)) and value
+    // stage (j+1)%2 (read by O(j-1)) are free
+    if (ok && j >= 1) ok = wait_all(mbO, static_cast<uint32_t>((j - 1) & 1), lane, prm.err);
+    tc::fence_after_sync();
+    if (j + 1 < n) load_tile<D>(sV + ((j + 1) & 1) * Cfg::TILE, V, (j + 1) * BLK, L, tid);
+    cp_async_commit();
+    if (ok) {
+      unsigned char* prow = sP + b * Cfg::PT + half * (BLK * 128) + rl * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(prow + ((c ^ (rl & 7)) << 4)) = make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2],
+                                                                            ph[4 * c + 3]);
+    }
+    cp_async_wait<1>();  // all but the value block j + 1 just requested
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();  // P(j) written, V(j) and K(j + 2) landed, S(j) read
+    tc::fence_after_sync();
+    if (tid == 0 && ok) {
+      issue_pv<D>(o_tmem, sP + b * Cfg::PT, sV + b * Cfg::TILE, j > 0);
+      tc::mma_commit(mbO);
+      if (j + 2 < n) {
+        issue_block<D>(tbase + b * BLK, sQ, sK + b * Cfg::TILE);
+        tc::mma_commit(&mbS[b]);
+      }
+    }
+  }
+  if (ok) ok = wait_all(mbO, static_cast<uint32_t>((n - 1) & 1), lane, prm.err);
+  tc::fence_after_sync();
+  griddep_launch();
+  if (ok) {
+    float* dst = prm.out + (static_cast<size_t>(pair) * L + row) * D + half * (D / 2);
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) {
+      float o[32];
+      tc::tmem_ld32(lane_addr + 2 * BLK + static_cast<uint32_t>(half * (D / 2) + c * 32), o);
+      if (row < L) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          reinterpret_cast<float4*>(dst + c * 32)[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+      }
+    }
+  }
+  // every MMA this CTA issued has completed before its TMEM is freed
+  if (tid == 0) {
+    tc::mma_commit(mbD);
+    if (!mbar_wait_bounded(mbD, 0, kWaitLimit) && prm.err) atomicOr(prm.err, ERR_MMA_TIMEOUT);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_free(tbase, kOutTmemCols);
 }
 
 template <typename Kern>
@@ -342,10 +539,13 @@ cudaError_t launch_prefill_colsum_tc(const PrefillParams& prm, int D, int pairs,
 
 cudaError_t launch_prefill_stats_tc(const PrefillParams& prm, int D, int pairs, cudaStream_t s) {
   if (prm.L <= 0) return cudaSuccess;
+  if (D != 64 && D != 128) return cudaErrorInvalidValue;
   const dim3 grid((prm.L + BLK - 1) / BLK, pairs);
-  if (D == 128) return launch_tc(stats_tc<128>, grid, TcCfg<128>::bytes, s, prm);
-  if (D == 64) return launch_tc(stats_tc<64>, grid, TcCfg<64>::bytes, s, prm);
-  return cudaErrorInvalidValue;
+  cudaError_t e = D == 128 ? launch_tc(stats_tc<128>, grid, TcCfg<128>::bytes, s, prm)
+                           : launch_tc(stats_tc<64>, grid, TcCfg<64>::bytes, s, prm);
+  if (e != cudaSuccess || prm.out == nullptr) return e;
+  return D == 128 ? launch_tc(out_tc<128>, grid, OutCfg<128>::bytes, s, prm)
+                  : launch_tc(out_tc<64>, grid, OutCfg<64>::bytes, s, prm);
 }
 
 }  // namespace h2o

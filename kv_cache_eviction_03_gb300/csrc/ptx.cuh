@@ -111,6 +111,13 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// 2^x by the SFU's approximate exponential (PTX ex2.approx.ftz.f32: relative
+// error a few units in the last place; results below 2^-126 flush to zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -185,10 +192,31 @@ __device__ __forceinline__ uint64_t desc_k_sw128(uint32_t saddr) {
   return d;
 }
 
+// MN-major operand (the M or N index contiguous) in the 128-byte swizzle: an
+// atom is 8 K-rows of 64 fp16 along MN (1024 bytes); atoms `mn_stride` bytes
+// apart along MN, 1024 bytes apart along K.
+__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t saddr, uint32_t mn_stride) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;  // leading byte offset: next MN atom
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;                    // stride byte offset: next 8 K-rows
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
 // Instruction descriptor of kind::f16 with fp16 A and B (both K-major) and an
 // fp32 accumulator, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
   return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+// The same with B MN-major (bit 16: B transposed).
+__host__ __device__ constexpr uint32_t idesc_f16_f32_bmn(int M, int N) { return idesc_f16_f32(M, N) | (1u << 16); }
+
+// Two floats to fp16x2 (round to nearest even), `lo` in the low half.
+__device__ __forceinline__ uint32_t cvt_half2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
