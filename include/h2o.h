@@ -132,15 +132,20 @@ H2O_API int h2o_cache_check(h2o_cache* cache, void* stream);
 
 /* Tuning of the decode kernel's launch shape: `splits` CTAs (one thread-block
  * cluster) share a pair, each streaming its slots through a ring of `stages`
- * 16-row shared-memory stages.  0 = automatic for either value.  splits must
- * be 1, 2, 4, 8 or 16, stages 4, 8, 12 or 16 (a multiple of the kernel's four
- * consumer warps); H2O_EINVAL otherwise or if the shape cannot be scheduled
- * on the current device. */
+ * 16-row shared-memory stages; splits must be 1, 2, 4, 8 or 16 and stages 4,
+ * 8, 12 or 16 (a multiple of the kernel's four consumer warps).  Or splits =
+ * H2O_DECODE_WARP_PER_PAIR: one warp streams a whole pair through its own
+ * ring of `stages` (2..8) and then takes its next pair, for many pairs of at
+ * most 1024 slots.  0 = automatic for either value (the automatic choice
+ * takes warp per pair when there are at least four pairs per SM).  Returns
+ * H2O_EINVAL for other values or if the shape cannot be scheduled on the
+ * current device.  Every shape computes the same step. */
+#define H2O_DECODE_WARP_PER_PAIR (-1)
 H2O_API int h2o_cache_set_decode_shape(h2o_cache* cache, int splits, int stages);
 
 /* info[0..9] = {batch, heads, head_dim, heavy, recent, kv_dtype,
- *               decode splits in use, decode stages in use, decode threads
- *               per CTA, 0}. */
+ *               decode splits in use (-1: warp per pair), decode stages in
+ *               use, decode threads per CTA, 0}. */
 H2O_API int h2o_cache_info(const h2o_cache* cache, int32_t* info);
 
 /* Column sums of the prefill without any device allocation.  The paper has

@@ -16,6 +16,7 @@ import numpy as np
 from . import _build
 
 H2O_F16, H2O_F32 = 0, 1
+H2O_DECODE_WARP_PER_PAIR = -1  # h2o_cache_set_decode_shape: one warp per pair
 STATUS = {0: "H2O_OK", -1: "H2O_EINVAL", -2: "H2O_ENOMEM", -3: "H2O_ECUDA", -4: "H2O_ESTATE", -5: "H2O_EDEVICE"}
 HEADER_INTS = 16
 MAGIC = 0x48324F31

@@ -36,6 +36,10 @@
 #include <cooperative_groups.h>
 #include <cuda_fp16.h>
 
+#include <array>
+#include <map>
+#include <mutex>
+
 #include "h2o_internal.cuh"
 #include "ptx.cuh"
 
@@ -51,21 +55,126 @@ constexpr float kNeg = -3.0e38f;  // finite "minus infinity" for running maxima
 constexpr uint32_t kWaitLimit = 200000u;
 constexpr int kMaxChunk = 4096;
 
-template <typename T, int D, int NCW, int TILE>
-struct DecodeCfg {
+// How a warp reads K/V rows of this type and width: each lane takes 16 bytes
+// of a row, so LPR lanes cover a row and a warp-wide load covers RPI rows.
+template <typename T, int D>
+struct RowGeom {
   static constexpr int E = sizeof(T);
   static constexpr int ROWB = D * E;     // bytes per K or V row
   static constexpr int EPV = 16 / E;     // elements per 16-byte vector
   static constexpr int LPR = ROWB / 16;  // lanes per row
   static constexpr int RPI = 32 / LPR;   // rows per warp-wide load
+  static_assert(LPR >= 1 && LPR <= 32, "row must be 16..512 bytes");
+};
+
+template <typename T, int D, int NCW, int TILE>
+struct DecodeCfg : RowGeom<T, D> {
+  using G = RowGeom<T, D>;
   static constexpr int NW = NCW + 1;     // consumer warps + one producer warp
   static constexpr int NT = NW * 32;
-  static constexpr int STAGE = 2 * TILE * ROWB;
-  static_assert(LPR >= 1 && LPR <= 32, "row must be 16..512 bytes");
-  static_assert(TILE % RPI == 0, "a stage holds whole row groups");
+  static constexpr int STAGE = 2 * TILE * G::ROWB;
+  static_assert(TILE % G::RPI == 0, "a stage holds whole row groups");
   static_assert(NCW * 32 >= D, "one consumer thread per output dimension in the merge");
   static_assert(TILE <= 64, "per-warp weight buffer holds 64 rows");
 };
+
+// One warp attends to one stage of `rows` (<= TILE) K/V rows: the logits
+// q . k_r (q pre-scaled into the base-2 domain) are kept in lg[0..rows), and
+// the warp's running softmax state (m, l, o) absorbs the rows.  Row group g
+// of the warp (LPR lanes) owns RG rows; every lane accumulates partial dot
+// products of those rows over its 16 bytes of the row, a butterfly exchange
+// sums them so that lane-group members end up holding whole-row logits (DUP
+// copies of each), and the probabilities go through the warp's shared buffer
+// wb to the lanes that weight V.  After the call the warp no longer reads the
+// stage.
+template <typename T, int D, int TILE>
+__device__ __forceinline__ void attend_tile(const unsigned char* sK, const unsigned char* sV, int rows,
+                                            const float (&qv)[RowGeom<T, D>::EPV], float& m, float& l,
+                                            float (&o)[RowGeom<T, D>::EPV], float* wb, float* lg, int lane) {
+  using Gm = RowGeom<T, D>;
+  constexpr int EPV = Gm::EPV, LPR = Gm::LPR, ROWB = Gm::ROWB;
+  constexpr int G = Gm::RPI;      // row groups per warp
+  constexpr int RG = TILE / G;    // rows per group per stage
+  constexpr int DUP = LPR / RG;   // lanes holding each row's total
+  static_assert(RG >= 1 && RG <= LPR && LPR % RG == 0, "butterfly shape");
+  const int grp = lane / LPR, lig = lane % LPR;
+  float acc[RG];
+#pragma unroll
+  for (int r = 0; r < RG; ++r) {
+    const int row = grp * RG + r;
+    float kf[EPV];
+    Vec16<T>::unpack(*reinterpret_cast<const uint4*>(sK + row * ROWB + lig * 16), kf);
+    float a = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) a = fmaf(qv[e], kf[e], a);
+    acc[r] = row < rows ? a : 0.f;
+  }
+  // butterfly: halve the rows held per lane at each step
+#pragma unroll
+  for (int off = LPR / 2, n = RG; off >= 1; off >>= 1) {
+    if (n > 1) {
+      const int half = n / 2;
+      const bool hi = (lig & off) != 0;
+#pragma unroll
+      for (int i = 0; i < half; ++i) {
+        const float keep = hi ? acc[half + i] : acc[i];
+        const float send = hi ? acc[i] : acc[half + i];
+        acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+      }
+      n = half;
+    } else {
+      acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], off);
+    }
+  }
+  const int rown = grp * RG + lig / DUP;  // the row whose logit this lane holds
+  const bool valid = rown < rows;
+  const float x = valid ? acc[0] : kNeg;
+  float mx = x;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  const float mn = fmaxf(m, mx);
+  const float corr = exp2f(m - mn);
+  m = mn;
+  if (lig % DUP == 0) {
+    wb[rown] = valid ? exp2f(x - mn) : 0.f;
+    if (valid) lg[rown] = x;
+  }
+  __syncwarp();
+  l *= corr;
+#pragma unroll
+  for (int e = 0; e < EPV; ++e) o[e] *= corr;
+#pragma unroll
+  for (int r = 0; r < RG; ++r) {
+    const int row = grp * RG + r;
+    if (row < rows) {
+      const float w = wb[row];
+      l += w;
+      float vf[EPV];
+      Vec16<T>::unpack(*reinterpret_cast<const uint4*>(sV + row * ROWB + lig * 16), vf);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) o[e] = fmaf(w, vf[e], o[e]);
+    }
+  }
+  __syncwarp();  // wb is rewritten by the next stage
+}
+
+// Merge the row groups of a warp: afterwards every group holds the same
+// (m, l, o) over all rows the warp has seen.
+template <typename T, int D>
+__device__ __forceinline__ void merge_groups(float& m, float& l, float (&o)[RowGeom<T, D>::EPV]) {
+  constexpr int EPV = RowGeom<T, D>::EPV, LPR = RowGeom<T, D>::LPR;
+#pragma unroll
+  for (int off = LPR; off < 32; off <<= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+    const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
+    const float M = fmaxf(m, m2);
+    const float a = exp2f(m - M), b = exp2f(m2 - M);
+    l = l * a + l2 * b;
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) o[e] = o[e] * a + __shfl_xor_sync(0xffffffffu, o[e], off) * b;
+    m = M;
+  }
+}
 
 constexpr int kMaxStages = 16;
 
@@ -117,7 +226,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
   // are rejected on the host; a kernel given one does no streaming.
   const int NSTAGE = prm.nstage;
   const bool ring_ok = NSTAGE >= NCW && NSTAGE % NCW == 0 && NSTAGE <= kMaxStages;
-  constexpr int EPV = Cfg::EPV, LPR = Cfg::LPR, RPI = Cfg::RPI, ROWB = Cfg::ROWB;
+  constexpr int EPV = Cfg::EPV, LPR = Cfg::LPR, ROWB = Cfg::ROWB;
   constexpr int NT = Cfg::NT, NW = Cfg::NW;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + Lay::full);
@@ -258,15 +367,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
       }
     }
     // Each consumer warp takes whole stages in turn (warp w: stages w, w+NCW,
-    // ...).  Within a stage, row group g of the warp (LPR lanes) owns RG rows;
-    // every lane accumulates partial dot products of those rows over its 16
-    // bytes of the row, a butterfly exchange sums them so that lane group
-    // members end up holding whole-row logits (DUP copies of each), and the
-    // probabilities go through shared memory to the lanes that weight V.
-    constexpr int G = RPI;          // row groups per warp
-    constexpr int RG = TILE / G;    // rows per group per stage
-    constexpr int DUP = LPR / RG;   // lanes holding each row's total
-    static_assert(RG >= 1 && RG <= LPR && LPR % RG == 0, "butterfly shape");
+    // ...).
     float* wb = wbuf + warp * TILE;
     // Every earlier kernel has completed, so the next step may start its own
     // prefetch now; triggering only after this step's inputs are loaded keeps
@@ -280,83 +381,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
         atomicOr(prm.err, ERR_MBAR_TIMEOUT);
       }
       const unsigned char* sK = stage_base + static_cast<size_t>(s) * Cfg::STAGE;
-      const unsigned char* sV = sK + TILE * ROWB;
       const int rows = ok ? min(TILE, nrows - t * TILE) : 0;
-      float acc[RG];
-#pragma unroll
-      for (int r = 0; r < RG; ++r) {
-        const int row = grp * RG + r;
-        float kf[EPV];
-        Vec16<T>::unpack(*reinterpret_cast<const uint4*>(sK + row * ROWB + lig * 16), kf);
-        float a = 0.f;
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) a = fmaf(qv[e], kf[e], a);
-        acc[r] = row < rows ? a : 0.f;
-      }
-      // butterfly: halve the rows held per lane at each step
-#pragma unroll
-      for (int off = LPR / 2, n = RG; off >= 1; off >>= 1) {
-        if (n > 1) {
-          const int half = n / 2;
-          const bool hi = (lig & off) != 0;
-#pragma unroll
-          for (int i = 0; i < half; ++i) {
-            const float keep = hi ? acc[half + i] : acc[i];
-            const float send = hi ? acc[i] : acc[half + i];
-            acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-          }
-          n = half;
-        } else {
-          acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], off);
-        }
-      }
-      const int rown = grp * RG + lig / DUP;  // the row whose logit this lane holds
-      const bool valid = rown < rows;
-      const float x = valid ? acc[0] : kNeg;
-      float mx = x;
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      const float mn = fmaxf(m, mx);
-      const float corr = exp2f(m - mn);
-      m = mn;
-      if (lig % DUP == 0) {
-        wb[rown] = valid ? exp2f(x - mn) : 0.f;
-        if (valid) lg[t * TILE + rown] = x;
-      }
-      __syncwarp();
-      l *= corr;
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) o[e] *= corr;
-#pragma unroll
-      for (int r = 0; r < RG; ++r) {
-        const int row = grp * RG + r;
-        if (row < rows) {
-          const float w = wb[row];
-          l += w;
-          float vf[EPV];
-          Vec16<T>::unpack(*reinterpret_cast<const uint4*>(sV + row * ROWB + lig * 16), vf);
-#pragma unroll
-          for (int e = 0; e < EPV; ++e) o[e] = fmaf(w, vf[e], o[e]);
-        }
-      }
-      __syncwarp();  // wb is rewritten by the next stage
+      attend_tile<T, D, TILE>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lg + t * TILE, lane);
       // stage s may be refilled; after a timeout the stage is not released,
       // so no new copy can target memory an unfinished copy still writes
       if (lane == 0 && ok) mbar_arrive(&empty_bar[s]);
     }
 
-    // merge the row groups of this warp (identical result in every group)
-#pragma unroll
-    for (int off = LPR; off < 32; off <<= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-      const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
-      const float M = fmaxf(m, m2);
-      const float a = exp2f(m - M), b = exp2f(m2 - M);
-      l = l * a + l2 * b;
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) o[e] = o[e] * a + __shfl_xor_sync(0xffffffffu, o[e], off) * b;
-      m = M;
-    }
+    merge_groups<T, D>(m, l, o);  // identical result in every row group
     float* myred = red + warp * (D + 4);
     if (lane == 0) {
       myred[0] = m;
@@ -511,6 +543,290 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
   if (clustered) cluster_wait_acquire();  // (3) peers are done reading this CTA's shared memory
 }
 
+// ------------------------------------------------------------ warp per pair
+// For many short pairs (thousands of (batch, head) pairs of about a hundred
+// slots) a CTA per pair spends most of its short life starting up and
+// finishing.  Here one warp handles a whole pair and then moves on: a grid of
+// resident CTAs, grid warp w taking pairs w, w + W, w + 2W, ... (W warps in
+// the grid).  Each warp feeds its own ring of stages; its lane 0 issues the
+// bulk copies of the next tiles as soon as a stage is consumed, running on
+// into the warp's next pair, so the copies never wait for a pair's epilogue.
+// Attention, score update, argmin and overwrite of a pair are all
+// warp-synchronous (shuffles, no block barrier), and a warp's ring is used by
+// that warp alone, so any ring depth is safe.
+constexpr int kWarpMaxStages = 8;
+constexpr int kWarpMaxPairs = 64;    // pairs per warp; larger problems get a larger grid
+constexpr int kWarpMaxSlots = 1024;  // slots per pair
+constexpr int kWarpNW = 4;           // warps per CTA
+
+template <typename T, int D>
+struct WarpLayout {
+  static constexpr int TILE = 16;
+  static constexpr int STAGE = 2 * TILE * RowGeom<T, D>::ROWB;
+  static constexpr size_t bars = 0;                                     // [NW][kWarpMaxStages]
+  static constexpr size_t ctrs = bars + 8 * kWarpNW * kWarpMaxStages;   // [NW][kWarpMaxPairs] int4
+  static constexpr size_t wbuf = ctrs + 16 * kWarpNW * kWarpMaxPairs;   // [NW][TILE] floats
+  static constexpr size_t state = wbuf + 4 * kWarpNW * TILE;            // [NW][3][Cp]: logits, scores, positions
+  __host__ __device__ static int cpad(int C) { return (C + 3) / 4 * 4; }
+  __host__ __device__ static size_t stages(int C) {
+    return (state + 12 * static_cast<size_t>(kWarpNW) * cpad(C) + 127) / 128 * 128;
+  }
+  __host__ __device__ static size_t bytes(int nstage, int C) {
+    return stages(C) + static_cast<size_t>(kWarpNW) * nstage * STAGE;
+  }
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kWarpNW * 32, 1) decode_warp_kernel(const DecodeParams prm) {
+  using Gm = RowGeom<T, D>;
+  using Lay = WarpLayout<T, D>;
+  constexpr int TILE = Lay::TILE, EPV = Gm::EPV, LPR = Gm::LPR, ROWB = Gm::ROWB;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int grp = lane / LPR, lig = lane % LPR;
+  const int C = prm.C, R = prm.R, NS = prm.nstage, pairs = prm.pairs;
+  const int Cp = Lay::cpad(C);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::bars) + warp * kWarpMaxStages;
+  int4* pctr = reinterpret_cast<int4*>(smem + Lay::ctrs) + warp * kWarpMaxPairs;
+  float* wb = reinterpret_cast<float*>(smem + Lay::wbuf) + warp * TILE;
+  float* lg = reinterpret_cast<float*>(smem + Lay::state) + static_cast<size_t>(warp) * 3 * Cp;
+  float* sc = lg + Cp;
+  int* ps = reinterpret_cast<int*>(sc + Cp);
+  unsigned char* stg = smem + Lay::stages(C) + static_cast<size_t>(warp) * NS * Lay::STAGE;
+
+  const int gw = blockIdx.x * kWarpNW + warp, W = gridDim.x * kWarpNW;
+  const int np = gw < pairs ? (pairs - 1 - gw) / W + 1 : 0;  // pairs of this warp
+  const bool ring_ok = NS >= 2 && NS <= kWarpMaxStages && np <= kWarpMaxPairs && C <= kWarpMaxSlots;
+  if (np == 0) return;
+  if (!ring_ok) {  // rejected on the host; a kernel given such a shape does nothing
+    if (lane == 0) atomicOr(prm.err, ERR_RING_TIMEOUT);
+    return;
+  }
+  if (lane == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  const unsigned char* gK = static_cast<const unsigned char*>(prm.K);
+  const unsigned char* gV = static_cast<const unsigned char*>(prm.V);
+  const uint64_t policy = policy_evict_first();
+  // Counters of this warp's pairs.  Cache-owned state: read before the
+  // grid-dependency wait only when no earlier kernel on the stream touched
+  // this cache (likewise the slot store the first copies read).
+  auto load_ctrs = [&]() {
+    for (int k = lane; k < np; k += 32)
+      pctr[k] = *reinterpret_cast<const int4*>(prm.ctr + gw + static_cast<size_t>(k) * W);
+    __syncwarp();
+  };
+  // Issue cursor, identical in every lane (lane 0 issues): tile t_i of the
+  // warp's pair k_i; `issued` tiles so far over all the warp's pairs.  Tile
+  // number n always goes to stage n % NS.
+  int k_i = 0, t_i = 0, issued = 0;
+  auto issue_upto = [&](int limit) {
+    while (issued < limit && k_i < np) {
+      const int cnt = min(max(pctr[k_i].y, 0), C);
+      if (t_i * TILE >= cnt) {
+        ++k_i;
+        t_i = 0;
+        continue;
+      }
+      if (lane == 0) {
+        const int rows = min(TILE, cnt - t_i * TILE);
+        const uint32_t bytes = static_cast<uint32_t>(rows * ROWB);
+        unsigned char* st = stg + static_cast<size_t>(issued % NS) * Lay::STAGE;
+        uint64_t* bar = &full[issued % NS];
+        const size_t row0 = (static_cast<size_t>(gw) + static_cast<size_t>(k_i) * W) * C +
+                            static_cast<size_t>(t_i) * TILE;
+        mbar_arrive_expect_tx(bar, 2 * bytes);
+        bulk_g2s_stream(st, gK + row0 * ROWB, bytes, bar, policy);
+        bulk_g2s_stream(st + TILE * ROWB, gV + row0 * ROWB, bytes, bar, policy);
+      }
+      ++t_i;
+      ++issued;
+    }
+  };
+  if (prm.prefetch) {
+    load_ctrs();
+    issue_upto(NS);
+  }
+  griddep_wait();  // every earlier kernel on the stream has completed
+  if (!prm.prefetch) {
+    load_ctrs();
+    issue_upto(NS);
+  }
+
+  int consumed = 0, landed = 0;  // tiles consumed / whose copies were seen complete
+  bool ok = true;
+  // This lane's 16-byte slices of q, k_new and v_new, one pair ahead: the
+  // next pair's are loaded while the current one streams.
+  auto load_inputs = [&](int pr, uint4& q4, uint4& k4, uint4& v4) {
+    const size_t off = static_cast<size_t>(pr) * ROWB + lig * 16;
+    q4 = *reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(prm.q) + off);
+    k4 = *reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(prm.k_new) + off);
+    v4 = *reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(prm.v_new) + off);
+  };
+  uint4 q4, k4, v4, nq4, nk4, nv4;
+  load_inputs(gw, q4, k4, v4);
+  for (int k = 0; k < np; ++k) {
+    const int pr = gw + k * W;
+    const int4 c4 = pctr[k];
+    const int p = c4.x, count = min(max(c4.y, 0), C), head = c4.z;
+    const size_t slot0 = static_cast<size_t>(pr) * C;
+    // this pair's scores and positions, needed from the epilogue on
+    for (int j = lane; j < count; j += 32) {
+      cp_async4(sc + j, prm.score + slot0 + j);
+      cp_async4(ps + j, prm.pos + slot0 + j);
+    }
+    cp_async_commit();
+    if (k + 1 < np) load_inputs(pr + W, nq4, nk4, nv4);
+    // q (pre-scaled into the base-2 domain); the new token attends to
+    // itself: row group 0 starts from it
+    float qv[EPV], kf[EPV], o[EPV];
+    Vec16<T>::unpack(q4, qv);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) qv[e] *= prm.qscale;
+    Vec16<T>::unpack(k4, kf);
+    float a = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) a = fmaf(qv[e], kf[e], a);
+#pragma unroll
+    for (int off = LPR / 2; off >= 1; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+    const float s_self = a;
+    float m = kNeg, l = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) o[e] = 0.f;
+    if (grp == 0) {
+      Vec16<T>::unpack(v4, o);
+      m = s_self;
+      l = 1.f;
+    }
+    if (k == 0) griddep_launch();  // this step's first inputs are loaded
+
+    const int nt = (count + TILE - 1) / TILE;
+    for (int t = 0; t < nt; ++t) {
+      const int s = consumed % NS;
+      if (ok) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait_bounded(&full[s], static_cast<uint32_t>((consumed / NS) & 1), kWaitLimit));
+        if (ok)
+          ++landed;
+        else if (lane == 0)
+          atomicOr(prm.err, ERR_MBAR_TIMEOUT);
+      }
+      const unsigned char* sK = stg + static_cast<size_t>(s) * Lay::STAGE;
+      const int rows = ok ? min(TILE, count - t * TILE) : 0;
+      attend_tile<T, D, TILE>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lg + t * TILE, lane);
+      ++consumed;
+      if (ok) issue_upto(consumed + NS);  // the stage just read may be refilled
+    }
+
+    merge_groups<T, D>(m, l, o);
+    const float inv = 1.f / l;
+    const float p_self = exp2f(s_self - m) * inv;
+    if (ok && grp == 0) {
+      float* dst = prm.out + static_cast<size_t>(pr) * D + lig * EPV;
+#pragma unroll
+      for (int e = 0; e < EPV; e += 4)
+        *reinterpret_cast<float4*>(dst + e) = make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+    }
+    // probabilities -> accumulated scores; the lowest candidate key (score
+    // bits, position) among kept positions <= p - R
+    cp_async_wait<0>();
+    __syncwarp();
+    const bool fullc = count >= C;
+    const int limit = p - R;
+    unsigned long long kmin = ~0ull;
+    int smin = -1;
+    for (int j = lane; j < count; j += 32) {
+      const float ns = sc[j] + exp2f(lg[j] - m) * inv;
+      sc[j] = ns;
+      if (fullc && ps[j] <= limit) {
+        const unsigned long long key =
+            (static_cast<unsigned long long>(__float_as_uint(ns)) << 32) | static_cast<uint32_t>(ps[j]);
+        if (key < kmin) {
+          kmin = key;
+          smin = j;
+        }
+      }
+    }
+    unsigned long long wk = kmin;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, wk, off);
+      wk = other < wk ? other : wk;
+    }
+    const unsigned holder = __ballot_sync(0xffffffffu, kmin == wk && kmin != ~0ull);
+    const int wslot = __shfl_sync(0xffffffffu, smin, holder ? __ffs(holder) - 1 : 0);
+    const int u = fullc ? (holder ? wslot : -1) : count;
+    __syncwarp();
+    if (ok) {
+      if (fullc && u < 0 && lane == 0) atomicOr(prm.err, ERR_NO_CANDIDATE);
+      for (int j = lane; j < count; j += 32) prm.score[slot0 + j] = (j == u) ? p_self : sc[j];
+      if (u >= 0) {
+        // the new row from the slices already in registers: row group 0
+        // writes K, group 1 writes V (one group covering the row: both)
+        const size_t us = (slot0 + u) * ROWB + lig * 16;
+        if (grp == 0) *reinterpret_cast<uint4*>(static_cast<unsigned char*>(prm.K) + us) = k4;
+        if (grp == (LPR == 32 ? 0 : 1)) *reinterpret_cast<uint4*>(static_cast<unsigned char*>(prm.V) + us) = v4;
+        if (lane == 0) {
+          prm.pos[slot0 + u] = p;
+          if (u >= count) prm.score[slot0 + u] = p_self;  // fill phase: the slot was empty
+        }
+      }
+      if (lane == 0) {
+        if (u >= 0) prm.ring[static_cast<size_t>(pr) * R + head] = u;
+        *reinterpret_cast<int4*>(prm.ctr + pr) = make_int4(p + 1, fullc ? C : count + 1, (head + 1) % R, 0);
+        if (prm.evicted) prm.evicted[pr] = fullc ? u : -1;
+      }
+    }
+    __syncwarp();  // sc, ps and lg are refilled for the next pair
+    q4 = nq4;
+    k4 = nk4;
+    v4 = nv4;
+  }
+  // no copy may still be landing in shared memory when the warp exits
+  if (lane == 0)
+    for (int n = landed; n < issued; ++n)
+      if (!mbar_wait_bounded(&full[n % NS], static_cast<uint32_t>((n / NS) & 1), kWaitLimit))
+        atomicOr(prm.err, ERR_RING_TIMEOUT);
+}
+
+template <typename T, int D>
+struct WarpKern {
+  using Lay = WarpLayout<T, D>;
+  static constexpr auto fn = decode_warp_kernel<T, D>;
+
+  static cudaError_t attrs() {
+    size_t most = Lay::bytes(kWarpMaxStages, kWarpMaxSlots);
+    if (most > 227 * 1024) most = 227 * 1024;
+    return kernel_attrs(reinterpret_cast<const void*>(fn), most, false);
+  }
+  // CTAs resident per SM (0 = cannot launch)
+  static int per_sm(int nstage, int C) {
+    const size_t bytes = Lay::bytes(nstage, C);
+    if (bytes > 227 * 1024 || attrs() != cudaSuccess) return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kWarpNW * 32, bytes) != cudaSuccess) return 0;
+    return n;
+  }
+  static cudaError_t launch(const DecodeParams& prm, int ctas, cudaStream_t s) {
+    cudaError_t e = attrs();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas, 1, 1);
+    cfg.blockDim = dim3(kWarpNW * 32, 1, 1);
+    cfg.dynamicSmemBytes = Lay::bytes(prm.nstage, prm.C);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, prm);
+  }
+};
+
 template <typename T, int D>
 struct Kern {
   static constexpr int NCW = 4, TILE = 16;
@@ -620,8 +936,26 @@ int decode_resident(int dtype, int D, int splits, int nstage, int chunk, int pai
 // slots), with a 12-stage ring (three stages in flight per consumer warp)
 // when two such CTAs fit on an SM.  Grids that need several waves anyway
 // (many pairs) use 4-stage rings so that more CTAs are resident.
+// Many short pairs (at least four per SM, each within the warp kernel's slot
+// limit) go to the warp-per-pair kernel.  More resident warps beat deeper
+// rings, so its ring is the deepest that still leaves as many resident warps
+// as there are pairs, up to the count the shallowest ring allows.
+int decode_warp_default_stages(int dtype, int D, int C, int pairs) {
+  const long long most = static_cast<long long>(decode_warp_resident(dtype, D, 2, C)) * kWarpNW;
+  const long long want = pairs < most ? pairs : most;
+  for (int st = kWarpMaxStages; st > 2; --st)
+    if (static_cast<long long>(decode_warp_resident(dtype, D, st, C)) * kWarpNW >= want) return st;
+  return 2;
+}
+
 DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C) {
   const int sms = device_sms();
+  if (sms > 0 && C <= kWarpMaxSlots && pairs >= 4 * sms && decode_warp_resident(dtype, D, 2, C) > 0) {
+    DecodeShape w;
+    w.splits = kDecodeWarpPerPair;
+    w.stages = decode_warp_default_stages(dtype, D, C, pairs);
+    return w;
+  }
   const long long target = sms > 0 ? (17LL * sms) / 10 : 256;
   DecodeShape sh;
   sh.splits = 1;
@@ -649,10 +983,61 @@ DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C) {
   return sh;
 }
 
+int decode_warp_max_slots() { return kWarpMaxSlots; }
+int decode_warp_min_stages() { return 2; }
+int decode_warp_max_stages() { return kWarpMaxStages; }
+
+int decode_warp_resident(int dtype, int D, int nstage, int C) {
+  if (nstage < 2 || nstage > kWarpMaxStages || C > kWarpMaxSlots) return 0;
+  const int sms = device_sms();
+  int per = 0;
+  if (dtype == 0 && D == 128) per = WarpKern<__half, 128>::per_sm(nstage, C);
+  else if (dtype == 0 && D == 64) per = WarpKern<__half, 64>::per_sm(nstage, C);
+  else if (dtype == 1 && D == 128) per = WarpKern<float, 128>::per_sm(nstage, C);
+  else per = WarpKern<float, 64>::per_sm(nstage, C);
+  cudaGetLastError();
+  return per * sms;
+}
+
+namespace {
+// resident CTAs of the warp-per-pair kernel for a shape, looked up once
+int warp_grid(int dtype, int D, int nstage, int C, int pairs) {
+  static std::mutex mu;
+  static std::map<std::array<int, 5>, int> known;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const std::array<int, 5> key{dtype, D, nstage, C, dev};
+  int res;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    auto it = known.find(key);
+    if (it != known.end()) {
+      res = it->second;
+    } else {
+      res = decode_warp_resident(dtype, D, nstage, C);
+      known[key] = res;
+    }
+  }
+  const int need = (pairs + kWarpNW - 1) / kWarpNW;                           // one pair per warp
+  const int least = (pairs + kWarpNW * kWarpMaxPairs - 1) / (kWarpNW * kWarpMaxPairs);  // pair-list bound
+  const int g = res < need ? res : need;
+  return g > least ? g : least;
+}
+}  // namespace
+
 cudaError_t launch_decode(const DecodeParams& prm, int dtype, int D, int pairs, int splits, int threads,
                           cudaStream_t s) {
   (void)threads;
   if ((dtype != 0 && dtype != 1) || (D != 64 && D != 128)) return cudaErrorInvalidValue;
+  if (splits == kDecodeWarpPerPair) {
+    if (prm.C > kWarpMaxSlots || prm.nstage < 2 || prm.nstage > kWarpMaxStages) return cudaErrorInvalidValue;
+    const int ctas = warp_grid(dtype, D, prm.nstage, prm.C, pairs);
+    if (ctas <= 0) return cudaErrorInvalidConfiguration;
+    if (dtype == 0 && D == 128) return WarpKern<__half, 128>::launch(prm, ctas, s);
+    if (dtype == 0 && D == 64) return WarpKern<__half, 64>::launch(prm, ctas, s);
+    if (dtype == 1 && D == 128) return WarpKern<float, 128>::launch(prm, ctas, s);
+    return WarpKern<float, 64>::launch(prm, ctas, s);
+  }
   return dispatch(dtype, D, [&](auto k) { return decltype(k)::launch(prm, pairs, splits, s); });
 }
 

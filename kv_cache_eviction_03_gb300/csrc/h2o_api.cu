@@ -64,7 +64,7 @@ void forget_cache(const h2o_cache* c) {
 }
 
 int splits_in_use(const h2o_cache* c) {
-  return c->splits_override > 0 ? c->splits_override : c->shape_auto.splits;
+  return c->splits_override != 0 ? c->splits_override : c->shape_auto.splits;
 }
 int stages_in_use(const h2o_cache* c) {
   return c->stages_override > 0 ? c->stages_override : c->shape_auto.stages;
@@ -286,6 +286,7 @@ int h2o_decode_step(h2o_cache* c, const void* q, const void* k_new, const void* 
   dp.nstage = stages_in_use(c);
   dp.qscale = scale * 1.4426950408889634f;
   dp.prefetch = touch_stream(c, stream) ? 1 : 0;
+  dp.pairs = c->P;
   cudaError_t e = h2o::launch_decode(dp, c->dtype, c->D, c->P, splits, 128, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "h2o_decode_step: launch");
   c->host_next_p += 1;
@@ -395,20 +396,39 @@ int h2o_cache_check(h2o_cache* c, void* stream) {
 
 int h2o_cache_set_decode_shape(h2o_cache* c, int splits, int stages) {
   if (!c) return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: cache is NULL");
-  if (splits != 0 && splits != 1 && splits != 2 && splits != 4 && splits != 8 && splits != 16)
-    return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: splits must be 0, 1, 2, 4, 8 or 16");
-  if (stages < 0 || stages > h2o::decode_max_stages() || stages % h2o::decode_stage_multiple() != 0)
-    return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: stages must be a multiple of %d in 0..%d",
-                h2o::decode_stage_multiple(), h2o::decode_max_stages());
-  const int s = splits > 0 ? splits : c->shape_auto.splits;
-  const int n = stages > 0 ? stages : c->shape_auto.stages;
-  if (chunk_for(c->C, s) > h2o::decode_max_chunk())
-    return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: %d splits leave more than %d slots per CTA", s,
-                h2o::decode_max_chunk());
-  if (h2o::decode_resident(c->dtype, c->D, s, n, chunk_for(c->C, s), c->P) < s)
-    return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: %d CTAs per pair with %d stages cannot be scheduled", s, n);
+  if (splits != 0 && splits != 1 && splits != 2 && splits != 4 && splits != 8 && splits != 16 &&
+      splits != h2o::kDecodeWarpPerPair)
+    return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: splits must be 0, 1, 2, 4, 8, 16 or -1 (warp per pair)");
+  const int s = splits != 0 ? splits : c->shape_auto.splits;
+  int n = stages;
+  if (n == 0) {
+    if (s == c->shape_auto.splits)
+      n = c->shape_auto.stages;
+    else
+      n = s == h2o::kDecodeWarpPerPair ? h2o::decode_warp_default_stages(c->dtype, c->D, c->C, c->P) : 4;
+  }
+  if (s == h2o::kDecodeWarpPerPair) {
+    if (c->C > h2o::decode_warp_max_slots())
+      return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: warp per pair takes at most %d slots per pair",
+                  h2o::decode_warp_max_slots());
+    if (n < h2o::decode_warp_min_stages() || n > h2o::decode_warp_max_stages())
+      return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: warp per pair takes %d..%d stages",
+                  h2o::decode_warp_min_stages(), h2o::decode_warp_max_stages());
+    if (h2o::decode_warp_resident(c->dtype, c->D, n, c->C) <= 0)
+      return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: warp per pair with %d stages cannot be scheduled", n);
+  } else {
+    if (n < 0 || n > h2o::decode_max_stages() || n % h2o::decode_stage_multiple() != 0)
+      return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: stages must be a multiple of %d in 0..%d",
+                  h2o::decode_stage_multiple(), h2o::decode_max_stages());
+    if (chunk_for(c->C, s) > h2o::decode_max_chunk())
+      return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: %d splits leave more than %d slots per CTA", s,
+                  h2o::decode_max_chunk());
+    if (h2o::decode_resident(c->dtype, c->D, s, n, chunk_for(c->C, s), c->P) < s)
+      return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: %d CTAs per pair with %d stages cannot be scheduled", s,
+                  n);
+  }
   c->splits_override = splits;
-  c->stages_override = stages;
+  c->stages_override = (splits == 0 && stages == 0) ? 0 : n;
   return H2O_OK;
 }
 
@@ -422,7 +442,7 @@ int h2o_cache_info(const h2o_cache* c, int32_t* info) {
   info[5] = c->dtype;
   info[6] = splits_in_use(c);
   info[7] = stages_in_use(c);
-  info[8] = h2o::decode_threads();
+  info[8] = splits_in_use(c) == h2o::kDecodeWarpPerPair ? 128 : h2o::decode_threads();
   info[9] = 0;
   return H2O_OK;
 }

@@ -45,6 +45,7 @@ struct DecodeParams {
   int prefetch;       // 1: the previous kernel on the stream did not touch
                       // this cache, so its slot store may be read before the
                       // grid-dependency wait
+  int pairs;          // P
 };
 
 struct PrefillParams {
@@ -85,9 +86,12 @@ cudaError_t kernel_attrs(const void* kern, size_t smem_bytes, bool nonportable_c
 // Launchers (return the launch error; they do not synchronise).
 cudaError_t launch_decode(const DecodeParams& prm, int dtype, int D, int pairs, int splits, int threads,
                           cudaStream_t s);
+// splits value selecting the warp-per-pair decode kernel (one warp streams
+// a whole pair, each CTA's warps work through several pairs in turn)
+constexpr int kDecodeWarpPerPair = -1;
 struct DecodeShape {
-  int splits;  // CTAs (one cluster) per pair
-  int stages;  // shared-memory ring depth per CTA
+  int splits;  // CTAs (one cluster) per pair, or kDecodeWarpPerPair
+  int stages;  // shared-memory ring depth per CTA (per warp in warp-per-pair mode)
 };
 DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C);
 // CTAs of this shape that fit on the device at once (0: cannot launch)
@@ -97,6 +101,12 @@ int decode_max_stages();
 int decode_stage_multiple();  // ring depths must be multiples of this
 int decode_max_chunk();
 int decode_threads();
+// warp-per-pair kernel: limits, and whether a shape can run (0 = no)
+int decode_warp_max_slots();
+int decode_warp_min_stages();
+int decode_warp_max_stages();
+int decode_warp_resident(int dtype, int D, int nstage, int C);
+int decode_warp_default_stages(int dtype, int D, int C, int pairs);
 
 cudaError_t launch_prefill_stats(const PrefillParams& prm, int dtype, int D, int pairs, cudaStream_t s);
 cudaError_t launch_prefill_colsum(const PrefillParams& prm, int dtype, int D, int pairs, cudaStream_t s);

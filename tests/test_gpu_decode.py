@@ -145,11 +145,11 @@ def test_small_shapes_every_step(case):
     assert rep.pairs == w.pairs * T
 
 
-@pytest.mark.parametrize("splits", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("splits", [1, 2, 4, 8, 16, B.H2O_DECODE_WARP_PER_PAIR])
 def test_splits_agree(splits):
-    """Every cluster size (CTAs per pair) gives the oracle's result, including
-    ragged last CTAs (301 slots) and CTAs whose slot range is still empty
-    while filling."""
+    """Every cluster size (CTAs per pair) and the warp-per-pair kernel give
+    the oracle's result, including ragged last CTAs (301 slots) and CTAs
+    whose slot range is still empty while filling."""
     w = W.Workload("splits", 1, 4, 128, "f16", 280, 40, 150, 151, 1.1)
     rep = run_stepwise(w, 11, check=set(range(0, 40, 3)) | {21, 22}, splits=splits)
     assert rep.pairs > 0
@@ -175,7 +175,34 @@ def test_ring_depth_must_be_a_multiple_of_four():
     B.h2o_cache_destroy(cache)
 
 
-@pytest.mark.parametrize("splits", [1, 4, 16])
+@pytest.mark.parametrize("stages", [2, 3, 5, 6])
+def test_warp_per_pair_ring_depths_and_pair_hand_over(stages):
+    """Warp per pair with more pairs than warps in the grid, so each warp's
+    ring runs on from one pair into the next (tiles of consecutive pairs
+    share stages), for several ring depths; ragged tiles (C = 61) and a
+    fill phase right after a short prompt."""
+    w = W.Workload("warp", 32, 100, 128, "f16", 50, 14, 31, 30, 1.1)
+    rep = run_stepwise(w, 31, check={0, 5, 10, 11, 12, 13}, splits=B.H2O_DECODE_WARP_PER_PAIR, stages=stages)
+    assert rep.pairs == w.pairs * 6
+
+
+def test_warp_per_pair_shape_limits():
+    cache = B.h2o_cache_create(1, 2, 128, 40, 40, B.H2O_F16)
+    for bad in (1, 9):
+        with pytest.raises(B.H2OError):
+            B.h2o_cache_set_decode_shape(cache, B.H2O_DECODE_WARP_PER_PAIR, bad)
+    B.h2o_cache_set_decode_shape(cache, B.H2O_DECODE_WARP_PER_PAIR, 5)
+    assert B.h2o_cache_info(cache)[6:8] == [-1, 5]
+    B.h2o_cache_set_decode_shape(cache, 0, 0)
+    assert B.h2o_cache_info(cache)[6] != -1  # two pairs: the automatic shape is a cluster per pair
+    B.h2o_cache_destroy(cache)
+    big = B.h2o_cache_create(1, 1, 64, 600, 500, B.H2O_F16)  # 1100 slots: beyond warp per pair
+    with pytest.raises(B.H2OError):
+        B.h2o_cache_set_decode_shape(big, B.H2O_DECODE_WARP_PER_PAIR, 0)
+    B.h2o_cache_destroy(big)
+
+
+@pytest.mark.parametrize("splits", [1, 4, 16, B.H2O_DECODE_WARP_PER_PAIR])
 def test_free_run_fp16(splits):
     w = W.Workload("free", 2, 4, 128, "f16", 300, 80, 40, 30, 1.1)
     worst, alive = run_free(w, 5, splits=splits)
