@@ -1,26 +1,40 @@
 // H2O prefill on the 5th-generation tensor cores (tcgen05, accumulators in
-// tensor memory): the row log-sum-exp pass and the column-sum pass for fp16
-// K/V.
+// tensor memory) for fp16 K/V: the row log-sum-exp pass, the attention
+// output pass and the column-sum pass.
 //
 // Method: "H2O: Heavy-Hitter Oracle ... 深度解读报告", section 3.4 (prefill
 // keep rule) with the score of section 3.3 / 2.3: every prompt token's score
 // is the attention mass it receives, colsum_j = sum_{i>=j} exp(s_ij - lse_i),
-// s_ij = scale * q_i . k_j.
+// s_ij = scale * q_i . k_j; the output is ordinary causal attention,
+// O_i = sum_j exp(s_ij - lse_i) v_j.
 //
-// Both passes work on 128 x 128 blocks of logits.  One thread issues
-// tcgen05.mma (M = N = 128, K = 16, fp16 operands from shared memory laid out
-// K-major with the 128-byte swizzle, fp32 accumulators in TMEM); the block's
-// 256 threads then read the accumulators with tcgen05.ld and do the
-// exponentials.  Two TMEM accumulators and two operand stages let the tensor
-// core work on block i+1 while the threads finish block i.
-//  - rows (stats_tc): A = 128 query rows, B = a 128-key block; TMEM lane =
-//    query row, so each thread keeps an online max / sum of its row.
-//  - columns (colsum_tc): A = 128 keys, B = a 128-query block, i.e. the
-//    transposed logits; TMEM lane = key, so each thread sums the
-//    probabilities its key receives with no cross-thread reduction (float32
-//    within a block, float64 across blocks: fixed order, deterministic).
-// Every wait is bounded; the TMEM allocation is freed on every path.
+// All three passes work on 128 x 128 blocks of logits and are warp
+// specialised.  Warp 0 streams operand tiles with TMA (3-D tensor maps over
+// [P, L, D], 64-element boxes in the 128-byte swizzle that the MMAs read;
+// rows past the prompt arrive as zeros) through rings of shared-memory
+// stages; one lane of warp 1 issues tcgen05.mma (M = N = 128, K = 16, fp32
+// accumulators in TMEM, two logit accumulators so the tensor core works on
+// block i+1 while block i is exponentiated); eight compute warps read the
+// accumulators with tcgen05.ld and do the exponentials.  Every hand-over is
+// an mbarrier (TMA bytes, tcgen05.commit, or one arrive per compute warp), so
+// no block-wide barrier sits in the streaming loops.
+//  - rows (stats_tc): A = 128 query rows, B = key blocks 0..diagonal; TMEM
+//    lane = query row; each compute thread keeps an online max / sum over
+//    half of its row's columns.
+//  - output (out_tc): with lse known, P = exp2(s - lse) needs no rescaling;
+//    the compute warps write P as fp16 into a K-major tile and the tensor
+//    core accumulates O += P V in TMEM (V as stored, [key][d], is the
+//    MN-major B operand).
+//  - columns (colsum_tc): A = 128 keys, B = query blocks from the diagonal
+//    down, i.e. the transposed logits; TMEM lane = key, so each thread sums
+//    the probabilities its key receives with no cross-thread reduction
+//    (float32 within a block, float64 across blocks: fixed order).
+// Every wait is bounded; on a timeout the role stops, sets a device error
+// bit, and the CTA still drains its copies and MMAs and frees its TMEM.
+#include <cuda.h>  // CUtensorMap and the encoder's argument types (the encoder is looked up at run time)
 #include <cuda_fp16.h>
+
+#include <mutex>
 
 #include "h2o_internal.cuh"
 #include "ptx.cuh"
@@ -29,40 +43,11 @@ namespace h2o {
 namespace {
 
 constexpr float kNeg = -3.0e38f;
-constexpr uint32_t kWaitLimit = 200000u;  // polls of <= 1 us: waits on this CTA's own MMAs
-constexpr int NT = 256;                    // 8 warps: 4 TMEM lane quarters x 2 column halves
+constexpr uint32_t kWaitLimit = 200000u;  // polls of <= 1 us: waits on this CTA's own copies and MMAs
 constexpr int BLK = 128;                   // rows / columns of a logits block
-constexpr uint32_t kTmemCols = 256;        // two 128-column fp32 accumulators
-constexpr size_t kMinSmem = 100 * 1024;    // at most two CTAs per SM: 2 x 256 TMEM columns fit
-
-template <int D>
-struct TcCfg {
-  static constexpr int TILE = BLK * D * 2;                  // one operand tile (bytes)
-  static constexpr int KB = BLK * 128;                      // bytes of one 64-element K block
-  static constexpr size_t tiles = 3 * static_cast<size_t>(TILE);  // fixed operand + 2 stages
-  static constexpr size_t lse = tiles;                      // [3][128] floats
-  static constexpr size_t bars = lse + 3 * BLK * 4;         // 2 mbarriers
-  static constexpr size_t tslot = bars + 16;                // TMEM base address
-  static constexpr size_t red = (tslot + 16 + 15) / 16 * 16;  // [128] doubles / float pairs
-  static constexpr size_t used = red + BLK * 8 * 2;
-  // + 1 KB so the operand tiles can start on a 1024-byte boundary
-  static constexpr size_t bytes = (used > kMinSmem ? used : kMinSmem) + 1024;
-};
-
-// 128 rows (row0..) of a [L, D] fp16 matrix into a K-major 128-byte-swizzled
-// tile: 64-element K block kb at tile + kb * 16 KB, row r at + r * 128 B,
-// 16-byte chunk c at chunk c ^ (r % 8).  Rows >= L are zero-filled.
-template <int D>
-__device__ __forceinline__ void load_tile(unsigned char* tile, const __half* src, int row0, int L, int tid) {
-  constexpr int CPR = D / 8;  // 16-byte chunks per row
-  for (int c = tid; c < BLK * CPR; c += NT) {
-    const int r = c / CPR, ch = c % CPR;
-    const int gr = row0 + r;
-    const bool ok = gr < L;
-    unsigned char* dst = tile + (ch >> 3) * TcCfg<D>::KB + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-    cp_async16(dst, src + static_cast<size_t>(ok ? gr : 0) * D + ch * 8, ok);
-  }
-}
+constexpr int NCOMP = 8;                   // compute warps: 4 TMEM lane quarters x 2 column halves
+constexpr int NT = (2 + NCOMP) * 32;       // + the TMA warp and the MMA warp
+constexpr int kCompBar = 1;                // named barrier of the compute warps
 
 // Log2-domain lse of query row row0 + t; rows past the prompt get a huge
 // value so that their probabilities exp2(s - lse) vanish without a mask.  A
@@ -72,105 +57,511 @@ __device__ __forceinline__ float lse_at(const float* src, int row0, int t, int L
   return row0 + t < L ? src[row0 + t] : kHugeLse;
 }
 
-// D[tmem] = A[128 x D] * B[128 x D]^T over the head dimension.
+// Kernel arguments: the pointers and sizes plus a tensor map per input.
+struct TcArgs {
+  CUtensorMap q, k, v;  // [P, L, D] fp16, box 64 x 128 x 1, 128-byte swizzle
+  PrefillParams prm;
+};
+
+template <int D>
+struct Tile {
+  static constexpr int BYTES = BLK * D * 2;  // a 128-row operand tile
+  static constexpr int KB = BLK * 128;       // bytes of one 64-element K block of it
+};
+
+// 128 rows (row0..) of one pair's [L, D] matrix into a K-major tile: K block
+// kb (64 elements) at tile + kb * 16 KB, row r at + r * 128 B, 16-byte chunk
+// c at chunk c ^ (r % 8) (the TMA 128-byte swizzle; the tile is 1024-byte
+// aligned).  Issued by one thread; completes Tile<D>::BYTES on `bar`.
+template <int D>
+__device__ __forceinline__ void tma_tile(unsigned char* tile, const CUtensorMap* map, int row0, int pair,
+                                         uint64_t* bar) {
+#pragma unroll
+  for (int kb = 0; kb < D / 64; ++kb) tc::tma_load_3d(tile + kb * Tile<D>::KB, map, kb * 64, row0, pair, bar);
+}
+
+// D[tmem] = A[128 x D] * B[128 x D]^T over the head dimension (both K-major).
 template <int D>
 __device__ __forceinline__ void issue_block(uint32_t d_tmem, const unsigned char* a, const unsigned char* b) {
   constexpr uint32_t idesc = tc::idesc_f16_f32(BLK, BLK);
   const uint32_t sa = smem_u32(a), sb = smem_u32(b);
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
-    const uint32_t off = static_cast<uint32_t>((ks >> 2) * TcCfg<D>::KB + (ks & 3) * 32);
+    const uint32_t off = static_cast<uint32_t>((ks >> 2) * Tile<D>::KB + (ks & 3) * 32);
     tc::mma_f16(d_tmem, tc::desc_k_sw128(sa + off), tc::desc_k_sw128(sb + off), idesc, ks > 0);
   }
 }
 
-// ---------------------------------------------------------------- column sums
-// The 128-byte swizzle is a function of address bits 4..9, so the operand
-// tiles start on a 1024-byte boundary of the shared window.
+// D[tmem] (+)= P[128 x 128 keys] * V[128 keys x D]; P K-major, V MN-major
+// (the head dimension contiguous, 64-element atoms 16 KB apart).
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, const unsigned char* p, const unsigned char* v, bool acc) {
+  constexpr uint32_t idesc = tc::idesc_f16_f32_bmn(BLK, D);
+  const uint32_t sp = smem_u32(p), sv = smem_u32(v);
+#pragma unroll
+  for (int ks = 0; ks < BLK / 16; ++ks) {
+    const uint32_t aoff = static_cast<uint32_t>((ks >> 2) * (BLK * 128) + (ks & 3) * 32);
+    tc::mma_f16(d_tmem, tc::desc_k_sw128(sp + aoff), tc::desc_mn_sw128(sv + ks * 2048u, BLK * 128), idesc,
+                acc || ks > 0);
+  }
+}
+
+// The swizzle is a function of address bits 4..9, so operand tiles start on
+// a 1024-byte boundary of the shared window.
 __device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
   return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
 }
 
-template <int D>
-__global__ void __launch_bounds__(NT, 2) colsum_tc(const PrefillParams prm) {
-  using Cfg = TcCfg<D>;
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* smem = align1024(smem_raw);
-  unsigned char* sK = smem;
-  unsigned char* sQ0 = smem + Cfg::TILE;
-  float* sL = reinterpret_cast<float*>(smem + Cfg::lse);
-  uint64_t* mb = reinterpret_cast<uint64_t*>(smem + Cfg::bars);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Cfg::tslot);
-  double* red = reinterpret_cast<double*>(smem + Cfg::red);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int L = prm.L, pair = blockIdx.y, kb = blockIdx.x;
-  const size_t base = static_cast<size_t>(pair) * L * D;
-  const __half* Q = static_cast<const __half*>(prm.q) + base;
-  const __half* K = static_cast<const __half*>(prm.k) + base;
-  const float* lse2 = prm.lse2 + static_cast<size_t>(pair) * L;
-  const int n = (L + BLK - 1) / BLK - kb;  // query blocks from the diagonal down
+// Bounded wait by one thread; a timeout latches the error bit.
+__device__ __forceinline__ bool wait1(uint64_t* bar, uint32_t parity, int* err) {
+  if (mbar_wait_bounded(bar, parity, kWaitLimit)) return true;
+  if (err) atomicOr(err, ERR_MMA_TIMEOUT);
+  return false;
+}
+// Bounded wait by a whole warp; the result is warp-uniform, so the
+// .sync.aligned TMEM loads that follow never diverge.
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, int lane, int* err) {
+  const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, kWaitLimit));
+  if (!ok && lane == 0 && err) atomicOr(err, ERR_MMA_TIMEOUT);
+  return ok;
+}
 
-  griddep_wait();
-  if (warp == 0) tc::tmem_alloc(tslot, kTmemCols);
-  if (tid == 0) {
-    mbar_init(&mb[0], 1);
-    mbar_init(&mb[1], 1);
-    fence_mbar_init();
+// A ring of N operand stages fed by TMA: use number u goes to stage u % N.
+template <int N>
+struct Ring {
+  uint64_t* full;   // [N] producer -> consumer (TMA bytes)
+  uint64_t* empty;  // [N] consumer -> producer
+  // producer: wait until stage u % N is free again (its previous use released)
+  __device__ bool acquire(int u, int* err) const {
+    return u < N || wait1(&empty[u % N], static_cast<uint32_t>((u / N - 1) & 1), err);
   }
-  load_tile<D>(sK, K, kb * BLK, L, tid);
-  load_tile<D>(sQ0, Q, kb * BLK, L, tid);
-  if (n > 1) load_tile<D>(sQ0 + Cfg::TILE, Q, (kb + 1) * BLK, L, tid);
-  if (tid < BLK) {
-    sL[tid] = lse_at(lse2, kb * BLK, tid, L);
-    sL[BLK + tid] = lse_at(lse2, (kb + 1) * BLK, tid, L);
+  __device__ uint64_t* full_of(int u) const { return &full[u % N]; }
+  __device__ static uint32_t parity(int u) { return static_cast<uint32_t>((u / N) & 1); }
+  // producer, at exit: every issued copy has landed (uses 0..issued-1)
+  __device__ void drain(int issued, int* err) const {
+    for (int u = issued - N > 0 ? issued - N : 0; u < issued; ++u) wait1(&full[u % N], parity(u), err);
   }
-  cp_async_commit();
-  cp_async_wait<0>();
-  fence_proxy_async_smem();
+};
+
+// Teardown: the MMA lane waits for all its MMAs, every thread meets, and
+// warp 1 (which allocated them) frees the TMEM columns.
+__device__ __forceinline__ void tmem_teardown(int warp, int lane, uint64_t* drain, uint32_t tbase, uint32_t cols,
+                                              int* err) {
+  if (warp == 1 && lane == 0) {
+    tc::mma_commit(drain);
+    wait1(drain, 0, err);
+  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tbase = *tslot;
-  if (tid == 0) {
-    issue_block<D>(tbase, sK, sQ0);
-    tc::mma_commit(&mb[0]);
-    if (n > 1) {
-      issue_block<D>(tbase + BLK, sK, sQ0 + Cfg::TILE);
-      tc::mma_commit(&mb[1]);
-    }
+  if (warp == 1) tc::tmem_free(tbase, cols);
+}
+
+// Set-up shared by the kernels: barrier init by one thread, TMEM allocation
+// by warp 1, and the allocation's address published to every thread.
+__device__ __forceinline__ uint32_t setup(int warp, uint64_t* bars, const uint32_t* counts, int nbars,
+                                          uint32_t* tslot, uint32_t cols) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nbars; ++i) mbar_init(&bars[i], counts[i]);
+    fence_mbar_init();
   }
-  const int quarter = warp & 3, half = warp >> 2;
-  const int key = kb * BLK + quarter * 32 + lane;  // this thread's TMEM lane
-  const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
-  double dacc = 0.0;
-  bool ok = true;
-  int waited = 0;  // MMAs known complete
-  for (int i = 0; i < n; ++i) {
-    const int b = i & 1, qb = kb + i;  // query block of this iteration
-    if (ok) {  // warp-uniform, so the .sync.aligned TMEM loads below never diverge
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&mb[b], static_cast<uint32_t>((i >> 1) & 1), kWaitLimit));
-      if (!ok && lane == 0 && prm.err) atomicOr(prm.err, ERR_MMA_TIMEOUT);
+  if (warp == 1) tc::tmem_alloc(tslot, cols);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  return *tslot;
+}
+
+// ------------------------------------------------------- row log-sum-exp
+template <int D>
+struct StatsCfg {
+  static constexpr int NS = 2;  // key stages
+  static constexpr size_t q = 0, k = Tile<D>::BYTES;
+  static constexpr size_t bars = k + NS * static_cast<size_t>(Tile<D>::BYTES);
+  static constexpr int NB = 10;  // qfull, kfull[2], kempty[2], sfull[2], sempty[2], drain
+  static constexpr size_t tslot = bars + 8 * NB;
+  static constexpr size_t red = (tslot + 16 + 15) / 16 * 16;  // [128] (m, l) of the upper column half
+  static constexpr size_t bytes = red + BLK * 8 + 1024;       // + alignment slack
+};
+
+template <int D>
+__global__ void __launch_bounds__(NT, 2) stats_tc(const __grid_constant__ TcArgs a) {
+  using Cfg = StatsCfg<D>;
+  constexpr int NS = Cfg::NS, TB = Tile<D>::BYTES;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = align1024(smem_raw);
+  unsigned char* sQ = smem + Cfg::q;
+  unsigned char* sK = smem + Cfg::k;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::bars);
+  uint64_t* qfull = bars;
+  const Ring<NS> kr{bars + 1, bars + 3};
+  uint64_t* sfull = bars + 5;
+  uint64_t* sempty = bars + 7;
+  uint64_t* drain = bars + 9;
+  float2* red = reinterpret_cast<float2*>(smem + Cfg::red);
+  const PrefillParams& prm = a.prm;
+  int* err = prm.err;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int L = prm.L, pair = blockIdx.y;
+  const int qb = gridDim.x - 1 - blockIdx.x;  // longest rows first
+  const int n = qb + 1;                      // key blocks 0..qb (causal)
+  const uint32_t counts[Cfg::NB] = {1, 1, 1, 1, 1, 1, 1, NCOMP, NCOMP, 1};
+
+  if (threadIdx.x == 0) {
+    tc::prefetch_tensormap(&a.q);
+    tc::prefetch_tensormap(&a.k);
+  }
+  griddep_wait();
+  const uint32_t tbase = setup(warp, bars, counts, Cfg::NB, reinterpret_cast<uint32_t*>(smem + Cfg::tslot), 256);
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer
+      mbar_arrive_expect_tx(qfull, TB);
+      tma_tile<D>(sQ, &a.q, qb * BLK, pair, qfull);
+      int u = 0;
+      for (; u < n && kr.acquire(u, err); ++u) {
+        mbar_arrive_expect_tx(kr.full_of(u), TB);
+        tma_tile<D>(sK + (u % NS) * TB, &a.k, u * BLK, pair, kr.full_of(u));
+      }
+      kr.drain(u, err);
+      wait1(qfull, 0, err);
     }
-    if (ok) waited = i + 1;
-    tc::fence_after_sync();
-    // the tensor core is done with stage b: bring in query block i + 2
-    // (its lse row is loaded now and stored after the exponentials)
-    float next_lse = kHugeLse;
-    if (i + 2 < n) {
-      load_tile<D>(sQ0 + b * Cfg::TILE, Q, (qb + 2) * BLK, L, tid);
-      if (tid < BLK) next_lse = lse_at(lse2, (qb + 2) * BLK, tid, L);
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      bool ok = wait1(qfull, 0, err);
+      for (int j = 0; ok && j < n; ++j) {
+        const int b = j & 1;
+        ok = wait1(kr.full_of(j), kr.parity(j), err) &&
+             (j < 2 || wait1(&sempty[b], static_cast<uint32_t>(((j - 2) >> 1) & 1), err));
+        if (!ok) break;
+        tc::fence_after_sync();
+        issue_block<D>(tbase + b * BLK, sQ, sK + (j % NS) * TB);
+        tc::mma_commit(&sfull[b]);
+        tc::mma_commit(&kr.empty[j % NS]);
+      }
     }
-    cp_async_commit();
-    float acc0 = 0.f, acc1 = 0.f;
-    const float* lse = sL + (i % 3) * BLK;
-    if (ok) {
-      const int kl = quarter * 32 + lane;  // key within the block
+    __syncwarp();
+  } else {  // compute warps
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
+    const int rl = quarter * 32 + lane, row = qb * BLK + rl;  // TMEM lane = query row
+    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+    float m = kNeg, l = 0.f;
+    for (int j = 0; j < n; ++j) {
+      const int b = j & 1;
+      if (!wait_warp(&sfull[b], static_cast<uint32_t>((j >> 1) & 1), lane, err)) break;
+      tc::fence_after_sync();
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        float v[32];
         const int col0 = half * 64 + c * 32;
+        float v[32];
         tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + col0), v);
-        const float4* l4 = reinterpret_cast<const float4*>(lse + col0);
+        if (j == qb) {  // diagonal block: key col0 + e is visible to row rl if it is <= rl
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = col0 + e <= rl ? v[e] : -INFINITY;
+        }
+        // the max of the raw logits (scale > 0 commutes with max)
+        float c0 = v[0], c1 = v[1];
+#pragma unroll
+        for (int e = 2; e < 32; e += 2) {
+          c0 = fmaxf(c0, v[e]);
+          c1 = fmaxf(c1, v[e + 1]);
+        }
+        const float mn = fmaxf(m, fmaxf(c0, c1) * prm.qscale);
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          s0 += ex2(fmaf(v[e], prm.qscale, -mn));
+          s1 += ex2(fmaf(v[e + 1], prm.qscale, -mn));
+        }
+        l = l * ex2(m - mn) + (s0 + s1);
+        m = mn;
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_plain(&sempty[b]);  // accumulator b may be overwritten
+    }
+    // merge the two column halves of each row
+    if (half == 1) red[rl] = make_float2(m, l);
+    tc::named_sync(kCompBar, NCOMP * 32);
+    if (half == 0 && row < L) {
+      const float2 o = red[rl];
+      const float M = fmaxf(m, o.x);
+      prm.lse2[static_cast<size_t>(pair) * L + row] = M + log2f(l * ex2(m - M) + o.y * ex2(o.x - M));
+    }
+    griddep_launch();
+  }
+  tmem_teardown(warp, lane, drain, tbase, 256, err);
+}
+
+// ------------------------------------------------------- attention output
+template <int D>
+struct OutCfg {
+  static constexpr int NK = 2, NV = 2;  // key / value stages
+  static constexpr int PT = BLK * BLK * 2;  // fp16 probabilities of one block
+  static constexpr size_t q = 0, k = Tile<D>::BYTES;
+  static constexpr size_t v = k + NK * static_cast<size_t>(Tile<D>::BYTES);
+  static constexpr size_t p = v + NV * static_cast<size_t>(Tile<D>::BYTES);  // 2 probability tiles
+  static constexpr size_t bars = p + 2 * static_cast<size_t>(PT);
+  // qfull, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], pfull[2], pempty[2], ofull, drain
+  static constexpr int NB = 17;
+  static constexpr size_t tslot = bars + 8 * NB;
+  static constexpr size_t bytes = tslot + 16 + 1024;
+};
+constexpr uint32_t kOutTmemCols = 512;  // two 128-column logit blocks + O (D <= 128 columns)
+
+template <int D>
+__global__ void __launch_bounds__(NT, 1) out_tc(const __grid_constant__ TcArgs a) {
+  using Cfg = OutCfg<D>;
+  constexpr int NK = Cfg::NK, NV = Cfg::NV, TB = Tile<D>::BYTES, PT = Cfg::PT;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = align1024(smem_raw);
+  unsigned char* sQ = smem + Cfg::q;
+  unsigned char* sK = smem + Cfg::k;
+  unsigned char* sV = smem + Cfg::v;
+  unsigned char* sP = smem + Cfg::p;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::bars);
+  uint64_t* qfull = bars;
+  const Ring<NK> kr{bars + 1, bars + 3};
+  const Ring<NV> vr{bars + 5, bars + 7};
+  uint64_t* sfull = bars + 9;
+  uint64_t* pfull = bars + 11;
+  uint64_t* pempty = bars + 13;
+  uint64_t* ofull = bars + 15;
+  uint64_t* drain = bars + 16;
+  const PrefillParams& prm = a.prm;
+  int* err = prm.err;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int L = prm.L, pair = blockIdx.y;
+  const int qb = gridDim.x - 1 - blockIdx.x;  // longest rows first
+  const int n = qb + 1;
+  const uint32_t counts[Cfg::NB] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, NCOMP, NCOMP, 1, 1, 1, 1};
+
+  if (threadIdx.x == 0) {
+    tc::prefetch_tensormap(&a.q);
+    tc::prefetch_tensormap(&a.k);
+    tc::prefetch_tensormap(&a.v);
+  }
+  griddep_wait();
+  const uint32_t tbase =
+      setup(warp, bars, counts, Cfg::NB, reinterpret_cast<uint32_t*>(smem + Cfg::tslot), kOutTmemCols);
+  const uint32_t o_tmem = tbase + 2 * BLK;
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer, in the order the MMAs consume: K0 K1 V0 K2 V1 K3 ...
+      mbar_arrive_expect_tx(qfull, TB);
+      tma_tile<D>(sQ, &a.q, qb * BLK, pair, qfull);
+      int uk = 0, uv = 0;
+      auto issue_k = [&](int j) {
+        if (!kr.acquire(j, err)) return false;
+        mbar_arrive_expect_tx(kr.full_of(j), TB);
+        tma_tile<D>(sK + (j % NK) * TB, &a.k, j * BLK, pair, kr.full_of(j));
+        uk = j + 1;
+        return true;
+      };
+      auto issue_v = [&](int j) {
+        if (!vr.acquire(j, err)) return false;
+        mbar_arrive_expect_tx(vr.full_of(j), TB);
+        tma_tile<D>(sV + (j % NV) * TB, &a.v, j * BLK, pair, vr.full_of(j));
+        uv = j + 1;
+        return true;
+      };
+      bool ok = issue_k(0) && (n < 2 || issue_k(1));
+      for (int j = 0; ok && j < n; ++j) ok = issue_v(j) && (j + 2 >= n || issue_k(j + 2));
+      kr.drain(uk, err);
+      vr.drain(uv, err);
+      wait1(qfull, 0, err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer: S0 S1 O0 S2 O1 S3 ...
+      bool ok = wait1(qfull, 0, err);
+      for (int j = 0; ok && j < 2 && j < n; ++j) {
+        ok = wait1(kr.full_of(j), kr.parity(j), err);
+        if (!ok) break;
+        tc::fence_after_sync();
+        issue_block<D>(tbase + j * BLK, sQ, sK + (j % NK) * TB);
+        tc::mma_commit(&sfull[j]);
+        tc::mma_commit(&kr.empty[j % NK]);
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        const int b = j & 1;
+        ok = wait1(&pfull[b], static_cast<uint32_t>((j >> 1) & 1), err) && wait1(vr.full_of(j), vr.parity(j), err);
+        if (!ok) break;
+        tc::fence_after_sync();
+        issue_pv<D>(o_tmem, sP + b * PT, sV + (j % NV) * TB, j > 0);
+        tc::mma_commit(&pempty[b]);
+        tc::mma_commit(&vr.empty[j % NV]);
+        if (j + 2 < n) {  // the compute warps are done with accumulator b (they have written P(j))
+          ok = wait1(kr.full_of(j + 2), kr.parity(j + 2), err);
+          if (!ok) break;
+          issue_block<D>(tbase + b * BLK, sQ, sK + ((j + 2) % NK) * TB);
+          tc::mma_commit(&sfull[b]);
+          tc::mma_commit(&kr.empty[(j + 2) % NK]);
+        }
+      }
+      if (ok) tc::mma_commit(ofull);
+    }
+    __syncwarp();
+  } else {  // compute warps
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
+    const int rl = quarter * 32 + lane, row = qb * BLK + rl;
+    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float lse = lse_at(prm.lse2 + static_cast<size_t>(pair) * L, qb * BLK, rl, L);
+    bool ok = true;
+    for (int j = 0; ok && j < n; ++j) {
+      const int b = j & 1;
+      ok = wait_warp(&sfull[b], static_cast<uint32_t>((j >> 1) & 1), lane, err);
+      if (!ok) break;
+      tc::fence_after_sync();
+      uint32_t ph[32];  // this thread's 64 probabilities as fp16 pairs
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int col0 = half * 64 + c * 32;
+        float v[32];
+        tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + col0), v);
+        if (j == qb) {  // diagonal block: key col0 + e is visible to row rl if it is <= rl
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = col0 + 2 * e <= rl ? ex2(fmaf(v[2 * e], prm.qscale, -lse)) : 0.f;
+            const float p1 = col0 + 2 * e + 1 <= rl ? ex2(fmaf(v[2 * e + 1], prm.qscale, -lse)) : 0.f;
+            ph[c * 16 + e] = tc::cvt_half2(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            ph[c * 16 + e] =
+                tc::cvt_half2(ex2(fmaf(v[2 * e], prm.qscale, -lse)), ex2(fmaf(v[2 * e + 1], prm.qscale, -lse)));
+        }
+      }
+      // probability tile b was last read by O(j-2)
+      if (j >= 2 && !(ok = wait_warp(&pempty[b], static_cast<uint32_t>(((j - 2) >> 1) & 1), lane, err))) break;
+      unsigned char* prow = sP + b * PT + half * (BLK * 128) + rl * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(prow + ((c ^ (rl & 7)) << 4)) =
+            make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
+      fence_proxy_async_smem();  // the tensor core reads what the threads wrote
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_plain(&pfull[b]);
+    }
+    ok = ok && wait_warp(ofull, 0, lane, err);
+    tc::fence_after_sync();
+    if (ok) {
+      float* dst = prm.out + (static_cast<size_t>(pair) * L + row) * D + half * (D / 2);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        float o[32];
+        tc::tmem_ld32(o_tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                          static_cast<uint32_t>(half * (D / 2) + c * 32),
+                      o);
+        if (row < L) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            reinterpret_cast<float4*>(dst + c * 32)[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+        }
+      }
+    }
+    griddep_launch();
+  }
+  tmem_teardown(warp, lane, drain, tbase, kOutTmemCols, err);
+}
+
+// ------------------------------------------------------------ column sums
+template <int D>
+struct ColCfg {
+  static constexpr int NS = 2;  // query stages
+  static constexpr size_t k = 0, q = Tile<D>::BYTES;
+  static constexpr size_t lse = q + NS * static_cast<size_t>(Tile<D>::BYTES);  // [NCOMP][2][64] floats
+  static constexpr size_t bars = lse + NCOMP * 2 * 64 * 4;
+  static constexpr int NB = 10;  // kfull, qfull[2], qempty[2], sfull[2], sempty[2], drain
+  static constexpr size_t tslot = bars + 8 * NB;
+  static constexpr size_t red = (tslot + 16 + 15) / 16 * 16;  // [128] doubles of the upper column half
+  static constexpr size_t bytes = red + BLK * 8 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(NT, 2) colsum_tc(const __grid_constant__ TcArgs a) {
+  using Cfg = ColCfg<D>;
+  constexpr int NS = Cfg::NS, TB = Tile<D>::BYTES;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = align1024(smem_raw);
+  unsigned char* sK = smem + Cfg::k;
+  unsigned char* sQ = smem + Cfg::q;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::bars);
+  uint64_t* kfull = bars;
+  const Ring<NS> qr{bars + 1, bars + 3};
+  uint64_t* sfull = bars + 5;
+  uint64_t* sempty = bars + 7;
+  uint64_t* drain = bars + 9;
+  double* red = reinterpret_cast<double*>(smem + Cfg::red);
+  const PrefillParams& prm = a.prm;
+  int* err = prm.err;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int L = prm.L, pair = blockIdx.y, kb = blockIdx.x;
+  const int n = (L + BLK - 1) / BLK - kb;  // query blocks from the diagonal down
+  const uint32_t counts[Cfg::NB] = {1, 1, 1, 1, 1, 1, 1, NCOMP, NCOMP, 1};
+
+  if (threadIdx.x == 0) {
+    tc::prefetch_tensormap(&a.q);
+    tc::prefetch_tensormap(&a.k);
+  }
+  griddep_wait();
+  const uint32_t tbase = setup(warp, bars, counts, Cfg::NB, reinterpret_cast<uint32_t*>(smem + Cfg::tslot), 256);
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer
+      mbar_arrive_expect_tx(kfull, TB);
+      tma_tile<D>(sK, &a.k, kb * BLK, pair, kfull);
+      int u = 0;
+      for (; u < n && qr.acquire(u, err); ++u) {
+        mbar_arrive_expect_tx(qr.full_of(u), TB);
+        tma_tile<D>(sQ + (u % NS) * TB, &a.q, (kb + u) * BLK, pair, qr.full_of(u));
+      }
+      qr.drain(u, err);
+      wait1(kfull, 0, err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer: S^T(i) = K Q_i^T
+      bool ok = wait1(kfull, 0, err);
+      for (int i = 0; ok && i < n; ++i) {
+        const int b = i & 1;
+        ok = wait1(qr.full_of(i), qr.parity(i), err) &&
+             (i < 2 || wait1(&sempty[b], static_cast<uint32_t>(((i - 2) >> 1) & 1), err));
+        if (!ok) break;
+        tc::fence_after_sync();
+        issue_block<D>(tbase + b * BLK, sK, sQ + (i % NS) * TB);
+        tc::mma_commit(&sfull[b]);
+        tc::mma_commit(&qr.empty[i % NS]);
+      }
+    }
+    __syncwarp();
+  } else {  // compute warps
+    const int cw = warp - 2, quarter = warp & 3, half = cw >> 2;
+    const int kl = quarter * 32 + lane, key = kb * BLK + kl;  // TMEM lane = key
+    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+    // this warp's 64 query columns' lse values, one block ahead: lane t
+    // fetches columns 2t, 2t + 1 of the next block while this one is worked on
+    const float* lse2 = prm.lse2 + static_cast<size_t>(pair) * L;
+    float* wl = reinterpret_cast<float*>(smem + Cfg::lse) + cw * 128;  // [2][64]
+    const int c0 = half * 64 + 2 * lane;
+    wl[2 * lane] = lse_at(lse2, kb * BLK, c0, L);
+    wl[2 * lane + 1] = lse_at(lse2, kb * BLK, c0 + 1, L);
+    __syncwarp();
+    double dacc = 0.0;
+    for (int i = 0; i < n; ++i) {
+      const int b = i & 1;
+      float n0 = kHugeLse, n1 = kHugeLse;
+      if (i + 1 < n) {
+        n0 = lse_at(lse2, (kb + i + 1) * BLK, c0, L);
+        n1 = lse_at(lse2, (kb + i + 1) * BLK, c0 + 1, L);
+      }
+      if (!wait_warp(&sfull[b], static_cast<uint32_t>((i >> 1) & 1), lane, err)) break;
+      tc::fence_after_sync();
+      const float* lse = wl + b * 64;
+      float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int col0 = half * 64 + c * 32;
+        float v[32];
+        tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + col0), v);
+        const float4* l4 = reinterpret_cast<const float4*>(lse + c * 32);
         if (i == 0) {  // diagonal block: query col0 + e sees key kl only if kl <= col0 + e
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -193,325 +584,59 @@ __global__ void __launch_bounds__(NT, 2) colsum_tc(const PrefillParams prm) {
           }
         }
       }
+      dacc += static_cast<double>(acc0 + acc1);
+      tc::fence_before_sync();
+      __syncwarp();  // also: every lane is done with lse slot b
+      if (lane == 0) tc::mbar_arrive_plain(&sempty[b]);  // accumulator b may be overwritten
+      wl[(b ^ 1) * 64 + 2 * lane] = n0;
+      wl[(b ^ 1) * 64 + 2 * lane + 1] = n1;
+      __syncwarp();
     }
-    const float acc = acc0 + acc1;
-    dacc += static_cast<double>(acc);
-    if (i + 2 < n && tid < BLK) sL[((i + 2) % 3) * BLK + tid] = next_lse;
-    tc::fence_before_sync();
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    __syncthreads();  // accumulator b is read; query block i + 2 is in stage b
-    tc::fence_after_sync();
-    if (tid == 0 && ok && i + 2 < n) {
-      issue_block<D>(tbase + b * BLK, sK, sQ0 + b * Cfg::TILE);
-      tc::mma_commit(&mb[b]);
-    }
+    if (half == 1) red[kl] = dacc;
+    tc::named_sync(kCompBar, NCOMP * 32);
+    if (half == 0 && key < L) prm.colsum[static_cast<size_t>(pair) * L + key] = static_cast<float>(dacc + red[kl]);
+    griddep_launch();
   }
-  griddep_launch();
-  // after a timed-out wait, give the MMAs still in flight a bounded chance to
-  // finish before the accumulators are freed
-  if (tid == 0 && !ok) {
-    const int issued = n < 2 ? n : min(n, waited + 2);
-    for (int i = waited; i < issued; ++i) mbar_wait_bounded(&mb[i & 1], static_cast<uint32_t>((i >> 1) & 1), kWaitLimit);
-  }
-  if (half == 1) red[quarter * 32 + lane] = dacc;
-  tc::fence_before_sync();
-  __syncthreads();
-  if (half == 0 && key < L)
-    prm.colsum[static_cast<size_t>(pair) * L + key] = static_cast<float>(dacc + red[quarter * 32 + lane]);
-  __syncwarp();
-  if (warp == 0) tc::tmem_free(tbase, kTmemCols);
+  tmem_teardown(warp, lane, drain, tbase, 256, err);
 }
 
-// ------------------------------------------------------- row log-sum-exp only
-template <int D>
-__global__ void __launch_bounds__(NT, 2) stats_tc(const PrefillParams prm) {
-  using Cfg = TcCfg<D>;
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* smem = align1024(smem_raw);
-  unsigned char* sQ = smem;
-  unsigned char* sK0 = smem + Cfg::TILE;
-  uint64_t* mb = reinterpret_cast<uint64_t*>(smem + Cfg::bars);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Cfg::tslot);
-  float* red = reinterpret_cast<float*>(smem + Cfg::red);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int L = prm.L, pair = blockIdx.y;
-  const int qb = gridDim.x - 1 - blockIdx.x;  // longest rows first
-  const size_t base = static_cast<size_t>(pair) * L * D;
-  const __half* Q = static_cast<const __half*>(prm.q) + base;
-  const __half* K = static_cast<const __half*>(prm.k) + base;
-  const int n = qb + 1;  // key blocks 0..qb (causal)
+// ------------------------------------------------------------------ host
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-  griddep_wait();
-  if (warp == 0) tc::tmem_alloc(tslot, kTmemCols);
-  if (tid == 0) {
-    mbar_init(&mb[0], 1);
-    mbar_init(&mb[1], 1);
-    fence_mbar_init();
-  }
-  load_tile<D>(sQ, Q, qb * BLK, L, tid);
-  load_tile<D>(sK0, K, 0, L, tid);
-  if (n > 1) load_tile<D>(sK0 + Cfg::TILE, K, BLK, L, tid);
-  cp_async_commit();
-  cp_async_wait<0>();
-  fence_proxy_async_smem();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tbase = *tslot;
-  if (tid == 0) {
-    issue_block<D>(tbase, sQ, sK0);
-    tc::mma_commit(&mb[0]);
-    if (n > 1) {
-      issue_block<D>(tbase + BLK, sQ, sK0 + Cfg::TILE);
-      tc::mma_commit(&mb[1]);
+// The driver's tensor-map encoder, looked up once through the runtime.
+EncodeTiled encoder() {
+  static const EncodeTiled fn = []() -> EncodeTiled {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return nullptr;
     }
-  }
-  const int quarter = warp & 3, half = warp >> 2;
-  const int row = qb * BLK + quarter * 32 + lane;  // this thread's query row (TMEM lane)
-  const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
-  float m = kNeg, l = 0.f;
-  bool ok = true;
-  int waited = 0;
-  for (int i = 0; i < n; ++i) {
-    const int b = i & 1;
-    if (ok) {  // warp-uniform, so the .sync.aligned TMEM loads below never diverge
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&mb[b], static_cast<uint32_t>((i >> 1) & 1), kWaitLimit));
-      if (!ok && lane == 0 && prm.err) atomicOr(prm.err, ERR_MMA_TIMEOUT);
-    }
-    if (ok) waited = i + 1;
-    tc::fence_after_sync();
-    if (i + 2 < n) load_tile<D>(sK0 + b * Cfg::TILE, K, (i + 2) * BLK, L, tid);
-    cp_async_commit();
-    if (ok) {
-      float v[64];
-      tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + half * 64), *reinterpret_cast<float(*)[32]>(v));
-      tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + half * 64 + 32),
-                    *reinterpret_cast<float(*)[32]>(v + 32));
-      if (i == qb) {  // diagonal block: key half * 64 + e is visible to row rl if it is <= rl
-        const int rl = quarter * 32 + lane;
-#pragma unroll
-        for (int e = 0; e < 64; ++e) v[e] = half * 64 + e <= rl ? v[e] : -INFINITY;
-      }
-      // the max of the raw logits (scale > 0 commutes with max)
-      float c0 = v[0], c1 = v[1];
-#pragma unroll
-      for (int e = 2; e < 64; e += 2) {
-        c0 = fmaxf(c0, v[e]);
-        c1 = fmaxf(c1, v[e + 1]);
-      }
-      const float mn = fmaxf(m, fmaxf(c0, c1) * prm.qscale);
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-      for (int e = 0; e < 64; e += 2) {
-        s0 += ex2(fmaf(v[e], prm.qscale, -mn));
-        s1 += ex2(fmaf(v[e + 1], prm.qscale, -mn));
-      }
-      l = l * ex2(m - mn) + (s0 + s1);
-      m = mn;
-    }
-    tc::fence_before_sync();
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    __syncthreads();
-    tc::fence_after_sync();
-    if (tid == 0 && ok && i + 2 < n) {
-      issue_block<D>(tbase + b * BLK, sQ, sK0 + b * Cfg::TILE);
-      tc::mma_commit(&mb[b]);
-    }
-  }
-  griddep_launch();
-  if (tid == 0 && !ok) {
-    const int issued = n < 2 ? n : min(n, waited + 2);
-    for (int i = waited; i < issued; ++i) mbar_wait_bounded(&mb[i & 1], static_cast<uint32_t>((i >> 1) & 1), kWaitLimit);
-  }
-  if (half == 1) {
-    red[2 * (quarter * 32 + lane)] = m;
-    red[2 * (quarter * 32 + lane) + 1] = l;
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  if (half == 0 && row < L) {
-    const float m2 = red[2 * (quarter * 32 + lane)], l2 = red[2 * (quarter * 32 + lane) + 1];
-    const float M = fmaxf(m, m2);
-    prm.lse2[static_cast<size_t>(pair) * L + row] = M + log2f(l * ex2(m - M) + l2 * ex2(m2 - M));
-  }
-  __syncwarp();
-  if (warp == 0) tc::tmem_free(tbase, kTmemCols);
+    return reinterpret_cast<EncodeTiled>(p);
+  }();
+  return fn;
 }
 
-// ------------------------------------------------------- attention output O
-// With every row's lse known, O_i = sum_j exp2(s_ij - lse_i) v_j needs no
-// online rescaling: per key block, S = Q K^T goes to TMEM, the threads turn
-// it into fp16 probabilities in a K-major shared tile, and O += P V
-// accumulates in TMEM across all key blocks (V as stored, [key][d], is the
-// MN-major B operand: same swizzled byte layout as load_tile gives).
-template <int D>
-struct OutCfg {
-  static constexpr int TILE = BLK * D * 2;
-  static constexpr int PT = BLK * BLK * 2;  // fp16 probabilities of one block
-  static constexpr size_t k = TILE;                              // 2 key stages
-  static constexpr size_t v = 3 * static_cast<size_t>(TILE);     // 2 value stages
-  static constexpr size_t p = 5 * static_cast<size_t>(TILE);     // 2 probability tiles
-  static constexpr size_t bars = p + 2 * static_cast<size_t>(PT);  // S[2], O, drain
-  static constexpr size_t tslot = bars + 32;
-  static constexpr size_t bytes = tslot + 16 + 1024;
-};
-constexpr uint32_t kOutTmemCols = 512;  // two 128-column logit blocks + O (D <= 128 columns)
-
-// D[tmem] (+)= P[128 x 128 keys] * V[128 keys x D].
-template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, const unsigned char* p, const unsigned char* v, bool acc) {
-  constexpr uint32_t idesc = tc::idesc_f16_f32_bmn(BLK, D);
-  const uint32_t sp = smem_u32(p), sv = smem_u32(v);
-#pragma unroll
-  for (int ks = 0; ks < BLK / 16; ++ks) {
-    const uint32_t aoff = static_cast<uint32_t>((ks >> 2) * (BLK * 128) + (ks & 3) * 32);
-    tc::mma_f16(d_tmem, tc::desc_k_sw128(sp + aoff), tc::desc_mn_sw128(sv + ks * 2048u, BLK * 128), idesc,
-                acc || ks > 0);
-  }
-}
-
-__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int lane, int* err) {
-  const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, kWaitLimit));
-  if (!ok && lane == 0 && err) atomicOr(err, ERR_MMA_TIMEOUT);
-  return ok;
-}
-
-template <int D>
-__global__ void __launch_bounds__(NT, 1) out_tc(const PrefillParams prm) {
-  using Cfg = OutCfg<D>;
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* smem = align1024(smem_raw);
-  unsigned char* sQ = smem;
-  unsigned char* sK = smem + Cfg::k;
-  unsigned char* sV = smem + Cfg::v;
-  unsigned char* sP = smem + Cfg::p;
-  uint64_t* mbS = reinterpret_cast<uint64_t*>(smem + Cfg::bars);
-  uint64_t* mbO = mbS + 2;
-  uint64_t* mbD = mbS + 3;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Cfg::tslot);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int L = prm.L, pair = blockIdx.y;
-  const int qb = gridDim.x - 1 - blockIdx.x;  // longest rows first
-  const size_t base = static_cast<size_t>(pair) * L * D;
-  const __half* Q = static_cast<const __half*>(prm.q) + base;
-  const __half* K = static_cast<const __half*>(prm.k) + base;
-  const __half* V = static_cast<const __half*>(prm.v) + base;
-  const int n = qb + 1;
-  const int quarter = warp & 3, half = warp >> 2;
-  const int rl = quarter * 32 + lane, row = qb * BLK + rl;  // this thread's TMEM lane / query row
-
-  griddep_wait();
-  if (warp == 0) tc::tmem_alloc(tslot, kOutTmemCols);
-  if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(&mbS[i], 1);
-    fence_mbar_init();
-  }
-  const float lse = lse_at(prm.lse2 + static_cast<size_t>(pair) * L, qb * BLK, rl, L);
-  load_tile<D>(sQ, Q, qb * BLK, L, tid);
-  load_tile<D>(sK, K, 0, L, tid);
-  if (n > 1) load_tile<D>(sK + Cfg::TILE, K, BLK, L, tid);
-  load_tile<D>(sV, V, 0, L, tid);
-  cp_async_commit();
-  cp_async_wait<0>();
-  fence_proxy_async_smem();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tbase = *tslot;
-  const uint32_t o_tmem = tbase + 2 * BLK;
-  if (tid == 0) {
-    issue_block<D>(tbase, sQ, sK);
-    tc::mma_commit(&mbS[0]);
-    if (n > 1) {
-      issue_block<D>(tbase + BLK, sQ, sK + Cfg::TILE);
-      tc::mma_commit(&mbS[1]);
-    }
-  }
-  const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
-  bool ok = true;
-  for (int j = 0; j < n; ++j) {
-    const int b = j & 1;
-    if (ok) ok = wait_all(&mbS[b], static_cast<uint32_t>((j >> 1) & 1), lane, prm.err);
-    tc::fence_after_sync();
-    if (j + 2 < n) load_tile<D>(sK + b * Cfg::TILE, K, (j + 2) * BLK, L, tid);  // S(j) has read stage b
-    cp_async_commit();
-    uint32_t ph[32];  // this thread's 64 probabilities as fp16 pairs
-    if (ok) {
-      float v[64];
-      tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + half * 64), *reinterpret_cast<float(*)[32]>(v));
-      tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + half * 64 + 32),
-                    *reinterpret_cast<float(*)[32]>(v + 32));
-      if (j == qb) {  // diagonal block: key half * 64 + e is visible to row rl if it is <= rl
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float p0 = half * 64 + 2 * e <= rl ? ex2(fmaf(v[2 * e], prm.qscale, -lse)) : 0.f;
-          const float p1 = half * 64 + 2 * e + 1 <= rl ? ex2(fmaf(v[2 * e + 1], prm.qscale, -lse)) : 0.f;
-          ph[e] = tc::cvt_half2(p0, p1);
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          ph[e] = tc::cvt_half2(ex2(fmaf(v[2 * e], prm.qscale, -lse)), ex2(fmaf(v[2 * e + 1], prm.qscale, -lse)));
-      }
-    }
-    // O(j-1) complete: probability tile b (last read by O(j-2)) and value
-    // stage (j+1)%2 (read by O(j-1)) are free
-    if (ok && j >= 1) ok = wait_all(mbO, static_cast<uint32_t>((j - 1) & 1), lane, prm.err);
-    tc::fence_after_sync();
-    if (j + 1 < n) load_tile<D>(sV + ((j + 1) & 1) * Cfg::TILE, V, (j + 1) * BLK, L, tid);
-    cp_async_commit();
-    if (ok) {
-      unsigned char* prow = sP + b * Cfg::PT + half * (BLK * 128) + rl * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(prow + ((c ^ (rl & 7)) << 4)) = make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2],
-                                                                            ph[4 * c + 3]);
-    }
-    cp_async_wait<1>();  // all but the value block j + 1 just requested
-    fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();  // P(j) written, V(j) and K(j + 2) landed, S(j) read
-    tc::fence_after_sync();
-    if (tid == 0 && ok) {
-      issue_pv<D>(o_tmem, sP + b * Cfg::PT, sV + b * Cfg::TILE, j > 0);
-      tc::mma_commit(mbO);
-      if (j + 2 < n) {
-        issue_block<D>(tbase + b * BLK, sQ, sK + b * Cfg::TILE);
-        tc::mma_commit(&mbS[b]);
-      }
-    }
-  }
-  if (ok) ok = wait_all(mbO, static_cast<uint32_t>((n - 1) & 1), lane, prm.err);
-  tc::fence_after_sync();
-  griddep_launch();
-  if (ok) {
-    float* dst = prm.out + (static_cast<size_t>(pair) * L + row) * D + half * (D / 2);
-#pragma unroll
-    for (int c = 0; c < D / 64; ++c) {
-      float o[32];
-      tc::tmem_ld32(lane_addr + 2 * BLK + static_cast<uint32_t>(half * (D / 2) + c * 32), o);
-      if (row < L) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          reinterpret_cast<float4*>(dst + c * 32)[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
-      }
-    }
-  }
-  // every MMA this CTA issued has completed before its TMEM is freed
-  if (tid == 0) {
-    tc::mma_commit(mbD);
-    if (!mbar_wait_bounded(mbD, 0, kWaitLimit) && prm.err) atomicOr(prm.err, ERR_MMA_TIMEOUT);
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  if (warp == 0) tc::tmem_free(tbase, kOutTmemCols);
+// Tensor map of a [P, L, D] fp16 array (16-byte aligned): 64 x 128 x 1
+// boxes, 128-byte swizzle, zeros past the ends.
+bool encode_map(CUtensorMap* m, const void* base, int D, int L, int P) {
+  const EncodeTiled enc = encoder();
+  if (!enc || !base) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(P)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(L) * D * 2};
+  const cuuint32_t box[3] = {64, BLK, 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <typename Kern>
-cudaError_t launch_tc(Kern kern, dim3 grid, size_t smem, cudaStream_t s, const PrefillParams& prm) {
+cudaError_t launch_tc(Kern kern, dim3 grid, size_t smem, cudaStream_t s, const TcArgs& args) {
   cudaError_t e = kernel_attrs(reinterpret_cast<const void*>(kern), smem, false);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -524,28 +649,39 @@ cudaError_t launch_tc(Kern kern, dim3 grid, size_t smem, cudaStream_t s, const P
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, prm);
+  return cudaLaunchKernelEx(&cfg, kern, args);
+}
+
+bool make_args(TcArgs& a, const PrefillParams& prm, int D, int pairs, bool with_v) {
+  a = TcArgs{};
+  a.prm = prm;
+  return encode_map(&a.q, prm.q, D, prm.L, pairs) && encode_map(&a.k, prm.k, D, prm.L, pairs) &&
+         (!with_v || encode_map(&a.v, prm.v, D, prm.L, pairs));
 }
 
 }  // namespace
 
-cudaError_t launch_prefill_colsum_tc(const PrefillParams& prm, int D, int pairs, cudaStream_t s) {
-  if (prm.L <= 0) return cudaSuccess;
-  const dim3 grid((prm.L + BLK - 1) / BLK, pairs);
-  if (D == 128) return launch_tc(colsum_tc<128>, grid, TcCfg<128>::bytes, s, prm);
-  if (D == 64) return launch_tc(colsum_tc<64>, grid, TcCfg<64>::bytes, s, prm);
-  return cudaErrorInvalidValue;
-}
-
 cudaError_t launch_prefill_stats_tc(const PrefillParams& prm, int D, int pairs, cudaStream_t s) {
   if (prm.L <= 0) return cudaSuccess;
   if (D != 64 && D != 128) return cudaErrorInvalidValue;
+  TcArgs args;
+  if (!make_args(args, prm, D, pairs, prm.out != nullptr)) return cudaErrorInvalidValue;
   const dim3 grid((prm.L + BLK - 1) / BLK, pairs);
-  cudaError_t e = D == 128 ? launch_tc(stats_tc<128>, grid, TcCfg<128>::bytes, s, prm)
-                           : launch_tc(stats_tc<64>, grid, TcCfg<64>::bytes, s, prm);
+  cudaError_t e = D == 128 ? launch_tc(stats_tc<128>, grid, StatsCfg<128>::bytes, s, args)
+                           : launch_tc(stats_tc<64>, grid, StatsCfg<64>::bytes, s, args);
   if (e != cudaSuccess || prm.out == nullptr) return e;
-  return D == 128 ? launch_tc(out_tc<128>, grid, OutCfg<128>::bytes, s, prm)
-                  : launch_tc(out_tc<64>, grid, OutCfg<64>::bytes, s, prm);
+  return D == 128 ? launch_tc(out_tc<128>, grid, OutCfg<128>::bytes, s, args)
+                  : launch_tc(out_tc<64>, grid, OutCfg<64>::bytes, s, args);
+}
+
+cudaError_t launch_prefill_colsum_tc(const PrefillParams& prm, int D, int pairs, cudaStream_t s) {
+  if (prm.L <= 0) return cudaSuccess;
+  if (D != 64 && D != 128) return cudaErrorInvalidValue;
+  TcArgs args;
+  if (!make_args(args, prm, D, pairs, false)) return cudaErrorInvalidValue;
+  const dim3 grid((prm.L + BLK - 1) / BLK, pairs);
+  return D == 128 ? launch_tc(colsum_tc<128>, grid, ColCfg<128>::bytes, s, args)
+                  : launch_tc(colsum_tc<64>, grid, ColCfg<64>::bytes, s, args);
 }
 
 }  // namespace h2o
