@@ -273,6 +273,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
   for (int e = 0; e < EPV; ++e) o[e] = 0.f;
   float s_self = 0.f;
   int p = 0, count = 0, head = 0;
+  uint4 newrow = make_uint4(0, 0, 0, 0);
 
   if (warp == NCW) {
     // ---------------------------------------------------------- producer warp
@@ -328,9 +329,22 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
         ps[j] = prm.pos[slot0 + j];
       }
     };
+    // warm L2 with this pair's q, k_new and v_new rows while waiting
+    {
+      constexpr int NLINE = (ROWB + 127) / 128;
+      if (tid < 3 * NLINE) {
+        const void* row = tid < NLINE ? prm.q : (tid < 2 * NLINE ? prm.k_new : prm.v_new);
+        prefetch_l2(static_cast<const unsigned char*>(row) + static_cast<size_t>(pair) * ROWB + (tid % NLINE) * 128);
+      }
+    }
     if (prm.prefetch) load_state();
     griddep_wait();    // every earlier kernel on the stream has completed
     if (!prm.prefetch) load_state();
+    // the slice of the new K (threads < LPR) or V row (LPR..2 LPR-1) that
+    // this thread writes if this CTA owns the evicted slot
+    if (tid < 2 * LPR)
+      newrow = *reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(tid < LPR ? prm.k_new : prm.v_new) +
+                                               static_cast<size_t>(pair) * ROWB + (tid % LPR) * 16);
     p = ctr.x;
     count = ctr.y;
     head = ctr.z;
@@ -524,11 +538,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
   if (u >= lo && u < lo + prm.chunk && u >= 0) {
     const size_t us = static_cast<size_t>(pair) * C + u;
     if (tid < 2 * LPR) {
-      const int part = tid % LPR;
-      const unsigned char* src = static_cast<const unsigned char*>(tid < LPR ? prm.k_new : prm.v_new) +
-                                 static_cast<size_t>(pair) * ROWB + part * 16;
-      unsigned char* dst = static_cast<unsigned char*>(tid < LPR ? prm.K : prm.V) + us * ROWB + part * 16;
-      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+      unsigned char* dst = static_cast<unsigned char*>(tid < LPR ? prm.K : prm.V) + us * ROWB + (tid % LPR) * 16;
+      *reinterpret_cast<uint4*>(dst) = newrow;
     }
     if (tid == 0) {
       prm.pos[us] = p;
@@ -646,6 +657,11 @@ __global__ void __launch_bounds__(kWarpNW * 32, 1) decode_warp_kernel(const Deco
       ++issued;
     }
   };
+  if (lane < 3 * ((ROWB + 127) / 128)) {  // warm L2 with the first pair's q, k_new and v_new rows
+    constexpr int NLINE = (ROWB + 127) / 128;
+    const void* row = lane < NLINE ? prm.q : (lane < 2 * NLINE ? prm.k_new : prm.v_new);
+    prefetch_l2(static_cast<const unsigned char*>(row) + static_cast<size_t>(gw) * ROWB + (lane % NLINE) * 128);
+  }
   if (prm.prefetch) {
     load_ctrs();
     issue_upto(NS);

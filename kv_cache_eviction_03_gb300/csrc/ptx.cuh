@@ -73,6 +73,11 @@ __device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+// Pull one 128-byte line into L2 (no register result; coherent, so it may
+// run before the producer of the data has finished).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
