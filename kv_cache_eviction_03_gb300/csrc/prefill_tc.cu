@@ -258,21 +258,30 @@ __global__ void __launch_bounds__(NT, 2) stats_tc(const __grid_constant__ TcArgs
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = col0 + e <= rl ? v[e] : -INFINITY;
         }
-        // the max of the raw logits (scale > 0 commutes with max)
-        float c0 = v[0], c1 = v[1];
+        // the max of the raw logits (scale > 0 commutes with max), two
+        // chains of three-input maxima
+        float c0 = max3(v[0], v[1], v[2]), c1 = v[3];
 #pragma unroll
-        for (int e = 2; e < 32; e += 2) {
-          c0 = fmaxf(c0, v[e]);
-          c1 = fmaxf(c1, v[e + 1]);
+        for (int e = 4; e < 32; e += 4) {
+          c0 = max3(c0, v[e], v[e + 1]);
+          c1 = max3(c1, v[e + 2], v[e + 3]);
         }
         const float mn = fmaxf(m, fmaxf(c0, c1) * prm.qscale);
-        float s0 = 0.f, s1 = 0.f;
+        // exp2(v * qscale - mn) summed, two columns per f32x2 FMA / add
+        const uint64_t qs2 = f2_pack(prm.qscale, prm.qscale), nm2 = f2_pack(-mn, -mn);
+        uint64_t s0 = 0, s1 = 0;  // packed (0.f, 0.f)
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          s0 += ex2(fmaf(v[e], prm.qscale, -mn));
-          s1 += ex2(fmaf(v[e + 1], prm.qscale, -mn));
+        for (int e = 0; e < 32; e += 4) {
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(v[e], v[e + 1]), qs2, nm2), x0, x1);
+          f2_unpack(f2_fma(f2_pack(v[e + 2], v[e + 3]), qs2, nm2), x2, x3);
+          s0 = f2_add(s0, f2_pack(ex2(x0), ex2(x1)));
+          s1 = f2_add(s1, f2_pack(ex2(x2), ex2(x3)));
         }
-        l = l * ex2(m - mn) + (s0 + s1);
+        float a0, a1, a2, a3;
+        f2_unpack(s0, a0, a1);
+        f2_unpack(s1, a2, a3);
+        l = l * ex2(m - mn) + ((a0 + a1) + (a2 + a3));
         m = mn;
       }
       tc::fence_before_sync();
@@ -424,10 +433,13 @@ __global__ void __launch_bounds__(NT, 1) out_tc(const __grid_constant__ TcArgs a
             ph[c * 16 + e] = tc::cvt_half2(p0, p1);
           }
         } else {
+          const uint64_t qs2 = f2_pack(prm.qscale, prm.qscale), nl2 = f2_pack(-lse, -lse);
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            ph[c * 16 + e] =
-                tc::cvt_half2(ex2(fmaf(v[2 * e], prm.qscale, -lse)), ex2(fmaf(v[2 * e + 1], prm.qscale, -lse)));
+          for (int e = 0; e < 16; ++e) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(v[2 * e], v[2 * e + 1]), qs2, nl2), x0, x1);
+            ph[c * 16 + e] = tc::cvt_half2(ex2(x0), ex2(x1));
+          }
         }
       }
       // probability tile b was last read by O(j-2)
@@ -536,55 +548,63 @@ __global__ void __launch_bounds__(NT, 2) colsum_tc(const __grid_constant__ TcArg
     const int cw = warp - 2, quarter = warp & 3, half = cw >> 2;
     const int kl = quarter * 32 + lane, key = kb * BLK + kl;  // TMEM lane = key
     const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
-    // this warp's 64 query columns' lse values, one block ahead: lane t
-    // fetches columns 2t, 2t + 1 of the next block while this one is worked on
+    // this warp's 64 query columns' lse values, negated, one block ahead:
+    // lane t fetches columns 2t, 2t + 1 of the next block while this one is
+    // worked on
     const float* lse2 = prm.lse2 + static_cast<size_t>(pair) * L;
     float* wl = reinterpret_cast<float*>(smem + Cfg::lse) + cw * 128;  // [2][64]
     const int c0 = half * 64 + 2 * lane;
-    wl[2 * lane] = lse_at(lse2, kb * BLK, c0, L);
-    wl[2 * lane + 1] = lse_at(lse2, kb * BLK, c0 + 1, L);
+    wl[2 * lane] = -lse_at(lse2, kb * BLK, c0, L);
+    wl[2 * lane + 1] = -lse_at(lse2, kb * BLK, c0 + 1, L);
     __syncwarp();
     double dacc = 0.0;
     for (int i = 0; i < n; ++i) {
       const int b = i & 1;
-      float n0 = kHugeLse, n1 = kHugeLse;
+      float n0 = -kHugeLse, n1 = -kHugeLse;
       if (i + 1 < n) {
-        n0 = lse_at(lse2, (kb + i + 1) * BLK, c0, L);
-        n1 = lse_at(lse2, (kb + i + 1) * BLK, c0 + 1, L);
+        n0 = -lse_at(lse2, (kb + i + 1) * BLK, c0, L);
+        n1 = -lse_at(lse2, (kb + i + 1) * BLK, c0 + 1, L);
       }
       if (!wait_warp(&sfull[b], static_cast<uint32_t>((i >> 1) & 1), lane, err)) break;
       tc::fence_after_sync();
-      const float* lse = wl + b * 64;
+      const float* nlse = wl + b * 64;
+      const uint64_t qs2 = f2_pack(prm.qscale, prm.qscale);
       float acc0 = 0.f, acc1 = 0.f;
+      uint64_t acc2 = 0, acc3 = 0;  // packed (0.f, 0.f)
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int col0 = half * 64 + c * 32;
         float v[32];
         tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + col0), v);
-        const float4* l4 = reinterpret_cast<const float4*>(lse + c * 32);
+        const float4* l4 = reinterpret_cast<const float4*>(nlse + c * 32);
         if (i == 0) {  // diagonal block: query col0 + e sees key kl only if kl <= col0 + e
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float4 t = l4[j];
             const int e = 4 * j;
-            acc0 += kl <= col0 + e ? ex2(fmaf(v[e], prm.qscale, -t.x)) : 0.f;
-            acc1 += kl <= col0 + e + 1 ? ex2(fmaf(v[e + 1], prm.qscale, -t.y)) : 0.f;
-            acc0 += kl <= col0 + e + 2 ? ex2(fmaf(v[e + 2], prm.qscale, -t.z)) : 0.f;
-            acc1 += kl <= col0 + e + 3 ? ex2(fmaf(v[e + 3], prm.qscale, -t.w)) : 0.f;
+            acc0 += kl <= col0 + e ? ex2(fmaf(v[e], prm.qscale, t.x)) : 0.f;
+            acc1 += kl <= col0 + e + 1 ? ex2(fmaf(v[e + 1], prm.qscale, t.y)) : 0.f;
+            acc0 += kl <= col0 + e + 2 ? ex2(fmaf(v[e + 2], prm.qscale, t.z)) : 0.f;
+            acc1 += kl <= col0 + e + 3 ? ex2(fmaf(v[e + 3], prm.qscale, t.w)) : 0.f;
           }
         } else {
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float4 t = l4[j];
             const int e = 4 * j;
-            acc0 += ex2(fmaf(v[e], prm.qscale, -t.x));
-            acc1 += ex2(fmaf(v[e + 1], prm.qscale, -t.y));
-            acc0 += ex2(fmaf(v[e + 2], prm.qscale, -t.z));
-            acc1 += ex2(fmaf(v[e + 3], prm.qscale, -t.w));
+            // two columns per f32x2 FMA / add
+            float x0, x1, x2, x3;
+            f2_unpack(f2_fma(f2_pack(v[e], v[e + 1]), qs2, f2_pack(t.x, t.y)), x0, x1);
+            f2_unpack(f2_fma(f2_pack(v[e + 2], v[e + 3]), qs2, f2_pack(t.z, t.w)), x2, x3);
+            acc2 = f2_add(acc2, f2_pack(ex2(x0), ex2(x1)));
+            acc3 = f2_add(acc3, f2_pack(ex2(x2), ex2(x3)));
           }
         }
       }
-      dacc += static_cast<double>(acc0 + acc1);
+      float a0, a1, a2, a3;
+      f2_unpack(acc2, a0, a1);
+      f2_unpack(acc3, a2, a3);
+      dacc += static_cast<double>((acc0 + acc1) + ((a0 + a1) + (a2 + a3)));
       tc::fence_before_sync();
       __syncwarp();  // also: every lane is done with lse slot b
       if (lane == 0) tc::mbar_arrive_plain(&sempty[b]);  // accumulator b may be overwritten
