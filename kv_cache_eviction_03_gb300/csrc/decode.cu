@@ -438,29 +438,39 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
   else
     __syncthreads();
 
-  if (tid < S) {
-    const Xch* rx = clustered ? cluster.map_shared_rank(xch, tid) : xch;
-    g_m[tid] = rx->m;
-    g_l[tid] = rx->l;
-    if (tid == 0) g_self[0] = rx->s_self;
+  // the pair's normaliser: merged over the cluster's CTAs, or, for a pair
+  // handled by one CTA, this CTA's own (published before the barrier above)
+  float M = kNeg, Ls = 0.f, sself;
+  if (clustered) {
+    if (tid < S) {
+      const Xch* rx = cluster.map_shared_rank(xch, tid);
+      g_m[tid] = rx->m;
+      g_l[tid] = rx->l;
+      if (tid == 0) g_self[0] = rx->s_self;
+    }
+    __syncthreads();
+    for (int r = 0; r < S; ++r) M = fmaxf(M, g_m[r]);
+    for (int r = 0; r < S; ++r) Ls = fmaf(g_l[r], exp2f(g_m[r] - M), Ls);
+    sself = g_self[0];
+  } else {
+    M = xch->m;
+    Ls = xch->l;
+    sself = xch->s_self;
   }
-  __syncthreads();
   p = blk_int[1];
   count = blk_int[2];
   head = blk_int[3];
   const bool full = count >= C;
   const int nrows = max(min(lo + prm.chunk, count) - lo, 0);
-  float M = kNeg;
-  for (int r = 0; r < S; ++r) M = fmaxf(M, g_m[r]);
-  float Ls = 0.f;
-  for (int r = 0; r < S; ++r) Ls = fmaf(g_l[r], exp2f(g_m[r] - M), Ls);
   const float inv = 1.f / Ls;
-  const float p_self = exp2f(g_self[0] - M) * inv;
+  const float p_self = exp2f(sself - M) * inv;
 
   if (rank == 0 && tid < D) {
-    float acc = 0.f;
-    for (int r = 0; r < S; ++r)
-      acc = fmaf((clustered ? cluster.map_shared_rank(xo, r) : xo)[tid], exp2f(g_m[r] - M), acc);
+    float acc = xo[tid];
+    if (clustered) {
+      acc = 0.f;
+      for (int r = 0; r < S; ++r) acc = fmaf(cluster.map_shared_rank(xo, r)[tid], exp2f(g_m[r] - M), acc);
+    }
     prm.out[static_cast<size_t>(pair) * D + tid] = acc * inv;
   }
 
