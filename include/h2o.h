@@ -88,6 +88,24 @@ H2O_API int h2o_prefill_ex(h2o_cache* cache, const void* q, const void* k, const
                    float scale, float* out_or_null, float* colsum_or_null, float* lse_or_null,
                    void* stream);
 
+/* Ragged batch: h2o_prefill_ex where batch row b's prompt has lengths[b]
+ * tokens (clamped to 0..max_len).  The prefill rule ("H2O ... 深度解读报告"
+ * §3.4) is applied to every (b, h) pair with its own length: keep all when
+ * lengths[b] <= heavy + recent, else the top-heavy column sums of positions
+ * < lengths[b] - recent plus the last `recent`; the pair's next decode
+ * position is lengths[b] (0: the pair starts empty).  lengths: [B] int32
+ * device pointer (4-byte aligned), read on the stream, so it may be written
+ * by earlier work on it.  q, k, v: [B, H, max_len, D] with row b valid in
+ * positions < lengths[b]; padded positions are read but contribute nothing
+ * and must hold finite values (zeros suit).  out_or_null, colsum_or_null,
+ * lse_or_null as in h2o_prefill_ex, [B, H, max_len, ...]; their entries at
+ * padded positions are unspecified.  max_len = 0 empties the cache.  Not in
+ * the pages, which pad every prompt to one length: this serves batches of
+ * prompts of different lengths without padding them into the keep rule. */
+H2O_API int h2o_prefill_ragged(h2o_cache* cache, const void* q, const void* k, const void* v, int max_len,
+                               const int32_t* lengths, float scale, float* out_or_null, float* colsum_or_null,
+                               float* lse_or_null, void* stream);
+
 /* One decode step for every pair ("... 深度解读报告", sections 3.1, 3.3, 3.4):
  *   1. attend over the kept slots and the new token: softmax of
  *      scale * q . k over kept + self only; out = sum_j p_j v_j;

@@ -32,6 +32,8 @@ SIGNATURES = {
     "h2o_prefill": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int, _c_float, _c_void_p, _c_void_p]),
     "h2o_prefill_ex": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int, _c_float, _c_void_p,
                                 _c_void_p, _c_void_p, _c_void_p]),
+    "h2o_prefill_ragged": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int, _c_void_p, _c_float,
+                                    _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "h2o_decode_step": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_float, _c_void_p, _c_void_p,
                                  _c_void_p]),
     "h2o_cache_reset": (_c_int, [_c_void_p, _c_void_p]),
@@ -162,6 +164,21 @@ def h2o_prefill_ex(cache: Cache, q, k, v, scale, out=None, colsum=None, lse=None
         cache.handle, _ptr(q, dt, shp, "q"), _ptr(k, dt, shp, "k"), _ptr(v, dt, shp, "v"), L, float(scale),
         _ptr(out, torch.float32, shp, "out"), _ptr(colsum, torch.float32, (B, H, L), "colsum"),
         _ptr(lse, torch.float32, (B, H, L), "lse"), _stream(stream)))
+
+
+def h2o_prefill_ragged(cache: Cache, q, k, v, lengths, scale, out=None, colsum=None, lse=None, stream=None):
+    """q, k, v: [B, H, max_len, D]; lengths: int32 CUDA tensor [B] of prompt lengths."""
+    import torch
+
+    B, H, D = cache.batch, cache.heads, cache.head_dim
+    L = q.shape[2]
+    dt = cache.torch_dtype()
+    shp = (B, H, L, D)
+    _check(lib().h2o_prefill_ragged(
+        cache.handle, _ptr(q, dt, shp, "q"), _ptr(k, dt, shp, "k"), _ptr(v, dt, shp, "v"), L,
+        _ptr(lengths, torch.int32, (B,), "lengths"), float(scale), _ptr(out, torch.float32, shp, "out"),
+        _ptr(colsum, torch.float32, (B, H, L), "colsum"), _ptr(lse, torch.float32, (B, H, L), "lse"),
+        _stream(stream)))
 
 
 def h2o_prefill(cache: Cache, q, k, v, scale, out=None, stream=None):

@@ -190,8 +190,11 @@ int h2o_cache_reset(h2o_cache* c, void* stream) {
   return H2O_OK;
 }
 
-int h2o_prefill_ex(h2o_cache* c, const void* q, const void* k, const void* v, int prompt_len, float scale,
-                   float* out_or_null, float* colsum_or_null, float* lse_or_null, void* stream) {
+// The prefill for a prompt of prompt_len rows per pair, or, with lens, of
+// lens[b] rows for batch row b (prompt_len then being the row stride).
+static int prefill_impl(h2o_cache* c, const void* q, const void* k, const void* v, int prompt_len,
+                        const int32_t* lens, float scale, float* out_or_null, float* colsum_or_null,
+                        float* lse_or_null, void* stream) {
   if (!c) return fail(H2O_EINVAL, "h2o_prefill: cache is NULL");
   if (prompt_len < 0) return fail(H2O_EINVAL, "h2o_prefill: prompt_len must be >= 0");
   if (prompt_len == 0) return h2o_cache_reset(c, stream);
@@ -224,6 +227,8 @@ int h2o_prefill_ex(h2o_cache* c, const void* q, const void* k, const void* v, in
   pp.L = prompt_len;
   pp.qscale = scale * 1.4426950408889634f;
   pp.err = c->err;
+  pp.lens = lens;
+  pp.heads = c->H;
   cudaStream_t s = as_stream(stream);
   touch_stream(c, stream);
   if ((e = h2o::launch_prefill_stats(pp, c->dtype, c->D, c->P, s)) != cudaSuccess)
@@ -245,12 +250,27 @@ int h2o_prefill_ex(h2o_cache* c, const void* q, const void* k, const void* v, in
   sp.heavy = c->heavy;
   sp.recent = c->recent;
   sp.C = c->C;
+  sp.lens = lens;
+  sp.heads = c->H;
   if ((e = h2o::launch_prefill_select(sp, c->dtype, c->D, c->P, s)) != cudaSuccess)
     return cuda_fail(e, "h2o_prefill: select launch");
   if (lse_or_null && (e = h2o::launch_lse_export(pp.lse2, lse_or_null, plen, s)) != cudaSuccess)
     return cuda_fail(e, "h2o_prefill: lse export");
-  c->host_next_p = prompt_len;
+  c->host_next_p = prompt_len;  // an upper bound on every pair's next position
   return H2O_OK;
+}
+
+int h2o_prefill_ex(h2o_cache* c, const void* q, const void* k, const void* v, int prompt_len, float scale,
+                   float* out_or_null, float* colsum_or_null, float* lse_or_null, void* stream) {
+  return prefill_impl(c, q, k, v, prompt_len, nullptr, scale, out_or_null, colsum_or_null, lse_or_null, stream);
+}
+
+int h2o_prefill_ragged(h2o_cache* c, const void* q, const void* k, const void* v, int max_len,
+                       const int32_t* lengths, float scale, float* out_or_null, float* colsum_or_null,
+                       float* lse_or_null, void* stream) {
+  if (!lengths || (reinterpret_cast<uintptr_t>(lengths) & 3u) != 0)
+    return fail(H2O_EINVAL, "h2o_prefill_ragged: lengths must be a 4-byte aligned device pointer");
+  return prefill_impl(c, q, k, v, max_len, lengths, scale, out_or_null, colsum_or_null, lse_or_null, stream);
 }
 
 int h2o_prefill(h2o_cache* c, const void* q, const void* k, const void* v, int prompt_len, float scale,

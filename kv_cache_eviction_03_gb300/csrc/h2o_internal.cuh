@@ -55,9 +55,11 @@ struct PrefillParams {
   float* out;     // [P, L, D] or nullptr
   float* lse2;    // [P, L] log2-domain row log-sum-exp of the scaled logits
   float* colsum;  // [P, L]
-  int L;
+  int L;          // row stride of the [P, L, D] inputs and [P, L] outputs (the longest prompt)
   float qscale;   // scale * log2(e)
   int* err = nullptr;  // device error bits, or nullptr
+  const int* lens = nullptr;  // [B] per-batch-row prompt lengths (device), or nullptr: all L
+  int heads = 1;              // pairs per batch row (maps a pair to its length)
 };
 
 struct SelectParams {
@@ -71,8 +73,19 @@ struct SelectParams {
   int* ring;
   PairCtr* ctr;
   int* err;
-  int L, heavy, recent, C;
+  int L, heavy, recent, C;    // L: row stride of the inputs (the longest prompt)
+  const int* lens = nullptr;  // [B] per-batch-row prompt lengths (device), or nullptr: all L
+  int heads = 1;
 };
+
+// Prompt length of pair `pair`: its batch row's length, clamped to [0, L],
+// when lengths are given, else L.  Read after the grid-dependency wait (the
+// lengths may come from an earlier kernel).
+__device__ __forceinline__ int pair_len(const int* lens, int heads, int L, int pair) {
+  if (!lens) return L;
+  const int n = lens[pair / heads];
+  return n < 0 ? 0 : (n > L ? L : n);
+}
 
 // Record the thread-local message returned by h2o_last_error(); returns code.
 int set_error(int code, const char* fmt, ...);

@@ -64,16 +64,18 @@ __global__ void __launch_bounds__(128) stats_f16(const PrefillParams prm) {
   unsigned char* sV = smem + 3 * TILE;             // [2] tiles (WITH_O)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
-  const int L = prm.L;
+  const int LS = prm.L;  // row stride; L below is this pair's prompt length
   const int pair = blockIdx.y;
   const int qb = gridDim.x - 1 - blockIdx.x;  // longest rows first
   const int q0 = qb * BM;
-  const size_t base = static_cast<size_t>(pair) * L * D;
+  const size_t base = static_cast<size_t>(pair) * LS * D;
   const __half* Q = static_cast<const __half*>(prm.q) + base;
   const __half* K = static_cast<const __half*>(prm.k) + base;
   const __half* V = static_cast<const __half*>(prm.v) + base;
 
   griddep_wait();
+  const int L = pair_len(prm.lens, prm.heads, LS, pair);
+  if (q0 >= L) return;
   load_tile<D, 128>(sQ, Q, q0, L, tid);
   load_tile<D, 128>(sK, K, 0, L, tid);
   if (WITH_O) load_tile<D, 128>(sV, V, 0, L, tid);
@@ -194,10 +196,10 @@ __global__ void __launch_bounds__(128) stats_f16(const PrefillParams prm) {
   for (int h = 0; h < 2; ++h) {
     const int qi = row_g + h * 8;
     if (qi < L) {
-      if (t4 == 0) prm.lse2[static_cast<size_t>(pair) * L + qi] = m[h] + log2f(l[h]);
+      if (t4 == 0) prm.lse2[static_cast<size_t>(pair) * LS + qi] = m[h] + log2f(l[h]);
       if (WITH_O) {
         const float inv = 1.f / l[h];
-        float* orow = prm.out + (static_cast<size_t>(pair) * L + qi) * D;
+        float* orow = prm.out + (static_cast<size_t>(pair) * LS + qi) * D;
 #pragma unroll
         for (int dt = 0; dt < DT; ++dt)
           *reinterpret_cast<float2*>(orow + dt * 8 + 2 * t4) =
@@ -218,16 +220,19 @@ __global__ void __launch_bounds__(128) colsum_f16(const PrefillParams prm) {
   float* sL = reinterpret_cast<float*>(smem + 3 * TILE);            // [2][BM] lse2
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
-  const int L = prm.L;
+  const int LS = prm.L;  // row stride; L below is this pair's prompt length
   const int pair = blockIdx.y;
   const int jb = blockIdx.x;  // key block; block 0 has the most query blocks
-  const size_t base = static_cast<size_t>(pair) * L * D;
+  const size_t base = static_cast<size_t>(pair) * LS * D;
   const __half* Q = static_cast<const __half*>(prm.q) + base;
   const __half* K = static_cast<const __half*>(prm.k) + base;
-  const float* lse2 = prm.lse2 + static_cast<size_t>(pair) * L;
-  const int nqb = (L + BM - 1) / BM;
+  const float* lse2 = prm.lse2 + static_cast<size_t>(pair) * LS;
+  
 
   griddep_wait();
+  const int L = pair_len(prm.lens, prm.heads, LS, pair);
+  const int nqb = (L + BM - 1) / BM;
+  if (jb * BN >= L) return;
   load_tile<D, 128>(sK, K, jb * BN, L, tid);
   load_tile<D, 128>(sQ, Q, jb * BM, L, tid);
   for (int r = tid; r < BM; r += 128) {
@@ -309,7 +314,7 @@ __global__ void __launch_bounds__(128) colsum_f16(const PrefillParams prm) {
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int kj = key0 + nt * 8 + 2 * t4 + c;
-        if (kj < L) prm.colsum[static_cast<size_t>(pair) * L + kj] = static_cast<float>(acc[nt][c]);
+        if (kj < L) prm.colsum[static_cast<size_t>(pair) * LS + kj] = static_cast<float>(acc[nt][c]);
       }
     }
   }
@@ -322,11 +327,12 @@ __global__ void __launch_bounds__(128) stats_f32(const PrefillParams prm) {
   constexpr int PER = D / 32;
   __shared__ __align__(16) float qs[4][D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int L = prm.L, pair = blockIdx.y;
+  const int LS = prm.L, pair = blockIdx.y;
   const int i = blockIdx.x * 4 + warp;
   griddep_wait();
+  const int L = pair_len(prm.lens, prm.heads, LS, pair);  // LS: row stride
   if (i >= L) return;
-  const size_t base = static_cast<size_t>(pair) * L * D;
+  const size_t base = static_cast<size_t>(pair) * LS * D;
   const float* Q = static_cast<const float*>(prm.q) + base;
   const float* K = static_cast<const float*>(prm.k) + base;
   const float* V = static_cast<const float*>(prm.v) + base;
@@ -373,11 +379,11 @@ __global__ void __launch_bounds__(128) stats_f32(const PrefillParams prm) {
   }
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-  if (lane == 0) prm.lse2[static_cast<size_t>(pair) * L + i] = m + log2f(l);
+  if (lane == 0) prm.lse2[static_cast<size_t>(pair) * LS + i] = m + log2f(l);
   if (prm.out) {
     const float inv = 1.f / l;
 #pragma unroll
-    for (int e = 0; e < PER; ++e) prm.out[(static_cast<size_t>(pair) * L + i) * D + lane + 32 * e] = o[e] * inv;
+    for (int e = 0; e < PER; ++e) prm.out[(static_cast<size_t>(pair) * LS + i) * D + lane + 32 * e] = o[e] * inv;
   }
 }
 
@@ -386,14 +392,15 @@ template <int D>
 __global__ void __launch_bounds__(128) colsum_f32(const PrefillParams prm) {
   __shared__ __align__(16) float ks[4][D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int L = prm.L, pair = blockIdx.y;
+  const int LS = prm.L, pair = blockIdx.y;
   const int j = blockIdx.x * 4 + warp;
   griddep_wait();
+  const int L = pair_len(prm.lens, prm.heads, LS, pair);  // LS: row stride
   if (j >= L) return;
-  const size_t base = static_cast<size_t>(pair) * L * D;
+  const size_t base = static_cast<size_t>(pair) * LS * D;
   const float* Q = static_cast<const float*>(prm.q) + base;
   const float* K = static_cast<const float*>(prm.k) + base;
-  const float* lse2 = prm.lse2 + static_cast<size_t>(pair) * L;
+  const float* lse2 = prm.lse2 + static_cast<size_t>(pair) * LS;
   for (int d = lane; d < D; d += 32) ks[warp][d] = K[static_cast<size_t>(j) * D + d];
   __syncwarp();
   double acc = 0.0;
@@ -412,7 +419,7 @@ __global__ void __launch_bounds__(128) colsum_f32(const PrefillParams prm) {
   }
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) prm.colsum[static_cast<size_t>(pair) * L + j] = static_cast<float>(acc);
+  if (lane == 0) prm.colsum[static_cast<size_t>(pair) * LS + j] = static_cast<float>(acc);
 }
 
 __global__ void lse_export_kernel(const float* lse2, float* lse, size_t n) {

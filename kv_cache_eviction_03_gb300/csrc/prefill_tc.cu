@@ -212,6 +212,8 @@ __global__ void __launch_bounds__(NT, 2) stats_tc(const __grid_constant__ TcArgs
     tc::prefetch_tensormap(&a.k);
   }
   griddep_wait();
+  const int Lp = pair_len(prm.lens, prm.heads, L, pair);  // this pair's prompt length (L: row stride)
+  if (qb * BLK >= Lp) return;                              // no rows of this pair here
   const uint32_t tbase = setup(warp, bars, counts, Cfg::NB, reinterpret_cast<uint32_t*>(smem + Cfg::tslot), 256);
   if (warp == 0) {
     if (lane == 0) {  // TMA producer
@@ -291,7 +293,7 @@ __global__ void __launch_bounds__(NT, 2) stats_tc(const __grid_constant__ TcArgs
     // merge the two column halves of each row
     if (half == 1) red[rl] = make_float2(m, l);
     tc::named_sync(kCompBar, NCOMP * 32);
-    if (half == 0 && row < L) {
+    if (half == 0 && row < Lp) {
       const float2 o = red[rl];
       const float M = fmaxf(m, o.x);
       prm.lse2[static_cast<size_t>(pair) * L + row] = M + log2f(l * ex2(m - M) + o.y * ex2(o.x - M));
@@ -350,6 +352,8 @@ __global__ void __launch_bounds__(NT, 1) out_tc(const __grid_constant__ TcArgs a
     tc::prefetch_tensormap(&a.v);
   }
   griddep_wait();
+  const int Lp = pair_len(prm.lens, prm.heads, L, pair);  // this pair's prompt length (L: row stride)
+  if (qb * BLK >= Lp) return;
   const uint32_t tbase =
       setup(warp, bars, counts, Cfg::NB, reinterpret_cast<uint32_t*>(smem + Cfg::tslot), kOutTmemCols);
   const uint32_t o_tmem = tbase + 2 * BLK;
@@ -412,7 +416,7 @@ __global__ void __launch_bounds__(NT, 1) out_tc(const __grid_constant__ TcArgs a
     const int quarter = warp & 3, half = (warp - 2) >> 2;
     const int rl = quarter * 32 + lane, row = qb * BLK + rl;
     const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
-    const float lse = lse_at(prm.lse2 + static_cast<size_t>(pair) * L, qb * BLK, rl, L);
+    const float lse = lse_at(prm.lse2 + static_cast<size_t>(pair) * L, qb * BLK, rl, Lp);
     bool ok = true;
     for (int j = 0; ok && j < n; ++j) {
       const int b = j & 1;
@@ -464,7 +468,7 @@ __global__ void __launch_bounds__(NT, 1) out_tc(const __grid_constant__ TcArgs a
         tc::tmem_ld32(o_tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                           static_cast<uint32_t>(half * (D / 2) + c * 32),
                       o);
-        if (row < L) {
+        if (row < Lp) {
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             reinterpret_cast<float4*>(dst + c * 32)[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
@@ -508,7 +512,7 @@ __global__ void __launch_bounds__(NT, 2) colsum_tc(const __grid_constant__ TcArg
   int* err = prm.err;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = prm.L, pair = blockIdx.y, kb = blockIdx.x;
-  const int n = (L + BLK - 1) / BLK - kb;  // query blocks from the diagonal down
+
   const uint32_t counts[Cfg::NB] = {1, 1, 1, 1, 1, 1, 1, NCOMP, NCOMP, 1};
 
   if (threadIdx.x == 0) {
@@ -516,6 +520,9 @@ __global__ void __launch_bounds__(NT, 2) colsum_tc(const __grid_constant__ TcArg
     tc::prefetch_tensormap(&a.k);
   }
   griddep_wait();
+  const int Lp = pair_len(prm.lens, prm.heads, L, pair);  // this pair's prompt length (L: row stride)
+  const int n = (Lp + BLK - 1) / BLK - kb;                 // query blocks from the diagonal down
+  if (n <= 0) return;
   const uint32_t tbase = setup(warp, bars, counts, Cfg::NB, reinterpret_cast<uint32_t*>(smem + Cfg::tslot), 256);
   if (warp == 0) {
     if (lane == 0) {  // TMA producer
@@ -554,16 +561,16 @@ __global__ void __launch_bounds__(NT, 2) colsum_tc(const __grid_constant__ TcArg
     const float* lse2 = prm.lse2 + static_cast<size_t>(pair) * L;
     float* wl = reinterpret_cast<float*>(smem + Cfg::lse) + cw * 128;  // [2][64]
     const int c0 = half * 64 + 2 * lane;
-    wl[2 * lane] = -lse_at(lse2, kb * BLK, c0, L);
-    wl[2 * lane + 1] = -lse_at(lse2, kb * BLK, c0 + 1, L);
+    wl[2 * lane] = -lse_at(lse2, kb * BLK, c0, Lp);
+    wl[2 * lane + 1] = -lse_at(lse2, kb * BLK, c0 + 1, Lp);
     __syncwarp();
     double dacc = 0.0;
     for (int i = 0; i < n; ++i) {
       const int b = i & 1;
       float n0 = -kHugeLse, n1 = -kHugeLse;
       if (i + 1 < n) {
-        n0 = -lse_at(lse2, (kb + i + 1) * BLK, c0, L);
-        n1 = -lse_at(lse2, (kb + i + 1) * BLK, c0 + 1, L);
+        n0 = -lse_at(lse2, (kb + i + 1) * BLK, c0, Lp);
+        n1 = -lse_at(lse2, (kb + i + 1) * BLK, c0 + 1, Lp);
       }
       if (!wait_warp(&sfull[b], static_cast<uint32_t>((i >> 1) & 1), lane, err)) break;
       tc::fence_after_sync();
@@ -614,7 +621,7 @@ __global__ void __launch_bounds__(NT, 2) colsum_tc(const __grid_constant__ TcArg
     }
     if (half == 1) red[kl] = dacc;
     tc::named_sync(kCompBar, NCOMP * 32);
-    if (half == 0 && key < L) prm.colsum[static_cast<size_t>(pair) * L + key] = static_cast<float>(dacc + red[kl]);
+    if (half == 0 && key < Lp) prm.colsum[static_cast<size_t>(pair) * L + key] = static_cast<float>(dacc + red[kl]);
     griddep_launch();
   }
   tmem_teardown(warp, lane, drain, tbase, 256, err);

@@ -79,16 +79,17 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const SelectParams prm) {
   __shared__ unsigned s_prefix, s_k, s_eq;
   const int tid = threadIdx.x;
   const int pair = blockIdx.x;
-  const int L = prm.L, heavy = prm.heavy, R = prm.recent, C = prm.C;
-  const float* colsum = prm.colsum + static_cast<size_t>(pair) * L;
-  const unsigned char* srcK = static_cast<const unsigned char*>(prm.k) + static_cast<size_t>(pair) * L * ROWB;
-  const unsigned char* srcV = static_cast<const unsigned char*>(prm.v) + static_cast<size_t>(pair) * L * ROWB;
+  const int LS = prm.L, heavy = prm.heavy, R = prm.recent, C = prm.C;  // LS: row stride
+  const float* colsum = prm.colsum + static_cast<size_t>(pair) * LS;
+  const unsigned char* srcK = static_cast<const unsigned char*>(prm.k) + static_cast<size_t>(pair) * LS * ROWB;
+  const unsigned char* srcV = static_cast<const unsigned char*>(prm.v) + static_cast<size_t>(pair) * LS * ROWB;
   unsigned char* dstK = static_cast<unsigned char*>(prm.K) + static_cast<size_t>(pair) * C * ROWB;
   unsigned char* dstV = static_cast<unsigned char*>(prm.V) + static_cast<size_t>(pair) * C * ROWB;
   float* score = prm.score + static_cast<size_t>(pair) * C;
   int* pos = prm.pos + static_cast<size_t>(pair) * C;
 
   griddep_wait();
+  const int L = pair_len(prm.lens, prm.heads, LS, pair);  // this pair's prompt length
 
   int n_keep;
   if (L <= C) {
