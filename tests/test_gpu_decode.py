@@ -202,6 +202,16 @@ def test_warp_per_pair_shape_limits():
     B.h2o_cache_destroy(big)
 
 
+@pytest.mark.parametrize("ratio", [0.04, 0.10, 0.20, 0.60])
+def test_budget_ratios_every_step(ratio):
+    """Cache budgets of 4, 10, 20 and 60% of a 1000-token prompt (heavy =
+    recent), every decode step checked from identical states."""
+    half = int(round(ratio * 1000 / 2))
+    w = W.Workload(f"budget{ratio}", 1, 4, 128, "f16", 1000, 16, half, half, 1.1)
+    rep = run_stepwise(w, 61)
+    assert rep.pairs == w.pairs * 16
+
+
 @pytest.mark.parametrize("splits", [1, 4, 16, B.H2O_DECODE_WARP_PER_PAIR])
 def test_free_run_fp16(splits):
     w = W.Workload("free", 2, 4, 128, "f16", 300, 80, 40, 30, 1.1)

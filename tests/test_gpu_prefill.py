@@ -139,3 +139,14 @@ def test_prefill_zero_length_empties_cache():
     g = B.unpack_state(cache, B.h2o_cache_export_state(cache))
     assert (g["pos"] == -1).all() and (g["count"] == 0).all() and (g["p"] == 0).all()
     B.h2o_cache_destroy(cache)
+
+
+BUDGETS = [0.04, 0.10, 0.20, 0.60]  # total cache budget as a fraction of the prompt, heavy = recent
+
+
+@pytest.mark.parametrize("ratio", BUDGETS, ids=[f"{int(r * 100)}pct" for r in BUDGETS])
+def test_prefill_budget_ratios(ratio):
+    L = 1000
+    half = int(round(ratio * L / 2))
+    w = W.Workload(f"budget{ratio}", 1, 4, 128, "f16", L, 0, half, half, 1.1)
+    check_prefill(w, 53, with_out=False)
