@@ -318,13 +318,8 @@ def run_ours(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded Zipf-keyed generator, drawn on the GPU)",
-        "config": {"workload": f"{WORKLOAD}: batch {w.batch}, {w.heads} heads, head_dim {w.head_dim}, fp16 K/V, "
-                               f"prompt {L} + {T} decode steps, heavy {w.heavy} + recent {w.recent} slots",
-                   "layers": NL, "batch": w.batch, "decode_steps": T, "prompt": L,
-                   "accumulate": "f32", "decode_splits": info[6],
-                   "l2": f"inputs larger than L2: {NL} layer caches rotated every decode step",
-                   "parallelism": f"weak: each of {world} GPUs runs its own batch" if world > 1 else "1 GPU",
-                   "decode_only": bool(args.decode_only)},
+        "config": workload_config(w, NL, world, args.decode_only),
+        "launch": {"decode_splits": info[6], "decode_stages": info[7]},
         "phases": {"prefill_ms_per_step": prefill_s / args.steps * 1e3,
                    "decode_ms_per_step": decode_s / args.steps * 1e3,
                    "decode_only_tokens_per_s_per_layer": tokens_per_layer * NL * args.steps / decode_s,
@@ -434,6 +429,16 @@ def run_e2e(args, w, NL, stream, set_a, capture, world, dist):
             "pipelined": "step s+1 host->device copy and step s-1 read-back overlap step s"}
 
 
+def workload_config(w, NL, world, decode_only):
+    """The `config` object of the JSON line, identical for both arms."""
+    return {"workload": f"{WORKLOAD}: batch {w.batch}, {w.heads} heads, head_dim {w.head_dim}, fp16 K/V, "
+                        f"prompt {w.prompt} + {w.decode} decode steps, heavy {w.heavy} + recent {w.recent} slots",
+            "layers": NL, "batch": w.batch, "decode_steps": w.decode, "prompt": w.prompt, "accumulate": "f32",
+            "l2": f"inputs larger than L2: {NL} layer caches rotated every decode step",
+            "parallelism": f"weak: each of {world} GPUs runs its own batch" if world > 1 else "1 GPU",
+            "decode_only": bool(decode_only)}
+
+
 def main():
     args = parse()
     rank, world, local_rank = dist_info()
@@ -454,7 +459,7 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.median(walls) * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic (seeded Zipf-keyed generator)",
-                "config": {"workload": WORKLOAD, "batch": w.batch, "decode_steps": w.decode, "prompt": w.prompt},
+                "config": workload_config(w, args.layers or w.layers, world, args.decode_only),
                 "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
                 "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
