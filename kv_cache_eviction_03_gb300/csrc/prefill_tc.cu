@@ -22,9 +22,9 @@
 //    lane = query row; each compute thread keeps an online max / sum over
 //    half of its row's columns.
 //  - output (out_tc): with lse known, P = exp2(s - lse) needs no rescaling;
-//    the compute warps write P as fp16 into a K-major tile and the tensor
-//    core accumulates O += P V in TMEM (V as stored, [key][d], is the
-//    MN-major B operand).
+//    the compute warps store P as fp16 into TMEM (tcgen05.st) and the tensor
+//    core accumulates O += P V in TMEM with A = P taken from TMEM and V as
+//    stored ([key][d]) the MN-major B operand in shared memory.
 //  - columns (colsum_tc): A = 128 keys, B = query blocks from the diagonal
 //    down, i.e. the transposed logits; TMEM lane = key, so each thread sums
 //    the probabilities its key receives with no cross-thread reduction
@@ -89,20 +89,6 @@ __device__ __forceinline__ void issue_block(uint32_t d_tmem, const unsigned char
   for (int ks = 0; ks < D / 16; ++ks) {
     const uint32_t off = static_cast<uint32_t>((ks >> 2) * Tile<D>::KB + (ks & 3) * 32);
     tc::mma_f16(d_tmem, tc::desc_k_sw128(sa + off), tc::desc_k_sw128(sb + off), idesc, ks > 0);
-  }
-}
-
-// D[tmem] (+)= P[128 x 128 keys] * V[128 keys x D]; P K-major, V MN-major
-// (the head dimension contiguous, 64-element atoms 16 KB apart).
-template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, const unsigned char* p, const unsigned char* v, bool acc) {
-  constexpr uint32_t idesc = tc::idesc_f16_f32_bmn(BLK, D);
-  const uint32_t sp = smem_u32(p), sv = smem_u32(v);
-#pragma unroll
-  for (int ks = 0; ks < BLK / 16; ++ks) {
-    const uint32_t aoff = static_cast<uint32_t>((ks >> 2) * (BLK * 128) + (ks & 3) * 32);
-    tc::mma_f16(d_tmem, tc::desc_k_sw128(sp + aoff), tc::desc_mn_sw128(sv + ks * 2048u, BLK * 128), idesc,
-                acc || ks > 0);
   }
 }
 
@@ -306,45 +292,60 @@ __global__ void __launch_bounds__(NT, 2) stats_tc(const __grid_constant__ TcArgs
 // ------------------------------------------------------- attention output
 template <int D>
 struct OutCfg {
-  static constexpr int NK = 2, NV = 2;  // key / value stages
-  static constexpr int PT = BLK * BLK * 2;  // fp16 probabilities of one block
+  static constexpr int NK = 3, NV = 3;  // key / value stages
   static constexpr size_t q = 0, k = Tile<D>::BYTES;
   static constexpr size_t v = k + NK * static_cast<size_t>(Tile<D>::BYTES);
-  static constexpr size_t p = v + NV * static_cast<size_t>(Tile<D>::BYTES);  // 2 probability tiles
-  static constexpr size_t bars = p + 2 * static_cast<size_t>(PT);
-  // qfull, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], pfull[2], pempty[2], ofull, drain
-  static constexpr int NB = 17;
+  static constexpr size_t bars = v + NV * static_cast<size_t>(Tile<D>::BYTES);
+  // qfull, kfull[3], kempty[3], vfull[3], vempty[3], sfull[2], pfull[2], pempty[2], ofull, drain
+  static constexpr int NB = 21;
   static constexpr size_t tslot = bars + 8 * NB;
   static constexpr size_t bytes = tslot + 16 + 1024;
 };
-constexpr uint32_t kOutTmemCols = 512;  // two 128-column logit blocks + O (D <= 128 columns)
+// TMEM columns: two 128-column logit blocks, O (D <= 128 columns), and two
+// 64-column fp16 probability blocks (P(j) is the A operand of O += P V)
+constexpr uint32_t kOutTmemCols = 512;
+constexpr uint32_t kOcol = 2 * BLK, kPcol = 3 * BLK;
+
+// D[tmem] (+)= P[128 x 128 keys, in TMEM] * V[128 keys x D, MN-major in smem].
+template <int D>
+__device__ __forceinline__ void issue_pv_t(uint32_t d_tmem, uint32_t p_tmem, const unsigned char* v, bool acc) {
+  constexpr uint32_t idesc = tc::idesc_f16_f32_bmn(BLK, D);
+  const uint32_t sv = smem_u32(v);
+#pragma unroll
+  for (int ks = 0; ks < BLK / 16; ++ks)  // 16 keys = 8 packed columns per step
+    tc::mma_f16_ta(d_tmem, p_tmem + ks * 8, tc::desc_mn_sw128(sv + ks * 2048u, BLK * 128), idesc, acc || ks > 0);
+}
 
 template <int D>
 __global__ void __launch_bounds__(NT, 1) out_tc(const __grid_constant__ TcArgs a) {
   using Cfg = OutCfg<D>;
-  constexpr int NK = Cfg::NK, NV = Cfg::NV, TB = Tile<D>::BYTES, PT = Cfg::PT;
+  constexpr int NK = Cfg::NK, NV = Cfg::NV, TB = Tile<D>::BYTES;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = align1024(smem_raw);
   unsigned char* sQ = smem + Cfg::q;
   unsigned char* sK = smem + Cfg::k;
   unsigned char* sV = smem + Cfg::v;
-  unsigned char* sP = smem + Cfg::p;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::bars);
   uint64_t* qfull = bars;
-  const Ring<NK> kr{bars + 1, bars + 3};
-  const Ring<NV> vr{bars + 5, bars + 7};
-  uint64_t* sfull = bars + 9;
-  uint64_t* pfull = bars + 11;
-  uint64_t* pempty = bars + 13;
-  uint64_t* ofull = bars + 15;
-  uint64_t* drain = bars + 16;
+  const Ring<NK> kr{bars + 1, bars + 1 + NK};
+  const Ring<NV> vr{bars + 1 + 2 * NK, bars + 1 + 2 * NK + NV};
+  uint64_t* sfull = bars + 1 + 2 * NK + 2 * NV;
+  uint64_t* pfull = sfull + 2;
+  uint64_t* pempty = sfull + 4;
+  uint64_t* ofull = sfull + 6;
+  uint64_t* drain = sfull + 7;
+  static_assert(1 + 2 * NK + 2 * NV + 8 == Cfg::NB, "barrier count");
   const PrefillParams& prm = a.prm;
   int* err = prm.err;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = prm.L, pair = blockIdx.y;
   const int qb = gridDim.x - 1 - blockIdx.x;  // longest rows first
   const int n = qb + 1;
-  const uint32_t counts[Cfg::NB] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, NCOMP, NCOMP, 1, 1, 1, 1};
+  // qfull, K full/empty, V full/empty, sfull[2]: one arrival (TMA or commit);
+  // pfull[2]: one per compute warp; pempty[2], ofull, drain: a commit
+  uint32_t counts[Cfg::NB];
+#pragma unroll
+  for (int i = 0; i < Cfg::NB; ++i) counts[i] = (i == 1 + 2 * NK + 2 * NV + 2 || i == 1 + 2 * NK + 2 * NV + 3) ? NCOMP : 1;
 
   if (threadIdx.x == 0) {
     tc::prefetch_tensormap(&a.q);
@@ -356,7 +357,7 @@ __global__ void __launch_bounds__(NT, 1) out_tc(const __grid_constant__ TcArgs a
   if (qb * BLK >= Lp) return;
   const uint32_t tbase =
       setup(warp, bars, counts, Cfg::NB, reinterpret_cast<uint32_t*>(smem + Cfg::tslot), kOutTmemCols);
-  const uint32_t o_tmem = tbase + 2 * BLK;
+  const uint32_t o_tmem = tbase + kOcol;
   if (warp == 0) {
     if (lane == 0) {  // TMA producer, in the order the MMAs consume: K0 K1 V0 K2 V1 K3 ...
       mbar_arrive_expect_tx(qfull, TB);
@@ -398,7 +399,7 @@ __global__ void __launch_bounds__(NT, 1) out_tc(const __grid_constant__ TcArgs a
         ok = wait1(&pfull[b], static_cast<uint32_t>((j >> 1) & 1), err) && wait1(vr.full_of(j), vr.parity(j), err);
         if (!ok) break;
         tc::fence_after_sync();
-        issue_pv<D>(o_tmem, sP + b * PT, sV + (j % NV) * TB, j > 0);
+        issue_pv_t<D>(o_tmem, tbase + kPcol + b * 64, sV + (j % NV) * TB, j > 0);
         tc::mma_commit(&pempty[b]);
         tc::mma_commit(&vr.empty[j % NV]);
         if (j + 2 < n) {  // the compute warps are done with accumulator b (they have written P(j))
@@ -446,14 +447,10 @@ __global__ void __launch_bounds__(NT, 1) out_tc(const __grid_constant__ TcArgs a
           }
         }
       }
-      // probability tile b was last read by O(j-2)
+      // probability block b (TMEM) was last read by O(j-2); this thread's 64
+      // keys go to its lane's 32 packed columns of that block
       if (j >= 2 && !(ok = wait_warp(&pempty[b], static_cast<uint32_t>(((j - 2) >> 1) & 1), lane, err))) break;
-      unsigned char* prow = sP + b * PT + half * (BLK * 128) + rl * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(prow + ((c ^ (rl & 7)) << 4)) =
-            make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
-      fence_proxy_async_smem();  // the tensor core reads what the threads wrote
+      tc::tmem_st32(lane_addr + kPcol + static_cast<uint32_t>(b * 64 + half * 32), ph);
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_plain(&pfull[b]);
@@ -465,9 +462,7 @@ __global__ void __launch_bounds__(NT, 1) out_tc(const __grid_constant__ TcArgs a
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         float o[32];
-        tc::tmem_ld32(o_tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
-                          static_cast<uint32_t>(half * (D / 2) + c * 32),
-                      o);
+        tc::tmem_ld32(lane_addr + kOcol + static_cast<uint32_t>(half * (D / 2) + c * 32), o);
         if (row < Lp) {
 #pragma unroll
           for (int e = 0; e < 8; ++e)
