@@ -60,6 +60,7 @@ __device__ __forceinline__ float lse_at(const float* src, int row0, int t, int L
 // Kernel arguments: the pointers and sizes plus a tensor map per input.
 struct TcArgs {
   CUtensorMap q, k, v;  // [P, L, D] fp16, box 64 x 128 x 1, 128-byte swizzle
+  CUtensorMap o;        // [P, L, D] fp32 output, box 32 x 128 x 1, 128-byte swizzle
   PrefillParams prm;
 };
 
@@ -351,6 +352,7 @@ __global__ void __launch_bounds__(NT, 1) out_tc(const __grid_constant__ TcArgs a
     tc::prefetch_tensormap(&a.q);
     tc::prefetch_tensormap(&a.k);
     tc::prefetch_tensormap(&a.v);
+    tc::prefetch_tensormap(&a.o);
   }
   griddep_wait();
   const int Lp = pair_len(prm.lens, prm.heads, L, pair);  // this pair's prompt length (L: row stride)
@@ -415,7 +417,7 @@ __global__ void __launch_bounds__(NT, 1) out_tc(const __grid_constant__ TcArgs a
     __syncwarp();
   } else {  // compute warps
     const int quarter = warp & 3, half = (warp - 2) >> 2;
-    const int rl = quarter * 32 + lane, row = qb * BLK + rl;
+    const int rl = quarter * 32 + lane;  // TMEM lane = query row qb * BLK + rl
     const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
     const float lse = lse_at(prm.lse2 + static_cast<size_t>(pair) * L, qb * BLK, rl, Lp);
     bool ok = true;
@@ -457,18 +459,30 @@ __global__ void __launch_bounds__(NT, 1) out_tc(const __grid_constant__ TcArgs a
     }
     ok = ok && wait_warp(ofull, 0, lane, err);
     tc::fence_after_sync();
+    // O leaves through shared memory (the key ring is free once every MMA has
+    // completed): boxes of 128 rows x 32 floats in the 128-byte swizzle (row
+    // r's 16-byte chunk c at chunk c ^ (r % 8): conflict-free for a warp's 32
+    // rows), written out by TMA stores clipped at the prompt's end.
+    unsigned char* sO = sK;
     if (ok) {
-      float* dst = prm.out + (static_cast<size_t>(pair) * L + row) * D + half * (D / 2);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         float o[32];
         tc::tmem_ld32(lane_addr + kOcol + static_cast<uint32_t>(half * (D / 2) + c * 32), o);
-        if (row < Lp) {
+        unsigned char* rowp = sO + (half * (D / 64) + c) * (BLK * 128) + rl * 128;
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            reinterpret_cast<float4*>(dst + c * 32)[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
-        }
+        for (int e = 0; e < 8; ++e)
+          *reinterpret_cast<float4*>(rowp + ((e ^ (rl & 7)) << 4)) =
+              make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
       }
+    }
+    fence_proxy_async_smem();
+    tc::named_sync(kCompBar, NCOMP * 32);
+    if (warp == 2 && lane == 0) {
+#pragma unroll
+      for (int bx = 0; bx < D / 32; ++bx) tc::tma_store_3d(&a.o, sO + bx * (BLK * 128), bx * 32, qb * BLK, pair);
+      tc::bulk_commit();
+      tc::bulk_wait_read_all();  // shared memory stays valid until the stores have read it
     }
     griddep_launch();
   }
@@ -643,18 +657,20 @@ EncodeTiled encoder() {
   return fn;
 }
 
-// Tensor map of a [P, L, D] fp16 array (16-byte aligned): 64 x 128 x 1
-// boxes, 128-byte swizzle, zeros past the ends.
-bool encode_map(CUtensorMap* m, const void* base, int D, int L, int P) {
+// Tensor map of a [P, L, D] array (16-byte aligned) of fp16 (boxes 64 x 128
+// x 1) or fp32 (boxes 32 x 128 x 1): 128-byte rows of a box, 128-byte
+// swizzle, zeros past the ends on loads, clipping on stores.
+bool encode_map(CUtensorMap* m, const void* base, int D, int L, int P, bool f32 = false) {
   const EncodeTiled enc = encoder();
   if (!enc || !base) return false;
+  const cuuint64_t e = f32 ? 4 : 2;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(P)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(L) * D * 2};
-  const cuuint32_t box[3] = {64, BLK, 1};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * e, static_cast<cuuint64_t>(L) * D * e};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / e), BLK, 1};
   const cuuint32_t estride[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estride,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base),
+             dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <typename Kern>
@@ -678,7 +694,7 @@ bool make_args(TcArgs& a, const PrefillParams& prm, int D, int pairs, bool with_
   a = TcArgs{};
   a.prm = prm;
   return encode_map(&a.q, prm.q, D, prm.L, pairs) && encode_map(&a.k, prm.k, D, prm.L, pairs) &&
-         (!with_v || encode_map(&a.v, prm.v, D, prm.L, pairs));
+         (!with_v || (encode_map(&a.v, prm.v, D, prm.L, pairs) && encode_map(&a.o, prm.out, D, prm.L, pairs, true)));
 }
 
 }  // namespace
