@@ -198,13 +198,16 @@ struct Layout {
   static constexpr size_t wbuf = (blk + 12 * (NCW + 1) + 16 + 15) / 16 * 16;  // per-warp row weights
   static constexpr size_t stages = (wbuf + NCW * 64 * 4 + 127) / 128 * 128;
   __host__ __device__ static size_t tail(int nstage) { return stages + static_cast<size_t>(nstage) * STAGE; }
-  __host__ __device__ static size_t bytes(int nstage, int chunk) {
+  __host__ __device__ static size_t bytes(int nstage, int chunk, int /*splits*/) {
     return tail(nstage) + static_cast<size_t>(chunk) * 12;  // logits, scores, positions
   }
 };
 
 __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_arrive_release() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
@@ -267,6 +270,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
     fence_mbar_init();
   }
   __syncthreads();
+  // The cluster's CTAs exchange partial results by writing into each other's
+  // shared memory; this arrival (waited for before the first such write)
+  // guarantees every peer has started.
+  if (S > 1) cluster_arrive_relaxed();
 
   float m = kNeg, l = 0.f, o[EPV];
 #pragma unroll
@@ -431,24 +438,29 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
     }
   }
   // A pair handled by one CTA needs no cluster barrier or distributed shared
-  // memory: plain block barriers and local shared memory do.
+  // memory: plain block barriers and local shared memory do.  In a cluster,
+  // every CTA writes its partial softmax (m, l) into each peer's g_m / g_l
+  // slot, then one cluster barrier makes them visible.  Rank 0 reads the
+  // peers' partial output rows from their shared memory before the second
+  // cluster barrier, after which no CTA touches another's shared memory.
   const bool clustered = S > 1;
-  if (clustered)
-    cluster.sync();  // (1) every CTA's partial softmax is published
-  else
+  if (clustered) {
+    __syncthreads();         // xo / xch of this CTA are complete (all 160 threads)
+    cluster_wait_acquire();  // every peer has started (the arrival at entry)
+    if (tid < S) {
+      cluster.map_shared_rank(g_m, tid)[rank] = xch->m;
+      cluster.map_shared_rank(g_l, tid)[rank] = xch->l;
+      if (rank == 0) cluster.map_shared_rank(g_self, tid)[0] = xch->s_self;
+    }
+    cluster.sync();  // (1) every CTA's partial softmax is in every CTA
+  } else {
     __syncthreads();
+  }
 
   // the pair's normaliser: merged over the cluster's CTAs, or, for a pair
   // handled by one CTA, this CTA's own (published before the barrier above)
   float M = kNeg, Ls = 0.f, sself;
   if (clustered) {
-    if (tid < S) {
-      const Xch* rx = cluster.map_shared_rank(xch, tid);
-      g_m[tid] = rx->m;
-      g_l[tid] = rx->l;
-      if (tid == 0) g_self[0] = rx->s_self;
-    }
-    __syncthreads();
     for (int r = 0; r < S; ++r) M = fmaxf(M, g_m[r]);
     for (int r = 0; r < S; ++r) Ls = fmaf(g_l[r], exp2f(g_m[r] - M), Ls);
     sself = g_self[0];
@@ -515,18 +527,15 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
 
   int u;
   if (clustered) {
-    if (tid == 0) {
-      xch->key = bk;
-      xch->slot = bslot;
+    // every thread holds this CTA's candidate (bk, bslot): thread r writes it
+    // into peer r's slot for this rank, then the barrier makes all visible;
+    // after it no CTA touches another's shared memory, so none waits at exit
+    if (tid < S) {
+      cluster.map_shared_rank(g_key, tid)[rank] = bk;
+      cluster.map_shared_rank(g_slot, tid)[rank] = bslot;
     }
-    cluster.sync();  // (2) every CTA's candidate is published
+    cluster.sync();  // (2) every CTA's candidate is in every CTA
     if (full) {
-      if (tid < S) {
-        const Xch* rx = cluster.map_shared_rank(xch, tid);
-        g_key[tid] = rx->key;
-        g_slot[tid] = rx->slot;
-      }
-      __syncthreads();
       unsigned long long best = ~0ull;
       u = -1;
       for (int r = 0; r < S; ++r)
@@ -541,7 +550,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
     u = full ? bslot : count;
   }
   if (full && u < 0 && tid == 0) atomicOr(prm.err, ERR_NO_CANDIDATE);
-  if (clustered) cluster_arrive_release();  // this CTA reads no more remote shared memory
+  // Clusters of more than two CTAs leave together (measured faster for 8-CTA
+  // clusters, slower for pairs of CTAs); nothing remote is read after (2).
+  const bool leave_together = S > 2;
+  if (leave_together) cluster_arrive_release();
 
   // write back: scores of this CTA's slots, the new token into slot u
   for (int j = tid; j < nrows; j += NT) prm.score[slot0 + j] = (lo + j == u) ? p_self : sc[j];
@@ -561,7 +573,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
     *reinterpret_cast<int4*>(prm.ctr + pair) = make_int4(p + 1, full ? C : count + 1, (head + 1) % R, 0);
     if (prm.evicted) prm.evicted[pair] = full ? u : -1;
   }
-  if (clustered) cluster_wait_acquire();  // (3) peers are done reading this CTA's shared memory
+  if (leave_together) cluster_wait_acquire();
 }
 
 // ------------------------------------------------------------ warp per pair
@@ -860,12 +872,12 @@ struct Kern {
   using Lay = Layout<D, NCW, Cfg::STAGE>;
   static constexpr auto fn = decode_kernel<T, D, NCW, TILE>;
 
-  static size_t smem(int nstage, int chunk) { return Lay::bytes(nstage, chunk); }
+  static size_t smem(int nstage, int chunk, int splits) { return Lay::bytes(nstage, chunk, splits); }
 
   static cudaError_t attrs() {
     // raised once for the largest configuration, so later launches (also
     // inside stream capture) make no attribute calls
-    size_t most = Lay::bytes(kMaxStages, kMaxChunk);
+    size_t most = Lay::bytes(kMaxStages, kMaxChunk, 16);
     if (most > 227 * 1024) most = 227 * 1024;
     return kernel_attrs(reinterpret_cast<const void*>(fn), most, true);
   }
@@ -876,7 +888,7 @@ struct Kern {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(splits, pairs, 1);
     cfg.blockDim = dim3(Cfg::NT, 1, 1);
-    cfg.dynamicSmemBytes = smem(prm.nstage, prm.chunk);
+    cfg.dynamicSmemBytes = smem(prm.nstage, prm.chunk, splits);
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -893,7 +905,7 @@ struct Kern {
   // CTAs that can be resident at once for this shape (0 = cannot launch)
   static int resident(int splits, int nstage, int chunk, int pairs, int sms) {
     if (attrs() != cudaSuccess) return 0;
-    const size_t bytes = smem(nstage, chunk);
+    const size_t bytes = smem(nstage, chunk, splits);
     if (bytes > 227 * 1024) return 0;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, Cfg::NT, bytes) != cudaSuccess) return 0;
