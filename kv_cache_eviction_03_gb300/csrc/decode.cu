@@ -178,10 +178,9 @@ __device__ __forceinline__ void merge_groups(float& m, float& l, float (&o)[RowG
 
 constexpr int kMaxStages = 16;
 
+// A CTA's merged partial softmax (max, normaliser, self logit).
 struct __align__(16) Xch {
   float m, l, s_self, pad;
-  unsigned long long key;
-  int slot, pad2;
 };
 
 // Shared-memory layout (bytes); identical on host and device.  The stage ring
