@@ -246,14 +246,36 @@ def test_import_rejects_bad_counters():
     B.h2o_cache_destroy(cache)
 
 
-def test_graph_replay_matches_eager():
-    """Counters live on the device, so a captured step replays correctly."""
+WARP_TYPES = [
+    # name, D, dtype: the warp-per-pair kernel's other instantiations
+    ("f16-d64", 64, "f16"),
+    ("f32-d128", 128, "f32"),
+    ("f32-d64", 64, "f32"),
+]
+
+
+@pytest.mark.parametrize("case", WARP_TYPES, ids=[c[0] for c in WARP_TYPES])
+def test_warp_per_pair_dtypes_and_head_dims(case):
+    """Every K/V type and head width of the warp-per-pair kernel, with more
+    pairs than warps (ragged C = 45, fill phase then evictions)."""
+    name, D, dt = case
+    w = W.Workload("warp-" + name, 24, 100, D, dt, 30, 24, 23, 22, 1.1)
+    rep = run_stepwise(w, 37, check={0, 7, 14, 15, 16, 23}, splits=B.H2O_DECODE_WARP_PER_PAIR, stages=3)
+    assert rep.pairs == w.pairs * 6
+
+
+@pytest.mark.parametrize("splits", [0, B.H2O_DECODE_WARP_PER_PAIR])
+def test_graph_replay_matches_eager(splits):
+    """Counters live on the device, so a captured step replays correctly
+    (automatic cluster shape, and the warp-per-pair kernel)."""
     w = W.Workload("graph", 2, 4, 128, "f16", 64, 24, 16, 16, 1.1)
     q, k, v = (torch.from_numpy(a).cuda() for a in W.prefill_inputs(w, 3))
     seq = [tuple(torch.from_numpy(a).cuda() for a in W.decode_inputs(w, w.prompt + t, 3)) for t in range(w.decode)]
     res = []
     for use_graph in (False, True):
         cache = B.h2o_cache_create(w.batch, w.heads, w.head_dim, w.heavy, w.recent, B.H2O_F16)
+        if splits:
+            B.h2o_cache_set_decode_shape(cache, splits)
         B.h2o_prefill(cache, q, k, v, w.scale)
         xq, xk, xv = (torch.empty_like(seq[0][0]) for _ in range(3))
         out = torch.empty((w.batch, w.heads, w.head_dim), dtype=torch.float32, device="cuda")
