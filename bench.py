@@ -260,6 +260,17 @@ def run_ours(args, rank, world, local_rank):
             decode_all(inp, dout, dev_ev)
         return g_pre, g_dec
 
+    def capture_layers(inp, pout):
+        """One prefill graph per layer, so each can wait for its own inputs."""
+        gs = []
+        for l in range(NL):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                q, k, v = inp["prefill"][l]
+                B.h2o_prefill(caches[l], q, k, v, w.scale, out=pout, stream=stream)
+            gs.append(g)
+        return gs
+
     # eager pass: allocates the prefill workspaces, checks every call works
     prefill_all(inp, pout)
     decode_all(inp, dout, dev_ev)
@@ -335,7 +346,8 @@ def run_ours(args, rank, world, local_rank):
     }
     # ---- end to end through the public API with pinned host buffers
     if not args.no_e2e:
-        result["e2e"] = run_e2e(args, w, NL, stream, (inp, pout, dout, dev_ev, g_pre, g_dec), capture, world, dist)
+        result["e2e"] = run_e2e(args, w, NL, stream, (inp, pout, dout, dev_ev, capture_layers(inp, pout), g_dec),
+                                capture, capture_layers, world, dist)
     del inp
     if dist:
         dist.barrier()
@@ -343,13 +355,14 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
-def run_e2e(args, w, NL, stream, set_a, capture, world, dist):
+def run_e2e(args, w, NL, stream, set_a, capture, capture_layers, world, dist):
     """The same step through the public API with pinned host buffers: every
     step copies all of its inputs host -> device and reads its decode outputs
-    and evicted slots back.  Two device buffer sets (each with its own pair of
-    graphs) let step s+1's host -> device copy and step s-1's read-back run
-    on copy streams while step s computes; every step's bytes still cross
-    the link inside the timed region."""
+    and evicted slots back.  Two device buffer sets (each with its own graphs:
+    one prefill graph per layer and the decode graph) let step s+1's
+    host -> device copy and step s-1's read-back run on copy streams while
+    step s computes, and each layer's prefill waits only for its own inputs;
+    every step's bytes still cross the link inside the timed region."""
     import torch
 
     def pinned(x):
@@ -362,13 +375,15 @@ def run_e2e(args, w, NL, stream, set_a, capture, world, dist):
     host_dec = [[pinned(x) for x in inp_a["decode"][l]] for l in range(NL)]
     inp_b = {k: [[torch.empty_like(x) for x in inp_a[k][l]] for l in range(NL)] for k in ("prefill", "decode")}
     pout_b, dout_b, ev_b = (torch.empty_like(x) for x in set_a[1:4])
-    sets = [set_a, (inp_b, pout_b, dout_b, ev_b) + capture(inp_b, pout_b, dout_b, ev_b)]
+    sets = [set_a, (inp_b, pout_b, dout_b, ev_b, capture_layers(inp_b, pout_b),
+                    capture(inp_b, pout_b, dout_b, ev_b)[1])]
     host_out = [torch.empty(set_a[2].shape, dtype=set_a[2].dtype, pin_memory=True) for _ in range(2)]
     host_ev = [torch.empty(set_a[3].shape, dtype=set_a[3].dtype, pin_memory=True) for _ in range(2)]
     h2d_bytes = sum(x.numel() * x.element_size() for l in range(NL) for x in host_pre[l] + host_dec[l])
     d2h_bytes = host_out[0].numel() * 4 + host_ev[0].numel() * 4
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of set X are on the device
+    ev_layer = [[torch.cuda.Event() for _ in range(NL)] for _ in range(2)]  # set X, layer l's prompt is on the device
+    ev_dec = [torch.cuda.Event() for _ in range(2)]   # set X's decode inputs are on the device
     ev_done = [torch.cuda.Event() for _ in range(2)]  # the step on set X has finished
     ev_out = [torch.cuda.Event() for _ in range(2)]   # outputs of set X are on the host
 
@@ -378,17 +393,23 @@ def run_e2e(args, w, NL, stream, set_a, capture, world, dist):
             up.wait_event(ev_done[x])  # the previous step on this set has read its inputs
         with torch.cuda.stream(up):
             for l in range(NL):
-                for dst, src in zip(inp["prefill"][l] + inp["decode"][l], host_pre[l] + host_dec[l]):
+                for dst, src in zip(inp["prefill"][l], host_pre[l]):
                     dst.copy_(src, non_blocking=True)
-        ev_in[x].record(up)
+                ev_layer[x][l].record(up)
+            for l in range(NL):
+                for dst, src in zip(inp["decode"][l], host_dec[l]):
+                    dst.copy_(src, non_blocking=True)
+            ev_dec[x].record(up)
 
     def compute(x, first):
         g_pre, g_dec = sets[x][4], sets[x][5]
-        stream.wait_event(ev_in[x])
         if not first:
             stream.wait_event(ev_out[x])  # the previous step's outputs on this set are read back
-        if not args.decode_only:
-            g_pre.replay()
+        for l in range(NL):
+            stream.wait_event(ev_layer[x][l])
+            if not args.decode_only:
+                g_pre[l].replay()
+        stream.wait_event(ev_dec[x])
         g_dec.replay()
         ev_done[x].record(stream)
 
