@@ -277,7 +277,8 @@ def run_ours(args, rank, world, local_rank):
     for c in caches:
         B.h2o_cache_check(c, stream=stream)
     g_pre, g_dec = capture(inp, pout, dout, dev_ev)
-    launches_per_step = (0 if args.decode_only else 3 * NL) + T * NL
+    # per layer: row statistics, attention output, column sums, keep rule; per decode step and layer: one
+    launches_per_step = (0 if args.decode_only else 4 * NL) + T * NL
 
     def step(evs=None):
         if not args.decode_only:
