@@ -178,6 +178,7 @@ void h2o_cache_destroy(h2o_cache* c) {
   cudaFree(c->ctr);
   cudaFree(c->err);
   cudaFree(c->ws);
+  cudaFree(c->wsp);
   delete c;
 }
 
@@ -216,6 +217,20 @@ static int prefill_impl(h2o_cache* c, const void* q, const void* k, const void* 
       return cuda_fail(e, "h2o_prefill: workspace cudaMalloc");
     c->ws_len = need;
   }
+  // with the attention output on the tensor-core path, the output pass also
+  // produces the column sums, through a partials workspace
+  const size_t need_p = (out_or_null && c->dtype == H2O_F16) ? h2o::colsum_partial_floats(prompt_len, c->P) : 0;
+  if (need_p > c->wsp_len) {
+    if (c->wsp) {
+      if ((e = cudaStreamSynchronize(as_stream(stream))) != cudaSuccess) return cuda_fail(e, "h2o_prefill: sync");
+      cudaFree(c->wsp);
+      c->wsp = nullptr;
+      c->wsp_len = 0;
+    }
+    if ((e = cudaMalloc(&c->wsp, need_p * sizeof(float))) != cudaSuccess)
+      return cuda_fail(e, "h2o_prefill: partials workspace cudaMalloc");
+    c->wsp_len = need_p;
+  }
   const size_t plen = static_cast<size_t>(c->P) * prompt_len;
   h2o::PrefillParams pp;
   pp.q = q;
@@ -229,6 +244,7 @@ static int prefill_impl(h2o_cache* c, const void* q, const void* k, const void* 
   pp.err = c->err;
   pp.lens = lens;
   pp.heads = c->H;
+  pp.cs_part = need_p ? c->wsp : nullptr;
   cudaStream_t s = as_stream(stream);
   touch_stream(c, stream);
   if ((e = h2o::launch_prefill_stats(pp, c->dtype, c->D, c->P, s)) != cudaSuccess)

@@ -60,7 +60,16 @@ struct PrefillParams {
   int* err = nullptr;  // device error bits, or nullptr
   const int* lens = nullptr;  // [B] per-batch-row prompt lengths (device), or nullptr: all L
   int heads = 1;              // pairs per batch row (maps a pair to its length)
+  // When the output pass runs: column-sum partials it writes, one 128-float
+  // row per (query block qb, key block kb <= qb, TMEM lane quarter), reduced
+  // into colsum afterwards; nullptr: the column pass computes colsum.
+  float* cs_part = nullptr;
 };
+// Floats of the column-sum partials for prompts of L rows (stride) and P pairs.
+__host__ __device__ inline size_t colsum_partial_floats(int L, int P) {
+  const size_t nb = (static_cast<size_t>(L) + 127) / 128;
+  return static_cast<size_t>(P) * (nb * (nb + 1) / 2) * 4 * 128;
+}
 
 struct SelectParams {
   const void* k;         // prompt keys   [P, L, D]
@@ -123,6 +132,8 @@ int decode_warp_default_stages(int dtype, int D, int C, int pairs);
 
 cudaError_t launch_prefill_stats(const PrefillParams& prm, int dtype, int D, int pairs, cudaStream_t s);
 cudaError_t launch_prefill_colsum(const PrefillParams& prm, int dtype, int D, int pairs, cudaStream_t s);
+// colsum from the output pass's partials (prm.cs_part)
+cudaError_t launch_colsum_reduce(const PrefillParams& prm, int pairs, cudaStream_t s);
 // fp16 passes on tcgen05 (row statistics without the attention output)
 cudaError_t launch_prefill_stats_tc(const PrefillParams& prm, int D, int pairs, cudaStream_t s);
 cudaError_t launch_prefill_colsum_tc(const PrefillParams& prm, int D, int pairs, cudaStream_t s);
@@ -147,6 +158,9 @@ struct h2o_cache {
   // prefill workspace, grown on demand: lse2 and colsum, [P, ws_len] each
   float* ws;
   size_t ws_len;
+  // column-sum partials of the output pass (colsum_partial_floats), grown on demand
+  float* wsp;
+  size_t wsp_len;
   int device, num_sms;
   int splits_override, stages_override;
   h2o::DecodeShape shape_auto;

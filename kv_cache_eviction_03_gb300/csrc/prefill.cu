@@ -478,7 +478,8 @@ cudaError_t launch_prefill_stats(const PrefillParams& prm, int dtype, int D, int
 
 cudaError_t launch_prefill_colsum(const PrefillParams& prm, int dtype, int D, int pairs, cudaStream_t s) {
   if (prm.L <= 0) return cudaSuccess;
-  if (dtype == 0 && prefill_use_tc()) return launch_prefill_colsum_tc(prm, D, pairs, s);
+  if (dtype == 0 && prefill_use_tc())  // with the output, the output pass left partials to reduce
+    return prm.out && prm.cs_part ? launch_colsum_reduce(prm, pairs, s) : launch_prefill_colsum_tc(prm, D, pairs, s);
   if (dtype == 0) {
     const dim3 grid((prm.L + BN - 1) / BN, pairs);
     const size_t smem = static_cast<size_t>(BM) * D * 2 * 3 + 2 * BM * sizeof(float);

@@ -420,6 +420,8 @@ __global__ void __launch_bounds__(NT, 1) out_tc(const __grid_constant__ TcArgs a
     const int rl = quarter * 32 + lane;  // TMEM lane = query row qb * BLK + rl
     const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
     const float lse = lse_at(prm.lse2 + static_cast<size_t>(pair) * L, qb * BLK, rl, Lp);
+    // this pair's column-sum partials: one 4 x 128-float row per (query block, key block <= it)
+    float* cs_part = prm.cs_part ? prm.cs_part + static_cast<size_t>(pair) * colsum_partial_floats(L, 1) : nullptr;
     bool ok = true;
     for (int j = 0; ok && j < n; ++j) {
       const int b = j & 1;
@@ -434,19 +436,33 @@ __global__ void __launch_bounds__(NT, 1) out_tc(const __grid_constant__ TcArgs a
         tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + col0), v);
         if (j == qb) {  // diagonal block: key col0 + e is visible to row rl if it is <= rl
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float p0 = col0 + 2 * e <= rl ? ex2(fmaf(v[2 * e], prm.qscale, -lse)) : 0.f;
-            const float p1 = col0 + 2 * e + 1 <= rl ? ex2(fmaf(v[2 * e + 1], prm.qscale, -lse)) : 0.f;
-            ph[c * 16 + e] = tc::cvt_half2(p0, p1);
-          }
+          for (int e = 0; e < 32; ++e) v[e] = col0 + e <= rl ? ex2(fmaf(v[e], prm.qscale, -lse)) : 0.f;
         } else {
           const uint64_t qs2 = f2_pack(prm.qscale, prm.qscale), nl2 = f2_pack(-lse, -lse);
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             float x0, x1;
             f2_unpack(f2_fma(f2_pack(v[2 * e], v[2 * e + 1]), qs2, nl2), x0, x1);
-            ph[c * 16 + e] = tc::cvt_half2(ex2(x0), ex2(x1));
+            v[2 * e] = ex2(x0);
+            v[2 * e + 1] = ex2(x1);
           }
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) ph[c * 16 + e] = tc::cvt_half2(v[2 * e], v[2 * e + 1]);
+        if (cs_part) {
+          // column sums over this warp's 32 rows (a reduce-scatter: after it
+          // lane t holds column col0 + t), one 128-byte store per warp
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) {
+            const bool hi = (lane & off) != 0;
+#pragma unroll
+            for (int i = 0; i < off; ++i) {
+              const float keep = hi ? v[i + off] : v[i];
+              const float send = hi ? v[i] : v[i + off];
+              v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            }
+          }
+          cs_part[(static_cast<size_t>(qb) * (qb + 1) / 2 + j) * (4 * BLK) + quarter * BLK + col0 + lane] = v[0];
         }
       }
       // probability block b (TMEM) was last read by O(j-2); this thread's 64
@@ -636,6 +652,31 @@ __global__ void __launch_bounds__(NT, 2) colsum_tc(const __grid_constant__ TcArg
   tmem_teardown(warp, lane, drain, tbase, 256, err);
 }
 
+// ------------------------------------------------- column sums from partials
+// colsum_j = sum over query blocks qb >= j / 128 and the four TMEM lane
+// quarters of the output pass's partial column sums, in that fixed order, in
+// float64 (each partial is a float32 sum over 32 rows).
+__global__ void __launch_bounds__(BLK) colsum_reduce_kernel(const PrefillParams prm) {
+  griddep_wait();
+  const int pair = blockIdx.y, kb = blockIdx.x, col = threadIdx.x;
+  const int L = prm.L;
+  const int Lp = pair_len(prm.lens, prm.heads, L, pair);
+  const int nbp = (Lp + BLK - 1) / BLK;  // query blocks the output pass ran for this pair
+  if (kb >= nbp) return;
+  const float* part = prm.cs_part + static_cast<size_t>(pair) * colsum_partial_floats(L, 1) + col;
+  double acc = 0.0;
+  for (int qb = kb; qb < nbp; ++qb) {
+    const float* row = part + (static_cast<size_t>(qb) * (qb + 1) / 2 + kb) * (4 * BLK);
+    acc += static_cast<double>(row[0]);
+    acc += static_cast<double>(row[BLK]);
+    acc += static_cast<double>(row[2 * BLK]);
+    acc += static_cast<double>(row[3 * BLK]);
+  }
+  griddep_launch();
+  const int key = kb * BLK + col;
+  if (key < Lp) prm.colsum[static_cast<size_t>(pair) * L + key] = static_cast<float>(acc);
+}
+
 // ------------------------------------------------------------------ host
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -710,6 +751,20 @@ cudaError_t launch_prefill_stats_tc(const PrefillParams& prm, int D, int pairs, 
   if (e != cudaSuccess || prm.out == nullptr) return e;
   return D == 128 ? launch_tc(out_tc<128>, grid, OutCfg<128>::bytes, s, args)
                   : launch_tc(out_tc<64>, grid, OutCfg<64>::bytes, s, args);
+}
+
+cudaError_t launch_colsum_reduce(const PrefillParams& prm, int pairs, cudaStream_t s) {
+  if (prm.L <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((prm.L + BLK - 1) / BLK, pairs);
+  cfg.blockDim = dim3(BLK);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, colsum_reduce_kernel, prm);
 }
 
 cudaError_t launch_prefill_colsum_tc(const PrefillParams& prm, int D, int pairs, cudaStream_t s) {
