@@ -360,18 +360,23 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
       blk_int[2] = count;
       blk_int[3] = head;
     }
+    // q, and for the self term k_new and v_new, requested together (one
+    // round trip rather than three)
+    const size_t in_off = static_cast<size_t>(pair) * ROWB + lig * 16;
+    const uint4 q4 = *reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(prm.q) + in_off);
+    uint4 k4 = make_uint4(0, 0, 0, 0), v4 = make_uint4(0, 0, 0, 0);
+    if (rank == 0 && warp == 0) {
+      k4 = *reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(prm.k_new) + in_off);
+      v4 = *reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(prm.v_new) + in_off);
+    }
     float qv[EPV];
-    Vec16<T>::unpack(*reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(prm.q) +
-                                                     static_cast<size_t>(pair) * ROWB + lig * 16),
-                     qv);
+    Vec16<T>::unpack(q4, qv);
 #pragma unroll
     for (int e = 0; e < EPV; ++e) qv[e] *= prm.qscale;  // exp2(logit) is the softmax numerator
     if (rank == 0 && warp == 0) {
       // the new token attends to itself: row group 0 of warp 0 starts from it
       float kf[EPV];
-      Vec16<T>::unpack(*reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(prm.k_new) +
-                                                       static_cast<size_t>(pair) * ROWB + lig * 16),
-                       kf);
+      Vec16<T>::unpack(k4, kf);
       float acc = 0.f;
 #pragma unroll
       for (int e = 0; e < EPV; ++e) acc = fmaf(qv[e], kf[e], acc);
@@ -379,9 +384,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
       for (int off = LPR / 2; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
       s_self = acc;
       if (grp == 0) {
-        Vec16<T>::unpack(*reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(prm.v_new) +
-                                                         static_cast<size_t>(pair) * ROWB + lig * 16),
-                         o);
+        Vec16<T>::unpack(v4, o);
         m = s_self;
         l = 1.f;
       }
