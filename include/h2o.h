@@ -76,7 +76,9 @@ H2O_API void h2o_cache_destroy(h2o_cache* cache);
  * the cache held.  q, k, v: [B, H, L, D] kv_dtype.  out_or_null: [B, H, L, D]
  * float32 causal attention output, or NULL to skip it.  prompt_len = 0 empties
  * the cache.  The first prefill at a new maximum prompt length allocates its
- * column-sum workspace (cudaMalloc); later ones allocate nothing. */
+ * workspaces (cudaMalloc: row statistics and column sums, and with fp16 K/V
+ * and an output also the output pass's column-sum partials, 2 KB per pair per
+ * pair of 128-token blocks); later ones allocate nothing. */
 H2O_API int h2o_prefill(h2o_cache* cache, const void* q, const void* k, const void* v, int prompt_len,
                 float scale, float* out_or_null, void* stream);
 
