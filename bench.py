@@ -388,10 +388,15 @@ def run_e2e(args, w, NL, stream, set_a, capture, capture_layers, world, dist):
     ev_done = [torch.cuda.Event() for _ in range(2)]  # the step on set X has finished
     ev_out = [torch.cuda.Event() for _ in range(2)]   # outputs of set X are on the host
 
+    copy_ev = []  # (start, end) events around each step's host -> device copies
+
     def h2d(x, first):
         inp = sets[x][0]
         if not first:
             up.wait_event(ev_done[x])  # the previous step on this set has read its inputs
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(up)
+        copy_ev.append((c0, c1))
         with torch.cuda.stream(up):
             for l in range(NL):
                 for dst, src in zip(inp["prefill"][l], host_pre[l]):
@@ -401,6 +406,7 @@ def run_e2e(args, w, NL, stream, set_a, capture, capture_layers, world, dist):
                 for dst, src in zip(inp["decode"][l], host_dec[l]):
                     dst.copy_(src, non_blocking=True)
             ev_dec[x].record(up)
+        c1.record(up)
 
     def compute(x, first):
         g_pre, g_dec = sets[x][4], sets[x][5]
@@ -435,6 +441,7 @@ def run_e2e(args, w, NL, stream, set_a, capture, capture_layers, world, dist):
 
     run(max(2, min(args.warmup, 3)))
     torch.cuda.synchronize()
+    copy_ev.clear()
     if dist:
         dist.barrier()
     a = torch.cuda.Event(enable_timing=True)
@@ -446,8 +453,10 @@ def run_e2e(args, w, NL, stream, set_a, capture, capture_layers, world, dist):
     torch.cuda.synchronize()
     el = a.elapsed_time(b) / 1e3
     el = sharding.max_over_ranks([el], dist, device="cuda")[0]
+    copy_s = sum(c0.elapsed_time(c1) for c0, c1 in copy_ev) / 1e3 / max(len(copy_ev), 1)
     return {"value": w.batch * w.decode * world * NL * args.steps / el, "unit": UNIT,
             "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+            "h2d_gbps_measured": h2d_bytes / copy_s / 1e9 if copy_s > 0 else None,
             "pipelined": "step s+1 host->device copy and step s-1 read-back overlap step s"}
 
 
