@@ -218,8 +218,10 @@ static int prefill_impl(h2o_cache* c, const void* q, const void* k, const void* 
     c->ws_len = need;
   }
   // with the attention output on the tensor-core path, the output pass also
-  // produces the column sums, through a partials workspace
-  const size_t need_p = (out_or_null && c->dtype == H2O_F16) ? h2o::colsum_partial_floats(prompt_len, c->P) : 0;
+  // produces the column sums, through a partials workspace that grows with
+  // the square of the prompt; beyond 2 GB the column pass runs instead
+  size_t need_p = (out_or_null && c->dtype == H2O_F16) ? h2o::colsum_partial_floats(prompt_len, c->P) : 0;
+  if (need_p * sizeof(float) > (static_cast<size_t>(2) << 30)) need_p = 0;
   if (need_p > c->wsp_len) {
     if (c->wsp) {
       if ((e = cudaStreamSynchronize(as_stream(stream))) != cudaSuccess) return cuda_fail(e, "h2o_prefill: sync");

@@ -150,3 +150,28 @@ def test_prefill_budget_ratios(ratio):
     half = int(round(ratio * L / 2))
     w = W.Workload(f"budget{ratio}", 1, 4, 128, "f16", L, 0, half, half, 1.1)
     check_prefill(w, 53, with_out=False)
+
+
+def test_long_prompt_output_with_separate_column_pass():
+    """4096 pairs x 4096 tokens: the output pass's column-sum partials would
+    take ~4.4 GB, past the 2 GB cap, so the separate column pass runs next to
+    the output pass; sampled pairs against the oracle."""
+    Bn, H, L, D, hv, rc = 64, 64, 4096, 64, 100, 60
+    g = torch.Generator(device="cuda").manual_seed(5)
+    q, k, v = (torch.randn((Bn, H, L, D), generator=g, device="cuda").half() for _ in range(3))
+    cache = B.h2o_cache_create(Bn, H, D, hv, rc, B.H2O_F16)
+    out = torch.empty((Bn, H, L, D), dtype=torch.float32, device="cuda")
+    cs = torch.empty((Bn, H, L), dtype=torch.float32, device="cuda")
+    scale = 1 / math.sqrt(D)
+    B.h2o_prefill_ex(cache, q, k, v, scale, out=out, colsum=cs)
+    B.h2o_cache_check(cache)
+    g_pos = B.unpack_state(cache, B.h2o_cache_export_state(cache))["pos"]
+    for i in (0, 1, 2047, Bn * H - 1):
+        b, h = divmod(i, H)
+        qf, kf, vf = (x[b, h].double().cpu().numpy() for x in (q, k, v))
+        st, c, o = O.prefill_pair(qf, kf, vf, hv, rc, scale)
+        assert np.max(np.abs(cs[b, h].cpu().numpy() - c) / c) <= 1e-5
+        assert np.max(np.abs(out[b, h].cpu().numpy() - o)) <= 2e-3
+        if not np.array_equal(g_pos[i], st.pos):
+            assert heavy_boundary_gap(O.to_f32(c), L, hv, rc) <= NEAR_TIE
+    B.h2o_cache_destroy(cache)
