@@ -299,3 +299,38 @@ def test_graph_replay_matches_eager(splits):
         B.h2o_cache_destroy(cache)
     assert torch.equal(res[0][0], res[1][0])
     assert np.array_equal(res[0][1], res[1][1])
+
+
+def test_maximum_cache_size_every_step():
+    """The largest cache a pair may have (65,536 slots: 16 CTAs of 4,096), full,
+    from a seeded synthetic state deep into a stream, every step checked."""
+    Hh = Rr = 32768
+    C, D, P, p0 = Hh + Rr, 128, 2, 1_000_000
+    rng = np.random.default_rng(123)
+    cache = B.h2o_cache_create(1, P, D, Hh, Rr, B.H2O_F16)
+    heavy_pos = np.sort(rng.choice(p0 - Rr, size=Hh, replace=False))
+    pos = np.concatenate([heavy_pos, np.arange(p0 - Rr, p0)])
+    K = rng.standard_normal((P, C, D)).astype(np.float16).astype(np.float64)
+    V = rng.standard_normal((P, C, D)).astype(np.float16).astype(np.float64)
+    score = O.to_f32(rng.pareto(1.5, size=(P, C)) * 0.05 + 1e-4)
+    ring = np.tile(np.arange(Hh, C), (P, 1))
+    st = O.CacheState(K, V, score, np.tile(pos, (P, 1)), ring, np.zeros(P, dtype=np.int64), np.full(P, C),
+                      np.full(P, p0))
+    out = torch.empty((1, P, D), dtype=torch.float32, device="cuda")
+    ev = torch.empty((1, P), dtype=torch.int32, device="cuda")
+    rep = StepReport()
+    scale = 1 / np.sqrt(D)
+    for t in range(4):
+        qd, kd, vd = (rng.standard_normal((1, P, D)).astype(np.float16) for _ in range(3))
+        nxt, r_out, r_ev, gap = O.decode_step(st, qd, kd, vd, Hh, Rr, scale)
+        B.h2o_cache_import_state(cache, oracle_image(cache, st))
+        B.h2o_decode_step(cache, torch.from_numpy(qd).cuda(), torch.from_numpy(kd).cuda(),
+                          torch.from_numpy(vd).cuda(), scale, out, ev)
+        B.h2o_cache_check(cache)
+        after = B.unpack_state(cache, B.h2o_cache_export_state(cache))
+        compare_decode_step(cache, after, out.cpu().numpy().reshape(P, D), ev.cpu().numpy().reshape(P), st, nxt,
+                            r_out, r_ev, gap, rep, inputs=(flat(qd), flat(kd), flat(vd)), scale=scale)
+        st = nxt
+    assert rep.pairs == 4 * P
+    assert B.h2o_cache_info(cache)[6] == 16  # 16 CTAs of 4,096 slots
+    B.h2o_cache_destroy(cache)
