@@ -25,14 +25,20 @@
 // previous kernel; only reads of the step's inputs (q, k_new, v_new) and all
 // writes wait for it.
 //
-// The cluster's CTAs then exchange partial (m, l, o) through distributed
-// shared memory, so every CTA knows the pair's global max and normaliser
-// without a second pass over K: each turns its own logits (kept in shared
-// memory) into probabilities, adds them to its slots' scores, and proposes its
-// lowest candidate key (score bits, position) packed in 64 bits (non-negative
-// float bits order like the floats).  The cluster minimum is the victim; the
-// CTA that owns it writes the new row.  Cluster barriers are hardware barriers
-// of co-scheduled CTAs: no CTA spins on another.
+// The cluster's CTAs then exchange partial (m, l) by writing them into each
+// other's distributed shared memory ahead of a cluster barrier, so every CTA
+// knows the pair's global max and normaliser without a second pass over K
+// (rank 0 also gathers the partial output rows): each turns its own logits
+// (kept in shared memory) into probabilities, adds them to its slots'
+// scores, and proposes its lowest candidate key (score bits, position) packed
+// in 64 bits (non-negative float bits order like the floats), again written
+// into every peer.  The cluster minimum is the victim; the CTA that owns it
+// writes the new row.  Cluster barriers are hardware barriers of co-scheduled
+// CTAs: no CTA spins on another.  A pair handled by a single CTA uses plain
+// block barriers and local shared memory instead.
+//
+// Many short pairs (thousands of pairs of up to 1024 slots) go to a second
+// kernel, decode_warp_kernel, further down: one warp per pair, persistent.
 #include <cooperative_groups.h>
 #include <cuda_fp16.h>
 
