@@ -48,6 +48,11 @@ constexpr int BLK = 128;                   // rows / columns of a logits block
 constexpr int NCOMP = 8;                   // compute warps: 4 TMEM lane quarters x 2 column halves
 constexpr int NT = (2 + NCOMP) * 32;       // + the TMA warp and the MMA warp
 constexpr int kCompBar = 1;                // named barrier of the compute warps
+// The output pass gives each compute warp a quarter of a block's columns (16
+// warps: four per TMEM lane quarter), so that more warps hide the latency
+// of its per-block chain (TMEM load, exponentials, reductions, TMEM store).
+constexpr int NCOMP_O = 16;
+constexpr int NT_O = (2 + NCOMP_O) * 32;
 
 // Log2-domain lse of query row row0 + t; rows past the prompt get a huge
 // value so that their probabilities exp2(s - lse) vanish without a mask.  A
@@ -318,7 +323,7 @@ __device__ __forceinline__ void issue_pv_t(uint32_t d_tmem, uint32_t p_tmem, con
 }
 
 template <int D>
-__global__ void __launch_bounds__(NT, 1) out_tc(const __grid_constant__ TcArgs a) {
+__global__ void __launch_bounds__(NT_O, 1) out_tc(const __grid_constant__ TcArgs a) {
   using Cfg = OutCfg<D>;
   constexpr int NK = Cfg::NK, NV = Cfg::NV, TB = Tile<D>::BYTES;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -346,7 +351,7 @@ __global__ void __launch_bounds__(NT, 1) out_tc(const __grid_constant__ TcArgs a
   // pfull[2]: one per compute warp; pempty[2], ofull, drain: a commit
   uint32_t counts[Cfg::NB];
 #pragma unroll
-  for (int i = 0; i < Cfg::NB; ++i) counts[i] = (i == 1 + 2 * NK + 2 * NV + 2 || i == 1 + 2 * NK + 2 * NV + 3) ? NCOMP : 1;
+  for (int i = 0; i < Cfg::NB; ++i) counts[i] = (i == 1 + 2 * NK + 2 * NV + 2 || i == 1 + 2 * NK + 2 * NV + 3) ? NCOMP_O : 1;
 
   if (threadIdx.x == 0) {
     tc::prefetch_tensormap(&a.q);
@@ -415,9 +420,10 @@ __global__ void __launch_bounds__(NT, 1) out_tc(const __grid_constant__ TcArgs a
       if (ok) tc::mma_commit(ofull);
     }
     __syncwarp();
-  } else {  // compute warps
-    const int quarter = warp & 3, half = (warp - 2) >> 2;
+  } else {  // compute warps: lane quarter (warp % 4) x column part (32 of the 128)
+    const int quarter = warp & 3, part = (warp - 2) >> 2;
     const int rl = quarter * 32 + lane;  // TMEM lane = query row qb * BLK + rl
+    const int col0 = part * 32;          // this warp's keys in a block / its O columns
     const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
     const float lse = lse_at(prm.lse2 + static_cast<size_t>(pair) * L, qb * BLK, rl, Lp);
     // this pair's column-sum partials: one 4 x 128-float row per (query block, key block <= it)
@@ -428,72 +434,67 @@ __global__ void __launch_bounds__(NT, 1) out_tc(const __grid_constant__ TcArgs a
       ok = wait_warp(&sfull[b], static_cast<uint32_t>((j >> 1) & 1), lane, err);
       if (!ok) break;
       tc::fence_after_sync();
-      uint32_t ph[32];  // this thread's 64 probabilities as fp16 pairs
+      float v[32];
+      tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + col0), v);
+      if (j == qb) {  // diagonal block: key col0 + e is visible to row rl if it is <= rl
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int col0 = half * 64 + c * 32;
-        float v[32];
-        tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + col0), v);
-        if (j == qb) {  // diagonal block: key col0 + e is visible to row rl if it is <= rl
+        for (int e = 0; e < 32; ++e) v[e] = col0 + e <= rl ? ex2(fmaf(v[e], prm.qscale, -lse)) : 0.f;
+      } else {
+        const uint64_t qs2 = f2_pack(prm.qscale, prm.qscale), nl2 = f2_pack(-lse, -lse);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = col0 + e <= rl ? ex2(fmaf(v[e], prm.qscale, -lse)) : 0.f;
-        } else {
-          const uint64_t qs2 = f2_pack(prm.qscale, prm.qscale), nl2 = f2_pack(-lse, -lse);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(v[2 * e], v[2 * e + 1]), qs2, nl2), x0, x1);
-            v[2 * e] = ex2(x0);
-            v[2 * e + 1] = ex2(x1);
-          }
-        }
-#pragma unroll
-        for (int e = 0; e < 16; ++e) ph[c * 16 + e] = tc::cvt_half2(v[2 * e], v[2 * e + 1]);
-        if (cs_part) {
-          // column sums over this warp's 32 rows (a reduce-scatter: after it
-          // lane t holds column col0 + t), one 128-byte store per warp
-#pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) {
-            const bool hi = (lane & off) != 0;
-#pragma unroll
-            for (int i = 0; i < off; ++i) {
-              const float keep = hi ? v[i + off] : v[i];
-              const float send = hi ? v[i] : v[i + off];
-              v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-            }
-          }
-          cs_part[(static_cast<size_t>(qb) * (qb + 1) / 2 + j) * (4 * BLK) + quarter * BLK + col0 + lane] = v[0];
+        for (int e = 0; e < 16; ++e) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(v[2 * e], v[2 * e + 1]), qs2, nl2), x0, x1);
+          v[2 * e] = ex2(x0);
+          v[2 * e + 1] = ex2(x1);
         }
       }
-      // probability block b (TMEM) was last read by O(j-2); this thread's 64
-      // keys go to its lane's 32 packed columns of that block
+      uint32_t ph[16];  // this thread's 32 probabilities as fp16 pairs
+#pragma unroll
+      for (int e = 0; e < 16; ++e) ph[e] = tc::cvt_half2(v[2 * e], v[2 * e + 1]);
+      // probability block b (TMEM) was last read by O(j-2); this thread's 32
+      // keys go to its lane's 16 packed columns of that block
       if (j >= 2 && !(ok = wait_warp(&pempty[b], static_cast<uint32_t>(((j - 2) >> 1) & 1), lane, err))) break;
-      tc::tmem_st32(lane_addr + kPcol + static_cast<uint32_t>(b * 64 + half * 32), ph);
+      tc::tmem_st16(lane_addr + kPcol + static_cast<uint32_t>(b * 64 + part * 16), ph);
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_plain(&pfull[b]);
+      if (cs_part) {
+        // while the tensor core works on P V: column sums over this warp's 32
+        // rows (a reduce-scatter: after it lane t holds column col0 + t), one
+        // 128-byte store per warp
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+          const bool hi = (lane & off) != 0;
+#pragma unroll
+          for (int i = 0; i < off; ++i) {
+            const float keep = hi ? v[i + off] : v[i];
+            const float send = hi ? v[i] : v[i + off];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+          }
+        }
+        cs_part[(static_cast<size_t>(qb) * (qb + 1) / 2 + j) * (4 * BLK) + quarter * BLK + col0 + lane] = v[0];
+      }
     }
     ok = ok && wait_warp(ofull, 0, lane, err);
     tc::fence_after_sync();
     // O leaves through shared memory (the key ring is free once every MMA has
     // completed): boxes of 128 rows x 32 floats in the 128-byte swizzle (row
     // r's 16-byte chunk c at chunk c ^ (r % 8): conflict-free for a warp's 32
-    // rows), written out by TMA stores clipped at the prompt's end.
+    // rows), written out by TMA stores clipped at the prompt's end.  Column
+    // part p of O is box p.
     unsigned char* sO = sK;
-    if (ok) {
+    if (ok && col0 < D) {
+      float o[32];
+      tc::tmem_ld32(lane_addr + kOcol + static_cast<uint32_t>(col0), o);
+      unsigned char* rowp = sO + part * (BLK * 128) + rl * 128;
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        float o[32];
-        tc::tmem_ld32(lane_addr + kOcol + static_cast<uint32_t>(half * (D / 2) + c * 32), o);
-        unsigned char* rowp = sO + (half * (D / 64) + c) * (BLK * 128) + rl * 128;
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          *reinterpret_cast<float4*>(rowp + ((e ^ (rl & 7)) << 4)) =
-              make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
-      }
+      for (int e = 0; e < 8; ++e)
+        *reinterpret_cast<float4*>(rowp + ((e ^ (rl & 7)) << 4)) =
+            make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
     }
     fence_proxy_async_smem();
-    tc::named_sync(kCompBar, NCOMP * 32);
+    tc::named_sync(kCompBar, NCOMP_O * 32);
     if (warp == 2 && lane == 0) {
 #pragma unroll
       for (int bx = 0; bx < D / 32; ++bx) tc::tma_store_3d(&a.o, sO + bx * (BLK * 128), bx * 32, qb * BLK, pair);
@@ -715,12 +716,12 @@ bool encode_map(CUtensorMap* m, const void* base, int D, int L, int P, bool f32 
 }
 
 template <typename Kern>
-cudaError_t launch_tc(Kern kern, dim3 grid, size_t smem, cudaStream_t s, const TcArgs& args) {
+cudaError_t launch_tc(Kern kern, dim3 grid, size_t smem, cudaStream_t s, const TcArgs& args, int threads = NT) {
   cudaError_t e = kernel_attrs(reinterpret_cast<const void*>(kern), smem, false);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(NT);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -749,8 +750,8 @@ cudaError_t launch_prefill_stats_tc(const PrefillParams& prm, int D, int pairs, 
   cudaError_t e = D == 128 ? launch_tc(stats_tc<128>, grid, StatsCfg<128>::bytes, s, args)
                            : launch_tc(stats_tc<64>, grid, StatsCfg<64>::bytes, s, args);
   if (e != cudaSuccess || prm.out == nullptr) return e;
-  return D == 128 ? launch_tc(out_tc<128>, grid, OutCfg<128>::bytes, s, args)
-                  : launch_tc(out_tc<64>, grid, OutCfg<64>::bytes, s, args);
+  return D == 128 ? launch_tc(out_tc<128>, grid, OutCfg<128>::bytes, s, args, NT_O)
+                  : launch_tc(out_tc<64>, grid, OutCfg<64>::bytes, s, args, NT_O);
 }
 
 cudaError_t launch_colsum_reduce(const PrefillParams& prm, int pairs, cudaStream_t s) {
