@@ -25,17 +25,20 @@
 // previous kernel; only reads of the step's inputs (q, k_new, v_new) and all
 // writes wait for it.
 //
-// The cluster's CTAs then exchange partial (m, l) by writing them into each
-// other's distributed shared memory ahead of a cluster barrier, so every CTA
-// knows the pair's global max and normaliser without a second pass over K
-// (rank 0 also gathers the partial output rows): each turns its own logits
-// (kept in shared memory) into probabilities, adds them to its slots'
-// scores, and proposes its lowest candidate key (score bits, position) packed
-// in 64 bits (non-negative float bits order like the floats), again written
-// into every peer.  The cluster minimum is the victim; the CTA that owns it
-// writes the new row.  Cluster barriers are hardware barriers of co-scheduled
-// CTAs: no CTA spins on another.  A pair handled by a single CTA uses plain
-// block barriers and local shared memory instead.
+// The cluster's CTAs then exchange their partial (m, l) without a second
+// pass over K: each pushes its pair into every peer's shared memory with
+// st.async stores whose bytes complete a transaction count on the receiver's
+// mbarrier (rank 0 also receives the other ranks' partial output rows), and
+// each waits only until the bytes it expects have landed.  Every CTA then
+// knows the pair's global max and normaliser, turns its own logits (kept in
+// shared memory) into probabilities, adds them to its slots' scores, and
+// pushes its lowest candidate key (score bits, position, packed in 64 bits:
+// non-negative float bits order like the floats) to every peer the same way.
+// The cluster minimum is the victim; the CTA that owns it writes the new row.
+// No CTA reads another's shared memory and every CTA waits for all bytes
+// pushed into it, so there is no cluster barrier after the one at entry that
+// guarantees every peer has set up its mbarriers.  A pair handled by a single
+// CTA uses plain block barriers and local shared memory instead.
 //
 // Many short pairs (thousands of pairs of up to 1024 slots) go to a second
 // kernel, decode_warp_kernel, further down: one warp per pair, persistent.
@@ -190,21 +193,28 @@ struct __align__(16) Xch {
 };
 
 // Shared-memory layout (bytes); identical on host and device.  The stage ring
-// depth and the CTA's slot count are launch parameters.
-template <int D, int NCW, int STAGE>
+// depth, the CTA's slot count and the cluster size are launch parameters.
+template <int D, int NCW, int TILE, int STAGE>
 struct Layout {
   static constexpr size_t full = 0;                            // kMaxStages mbarriers
   static constexpr size_t empty = 8 * kMaxStages;              // kMaxStages mbarriers
-  static constexpr size_t xch = 16 * kMaxStages;
-  static constexpr size_t xo = xch + sizeof(Xch);              // cluster-visible partial o[D]
+  static constexpr size_t xbar = 16 * kMaxStages;              // mbarrier: the peers' partials have landed
+  static constexpr size_t kbar = xbar + 8;                     // mbarrier: the peers' candidates have landed
+  static constexpr size_t xch = xbar + 16;
+  static constexpr size_t xo = xch + sizeof(Xch);              // this CTA's partial o[D]
   static constexpr size_t red = (xo + D * 4 + 127) / 128 * 128;
-  static constexpr size_t gm = red + NCW * (D + 4) * 4;        // per-rank m / l / self / key / slot
-  static constexpr size_t blk = gm + 16 * 24;                  // block argmin scratch + counters
+  static constexpr size_t gm = red + NCW * (D + 4) * 4;        // per-rank partials [16], candidates [16]
+  static constexpr size_t blk = gm + 16 * 32;                  // block argmin scratch + counters
   static constexpr size_t wbuf = (blk + 12 * (NCW + 1) + 16 + 15) / 16 * 16;  // per-warp row weights
-  static constexpr size_t stages = (wbuf + NCW * 64 * 4 + 127) / 128 * 128;
+  static constexpr size_t stages = (wbuf + NCW * TILE * 4 + 127) / 128 * 128;
   __host__ __device__ static size_t tail(int nstage) { return stages + static_cast<size_t>(nstage) * STAGE; }
-  __host__ __device__ static size_t bytes(int nstage, int chunk, int /*splits*/) {
-    return tail(nstage) + static_cast<size_t>(chunk) * 12;  // logits, scores, positions
+  // after the logits, scores and positions of the CTA's slots: rank 0's
+  // copies of the other ranks' partial output rows (rank r at r - 1)
+  __host__ __device__ static size_t rows_in(int nstage, int chunk) {
+    return (tail(nstage) + static_cast<size_t>(chunk) * 12 + 15) / 16 * 16;
+  }
+  __host__ __device__ static size_t bytes(int nstage, int chunk, int splits) {
+    return rows_in(nstage, chunk) + (splits > 1 ? static_cast<size_t>(splits - 1) * D * 4 : 0);
   }
 };
 
@@ -213,9 +223,6 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 }
 __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_arrive_release() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -227,7 +234,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 template <typename T, int D, int NCW, int TILE>
 __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeParams prm) {
   using Cfg = DecodeCfg<T, D, NCW, TILE>;
-  using Lay = Layout<D, NCW, Cfg::STAGE>;
+  using Lay = Layout<D, NCW, TILE, Cfg::STAGE>;
   // Stage s is always consumed by warp s % NCW: with a ring depth that is a
   // multiple of NCW a warp never waits two phases ahead on a stage another
   // warp still owns, so mbarrier parity waits cannot alias.  Other depths
@@ -242,11 +249,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
   Xch* xch = reinterpret_cast<Xch*>(smem + Lay::xch);
   float* xo = reinterpret_cast<float*>(smem + Lay::xo);
   float* red = reinterpret_cast<float*>(smem + Lay::red);
-  float* g_m = reinterpret_cast<float*>(smem + Lay::gm);
-  float* g_l = g_m + 16;
-  float* g_self = g_l + 16;
-  unsigned long long* g_key = reinterpret_cast<unsigned long long*>(g_self + 16);
-  int* g_slot = reinterpret_cast<int*>(g_key + 16);
+  Xch* xin = reinterpret_cast<Xch*>(smem + Lay::gm);         // rank r's (m, l, self) at [r]
+  uint4* kin = reinterpret_cast<uint4*>(smem + Lay::gm + 256);  // rank r's candidate (key, slot) at [r]
+  uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + Lay::xbar);
+  uint64_t* kbar = reinterpret_cast<uint64_t*>(smem + Lay::kbar);
   unsigned long long* blk_key = reinterpret_cast<unsigned long long*>(smem + Lay::blk);
   int* blk_slot = reinterpret_cast<int*>(blk_key + NW);  // per-warp candidate slot
   int* blk_int = blk_slot + NW;                           // [1..3] p, count, head
@@ -255,6 +261,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
   float* lg = reinterpret_cast<float*>(smem + Lay::tail(NSTAGE));
   float* sc = lg + prm.chunk;
   int* ps = reinterpret_cast<int*>(sc + prm.chunk);
+  float* xo_in = reinterpret_cast<float*>(smem + Lay::rows_in(NSTAGE, prm.chunk));
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
@@ -272,7 +279,15 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
+    mbar_init(xbar, 1);
+    mbar_init(kbar, 1);
     fence_mbar_init();
+    if (S > 1) {
+      // the bytes the peers will push: (m, l, self) from each, the partial
+      // output rows into rank 0, and later one candidate from each
+      mbar_arrive_expect_tx(xbar, static_cast<uint32_t>((S - 1) * 16 + (rank == 0 ? (S - 1) * D * 4 : 0)));
+      mbar_arrive_expect_tx(kbar, static_cast<uint32_t>((S - 1) * 16));
+    }
   }
   __syncthreads();
   // The cluster's CTAs exchange partial results by writing into each other's
@@ -442,25 +457,28 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
         xch->m = M;
         xch->l = Ls;
         xch->s_self = s_self;
+        xin[rank] = *xch;
       }
     }
   }
-  // A pair handled by one CTA needs no cluster barrier or distributed shared
-  // memory: plain block barriers and local shared memory do.  In a cluster,
-  // every CTA writes its partial softmax (m, l) into each peer's g_m / g_l
-  // slot, then one cluster barrier makes them visible.  Rank 0 reads the
-  // peers' partial output rows from their shared memory before the second
-  // cluster barrier, after which no CTA touches another's shared memory.
+  // A pair handled by one CTA needs no cluster or distributed shared
+  // memory.  In a cluster, every CTA pushes its partial softmax (m, l) into
+  // each peer's xin[rank] and the other ranks push their partial output rows
+  // into rank 0, all with st.async counted on the receiver's xbar: each CTA
+  // waits only for the bytes it receives, never on a cluster barrier.
   const bool clustered = S > 1;
   if (clustered) {
-    __syncthreads();         // xo / xch of this CTA are complete (all 160 threads)
-    cluster_wait_acquire();  // every peer has started (the arrival at entry)
-    if (tid < S) {
-      cluster.map_shared_rank(g_m, tid)[rank] = xch->m;
-      cluster.map_shared_rank(g_l, tid)[rank] = xch->l;
-      if (rank == 0) cluster.map_shared_rank(g_self, tid)[0] = xch->s_self;
+    __syncthreads();         // xo / xch of this CTA are complete (all threads)
+    cluster_wait_acquire();  // every peer has started and set up its barriers
+    if (tid < S && tid != rank) {
+      const uint4 v = make_uint4(__float_as_uint(xch->m), __float_as_uint(xch->l), __float_as_uint(xch->s_self), 0u);
+      st_async_v4(mapa_shared(smem_u32(&xin[rank]), tid), v, mapa_shared(smem_u32(xbar), tid));
     }
-    cluster.sync();  // (1) every CTA's partial softmax is in every CTA
+    if (rank != 0 && tid < D / 4) {
+      const uint4 v = *reinterpret_cast<const uint4*>(xo + tid * 4);
+      st_async_v4(mapa_shared(smem_u32(xo_in + (rank - 1) * D + tid * 4), 0), v, mapa_shared(smem_u32(xbar), 0));
+    }
+    if (!mbar_wait_cluster_bounded(xbar, 0, kWaitLimit) && tid == 0) atomicOr(prm.err, ERR_XCH_TIMEOUT);
   } else {
     __syncthreads();
   }
@@ -469,9 +487,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
   // handled by one CTA, this CTA's own (published before the barrier above)
   float M = kNeg, Ls = 0.f, sself;
   if (clustered) {
-    for (int r = 0; r < S; ++r) M = fmaxf(M, g_m[r]);
-    for (int r = 0; r < S; ++r) Ls = fmaf(g_l[r], exp2f(g_m[r] - M), Ls);
-    sself = g_self[0];
+    for (int r = 0; r < S; ++r) M = fmaxf(M, xin[r].m);
+    for (int r = 0; r < S; ++r) Ls = fmaf(xin[r].l, exp2f(xin[r].m - M), Ls);
+    sself = xin[0].s_self;
   } else {
     M = xch->m;
     Ls = xch->l;
@@ -489,7 +507,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
     float acc = xo[tid];
     if (clustered) {
       acc = 0.f;
-      for (int r = 0; r < S; ++r) acc = fmaf(cluster.map_shared_rank(xo, r)[tid], exp2f(g_m[r] - M), acc);
+      for (int r = 0; r < S; ++r) acc = fmaf(r == 0 ? xo[tid] : xo_in[(r - 1) * D + tid], exp2f(xin[r].m - M), acc);
     }
     prm.out[static_cast<size_t>(pair) * D + tid] = acc * inv;
   }
@@ -535,22 +553,25 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
 
   int u;
   if (clustered) {
-    // every thread holds this CTA's candidate (bk, bslot): thread r writes it
-    // into peer r's slot for this rank, then the barrier makes all visible;
-    // after it no CTA touches another's shared memory, so none waits at exit
-    if (tid < S) {
-      cluster.map_shared_rank(g_key, tid)[rank] = bk;
-      cluster.map_shared_rank(g_slot, tid)[rank] = bslot;
+    // every thread holds this CTA's candidate (bk, bslot): thread r pushes it
+    // into peer r's kin[rank]; each CTA waits for its peers' candidates
+    if (tid < S && tid != rank) {
+      const uint4 v = make_uint4(static_cast<uint32_t>(bk), static_cast<uint32_t>(bk >> 32),
+                                 static_cast<uint32_t>(bslot), 0u);
+      st_async_v4(mapa_shared(smem_u32(&kin[rank]), tid), v, mapa_shared(smem_u32(kbar), tid));
     }
-    cluster.sync();  // (2) every CTA's candidate is in every CTA
+    if (!mbar_wait_cluster_bounded(kbar, 0, kWaitLimit) && tid == 0) atomicOr(prm.err, ERR_XCH_TIMEOUT);
     if (full) {
       unsigned long long best = ~0ull;
       u = -1;
-      for (int r = 0; r < S; ++r)
-        if (g_key[r] < best) {
-          best = g_key[r];
-          u = g_slot[r];
+      for (int r = 0; r < S; ++r) {
+        const uint4 c = kin[r];
+        const unsigned long long key = r == rank ? bk : (static_cast<unsigned long long>(c.y) << 32 | c.x);
+        if (key < best) {
+          best = key;
+          u = r == rank ? bslot : static_cast<int>(c.z);
         }
+      }
     } else {
       u = count;
     }
@@ -558,10 +579,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
     u = full ? bslot : count;
   }
   if (full && u < 0 && tid == 0) atomicOr(prm.err, ERR_NO_CANDIDATE);
-  // Clusters of more than two CTAs leave together (measured faster for 8-CTA
-  // clusters, slower for pairs of CTAs); nothing remote is read after (2).
-  const bool leave_together = S > 2;
-  if (leave_together) cluster_arrive_release();
+  // Every byte pushed into this CTA has landed (both waits above) and no CTA
+  // reads another's shared memory, so the CTAs of a cluster leave without a
+  // cluster barrier.
 
   // write back: scores of this CTA's slots, the new token into slot u
   for (int j = tid; j < nrows; j += NT) prm.score[slot0 + j] = (lo + j == u) ? p_self : sc[j];
@@ -581,7 +601,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
     *reinterpret_cast<int4*>(prm.ctr + pair) = make_int4(p + 1, full ? C : count + 1, (head + 1) % R, 0);
     if (prm.evicted) prm.evicted[pair] = full ? u : -1;
   }
-  if (leave_together) cluster_wait_acquire();
 }
 
 // ------------------------------------------------------------ warp per pair
@@ -877,7 +896,7 @@ template <typename T, int D>
 struct Kern {
   static constexpr int NCW = 4, TILE = 16;
   using Cfg = DecodeCfg<T, D, NCW, TILE>;
-  using Lay = Layout<D, NCW, Cfg::STAGE>;
+  using Lay = Layout<D, NCW, TILE, Cfg::STAGE>;
   static constexpr auto fn = decode_kernel<T, D, NCW, TILE>;
 
   static size_t smem(int nstage, int chunk, int splits) { return Lay::bytes(nstage, chunk, splits); }

@@ -422,12 +422,13 @@ int h2o_cache_check(h2o_cache* c, void* stream) {
   if (flags) {
     cudaMemset(c->err, 0, sizeof(int));
     cudaDeviceSynchronize();
-    return fail(H2O_EDEVICE, "h2o_cache_check: device check fired (flags 0x%x:%s%s%s%s%s)", flags,
+    return fail(H2O_EDEVICE, "h2o_cache_check: device check fired (flags 0x%x:%s%s%s%s%s%s)", flags,
                 (flags & h2o::ERR_MBAR_TIMEOUT) ? " copy-wait-timeout" : "",
                 (flags & h2o::ERR_NO_CANDIDATE) ? " no-eviction-candidate" : "",
                 (flags & h2o::ERR_SELECT) ? " prefill-select" : "",
                 (flags & h2o::ERR_RING_TIMEOUT) ? " ring-wait-timeout" : "",
-                (flags & h2o::ERR_MMA_TIMEOUT) ? " tensor-core-wait-timeout" : "");
+                (flags & h2o::ERR_MMA_TIMEOUT) ? " tensor-core-wait-timeout" : "",
+                (flags & h2o::ERR_XCH_TIMEOUT) ? " cluster-exchange-timeout" : "");
   }
   return H2O_OK;
 }

@@ -14,6 +14,7 @@ enum : int {
   ERR_SELECT = 4,        // prefill selection did not find `heavy` keys
   ERR_RING_TIMEOUT = 8,  // the producer's wait for a free stage gave up
   ERR_MMA_TIMEOUT = 16,  // a prefill wait for tensor-core results gave up
+  ERR_XCH_TIMEOUT = 32,  // a wait for the partial results a peer CTA pushes gave up
 };
 
 // Per-pair counters kept on the device so decode steps can be replayed from
