@@ -152,8 +152,9 @@ H2O_API int h2o_cache_check(h2o_cache* cache, void* stream);
 
 /* Tuning of the decode kernel's launch shape: `splits` CTAs (one thread-block
  * cluster) share a pair, each streaming its slots through a ring of `stages`
- * 16-row shared-memory stages; splits must be 1, 2, 4, 8 or 16 and stages 4,
- * 8, 12 or 16 (a multiple of the kernel's four consumer warps).  Or splits =
+ * 16-row shared-memory stages; splits must be 1, 2, 4, 8 or 16, and stages a
+ * multiple of the kernel's consumer warps up to 18: 6, 12 or 18 for one CTA
+ * per pair (six consumer warps), 4, 8, 12 or 16 for clusters (four).  Or splits =
  * H2O_DECODE_WARP_PER_PAIR: one warp streams a whole pair through its own
  * ring of `stages` (2..8) and then takes its next pair, for many pairs of at
  * most 1024 slots.  0 = automatic for either value (the automatic choice

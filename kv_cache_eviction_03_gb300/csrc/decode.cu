@@ -16,7 +16,8 @@
 //
 // Inside a CTA one producer warp streams the CTA's K and V rows, 16 rows per
 // stage, through a ring of shared-memory stages with 1-D bulk async copies
-// (cp.async.bulk, full/empty mbarriers, L2 evict-first); four consumer warps
+// (cp.async.bulk, full/empty mbarriers, L2 evict-first); six consumer warps
+// (four when a cluster shares the pair)
 // compute the logits and a base-2 online softmax (m, l, o) per row group and
 // release each stage with an mbarrier arrive, so the streaming loop has no
 // block-wide barrier.  When the previous kernel on the stream worked on a
@@ -185,7 +186,13 @@ __device__ __forceinline__ void merge_groups(float& m, float& l, float (&o)[RowG
   }
 }
 
-constexpr int kMaxStages = 16;
+constexpr int kMaxStages = 18;
+// Consumer warps of the cluster kernel.  A pair handled by one CTA gets six
+// (two stages of the 12-stage ring in flight per warp), the CTAs of a
+// cluster four (three each): measured, six is 2.5% faster than four for one
+// CTA per pair (OPT-6.7B shape) and four is 1-3% faster in 2- and 8-CTA
+// clusters (streaming, LLaMA-16K shapes).
+__host__ __device__ constexpr int consumer_warps(int splits) { return splits > 1 ? 4 : 6; }
 
 // A CTA's merged partial softmax (max, normaliser, self logit).
 struct __align__(16) Xch {
@@ -202,8 +209,7 @@ struct Layout {
   static constexpr size_t kbar = xbar + 8;                     // mbarrier: the peers' candidates have landed
   static constexpr size_t xch = xbar + 16;
   static constexpr size_t xo = xch + sizeof(Xch);              // this CTA's partial o[D]
-  static constexpr size_t red = (xo + D * 4 + 127) / 128 * 128;
-  static constexpr size_t gm = red + NCW * (D + 4) * 4;        // per-rank partials [16], candidates [16]
+  static constexpr size_t gm = (xo + D * 4 + 15) / 16 * 16;    // per-rank partials [16], candidates [16]
   static constexpr size_t blk = gm + 16 * 32;                  // block argmin scratch + counters
   static constexpr size_t wbuf = (blk + 12 * (NCW + 1) + 16 + 15) / 16 * 16;  // per-warp row weights
   static constexpr size_t stages = (wbuf + NCW * TILE * 4 + 127) / 128 * 128;
@@ -232,15 +238,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 }
 
 template <typename T, int D, int NCW, int TILE>
-__global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeParams prm) {
+__global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel(const DecodeParams prm) {
   using Cfg = DecodeCfg<T, D, NCW, TILE>;
   using Lay = Layout<D, NCW, TILE, Cfg::STAGE>;
   // Stage s is always consumed by warp s % NCW: with a ring depth that is a
   // multiple of NCW a warp never waits two phases ahead on a stage another
   // warp still owns, so mbarrier parity waits cannot alias.  Other depths
-  // are rejected on the host; a kernel given one does no streaming.
+  // are rejected on the host; a kernel given one only reports it.
   const int NSTAGE = prm.nstage;
-  const bool ring_ok = NSTAGE >= NCW && NSTAGE % NCW == 0 && NSTAGE <= kMaxStages;
+  if (!(NSTAGE >= NCW && NSTAGE % NCW == 0 && NSTAGE <= kMaxStages)) {
+    if (threadIdx.x == 0) atomicOr(prm.err, ERR_RING_TIMEOUT);
+    return;
+  }
   constexpr int EPV = Cfg::EPV, LPR = Cfg::LPR, ROWB = Cfg::ROWB;
   constexpr int NT = Cfg::NT, NW = Cfg::NW;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -248,7 +257,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
   uint64_t* empty_bar = reinterpret_cast<uint64_t*>(smem + Lay::empty);
   Xch* xch = reinterpret_cast<Xch*>(smem + Lay::xch);
   float* xo = reinterpret_cast<float*>(smem + Lay::xo);
-  float* red = reinterpret_cast<float*>(smem + Lay::red);
   Xch* xin = reinterpret_cast<Xch*>(smem + Lay::gm);         // rank r's (m, l, self) at [r]
   uint4* kin = reinterpret_cast<uint4*>(smem + Lay::gm + 256);  // rank r's candidate (key, slot) at [r]
   uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + Lay::xbar);
@@ -274,7 +282,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
   const size_t slot0 = static_cast<size_t>(pair) * C + lo;
 
   if (tid == 0) {
-    if (!ring_ok) atomicOr(prm.err, ERR_RING_TIMEOUT);
     for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
@@ -309,7 +316,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
       // previous kernel on this stream did not touch this cache.
       if (!prm.prefetch) griddep_wait();
       const int cnt = prm.ctr[pair].count;
-      const int nrows = ring_ok ? max(min(lo + prm.chunk, cnt) - lo, 0) : 0;
+      const int nrows = max(min(lo + prm.chunk, cnt) - lo, 0);
       const int ntiles = (nrows + TILE - 1) / TILE;
       const unsigned char* gK = static_cast<const unsigned char*>(prm.K) + slot0 * ROWB;
       const unsigned char* gV = static_cast<const unsigned char*>(prm.V) + slot0 * ROWB;
@@ -350,7 +357,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
     int nrows = 0;
     auto load_state = [&]() {
       ctr = *reinterpret_cast<const int4*>(prm.ctr + pair);  // {p, count, head, -}
-      nrows = ring_ok ? max(min(lo + prm.chunk, ctr.y) - lo, 0) : 0;
+      nrows = max(min(lo + prm.chunk, ctr.y) - lo, 0);
       for (int j = tid; j < nrows; j += NCW * 32) {
         sc[j] = prm.score[slot0 + j];
         ps[j] = prm.pos[slot0 + j];
@@ -433,7 +440,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
     }
 
     merge_groups<T, D>(m, l, o);  // identical result in every row group
-    float* myred = red + warp * (D + 4);
+    // Each warp's merged (m, l, o) goes into its own first stage: every stage
+    // of warp w (s % NCW == w) has been consumed, and no copy targets it, once
+    // the warp has left its loop.
+    auto red_of = [&](int w) { return reinterpret_cast<float*>(stage_base + static_cast<size_t>(w) * Cfg::STAGE); };
+    float* myred = red_of(warp);
     if (lane == 0) {
       myred[0] = m;
       myred[1] = l;
@@ -445,12 +456,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 4) decode_kernel(const DecodeP
     consumer_sync(NCW * 32);
     if (tid < D) {
       float M = kNeg;
-      for (int w = 0; w < NCW; ++w) M = fmaxf(M, red[w * (D + 4)]);
+      for (int w = 0; w < NCW; ++w) M = fmaxf(M, red_of(w)[0]);
       float Ls = 0.f, Od = 0.f;
       for (int w = 0; w < NCW; ++w) {
-        const float a = exp2f(red[w * (D + 4)] - M);
-        Ls = fmaf(red[w * (D + 4) + 1], a, Ls);
-        Od = fmaf(red[w * (D + 4) + 4 + tid], a, Od);
+        const float* rw = red_of(w);
+        const float a = exp2f(rw[0] - M);
+        Ls = fmaf(rw[1], a, Ls);
+        Od = fmaf(rw[4 + tid], a, Od);
       }
       xo[tid] = Od;
       if (tid == 0) {
@@ -892,9 +904,9 @@ struct WarpKern {
   }
 };
 
-template <typename T, int D>
+template <typename T, int D, int NCW>
 struct Kern {
-  static constexpr int NCW = 4, TILE = 16;
+  static constexpr int TILE = 16;
   using Cfg = DecodeCfg<T, D, NCW, TILE>;
   using Lay = Layout<D, NCW, TILE, Cfg::STAGE>;
   static constexpr auto fn = decode_kernel<T, D, NCW, TILE>;
@@ -960,12 +972,18 @@ int chunk_for(int C, int splits) {
   return (ch + 3) / 4 * 4;
 }
 
+template <int NCW, typename F>
+auto dispatch_ncw(int dtype, int D, F&& f) -> decltype(f(Kern<__half, 128, NCW>{})) {
+  if (dtype == 0 && D == 128) return f(Kern<__half, 128, NCW>{});
+  if (dtype == 0 && D == 64) return f(Kern<__half, 64, NCW>{});
+  if (dtype == 1 && D == 128) return f(Kern<float, 128, NCW>{});
+  return f(Kern<float, 64, NCW>{});
+}
+// the kernel instance for a dtype, head width and cluster size
 template <typename F>
-auto dispatch(int dtype, int D, F&& f) -> decltype(f(Kern<__half, 128>{})) {
-  if (dtype == 0 && D == 128) return f(Kern<__half, 128>{});
-  if (dtype == 0 && D == 64) return f(Kern<__half, 64>{});
-  if (dtype == 1 && D == 128) return f(Kern<float, 128>{});
-  return f(Kern<float, 64>{});
+auto dispatch(int dtype, int D, int splits, F&& f) -> decltype(f(Kern<__half, 128, 4>{})) {
+  if (consumer_warps(splits) == 4) return dispatch_ncw<4>(dtype, D, f);
+  return dispatch_ncw<6>(dtype, D, f);
 }
 
 }  // namespace
@@ -975,7 +993,7 @@ int decode_max_chunk() { return kMaxChunk; }
 int decode_chunk(int C, int splits) { return chunk_for(C, splits); }
 
 int decode_max_stages() { return kMaxStages; }
-int decode_stage_multiple() { return Kern<__half, 128>::NCW; }
+int decode_stage_multiple(int splits) { return consumer_warps(splits); }
 
 int device_sms() {
   int sms = 0, dev = 0;
@@ -989,7 +1007,8 @@ int device_sms() {
 
 int decode_resident(int dtype, int D, int splits, int nstage, int chunk, int pairs) {
   const int sms = device_sms();
-  const int r = dispatch(dtype, D, [&](auto k) { return decltype(k)::resident(splits, nstage, chunk, pairs, sms); });
+  const int r =
+      dispatch(dtype, D, splits, [&](auto k) { return decltype(k)::resident(splits, nstage, chunk, pairs, sms); });
   cudaGetLastError();
   return r;
 }
@@ -998,9 +1017,10 @@ int decode_resident(int dtype, int D, int splits, int nstage, int chunk, int pai
 // overlap: the next kernel's CTAs start filling their rings while this one
 // finishes, so one step should take about 1.7 CTAs per SM (the largest
 // cluster size whose grid stays within that, each CTA keeping at least 32
-// slots), with a 12-stage ring (three stages in flight per consumer warp)
+// slots), with a 12-stage ring (two or three stages in flight per consumer warp)
 // when two such CTAs fit on an SM.  Grids that need several waves anyway
-// (many pairs) use 4-stage rings so that more CTAs are resident.
+// (many pairs) use rings of one stage per consumer warp so that more CTAs
+// are resident.
 // Many short pairs (at least four per SM, each within the warp kernel's slot
 // limit) go to the warp-per-pair kernel.  More resident warps beat deeper
 // rings, so its ring is the deepest that still leaves as many resident warps
@@ -1034,10 +1054,11 @@ DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C) {
   }
   while (sh.splits < 16 && chunk_for(C, sh.splits) > kMaxChunk) sh.splits *= 2;
   const long long ctas = static_cast<long long>(pairs) * sh.splits;
-  sh.stages = 4;
+  const int ncw = consumer_warps(sh.splits);
+  sh.stages = ncw;
   if (ctas <= 2LL * sms) {
     const int ch = chunk_for(C, sh.splits);
-    for (int st : {12, 8}) {
+    for (int st : {12, ncw == 6 ? 6 : 8}) {
       const int res = decode_resident(dtype, D, sh.splits, st, ch, pairs);
       if (res >= 2 * sms || static_cast<long long>(res) >= ctas) {
         sh.stages = st;
@@ -1103,9 +1124,9 @@ cudaError_t launch_decode(const DecodeParams& prm, int dtype, int D, int pairs, 
     if (dtype == 1 && D == 128) return WarpKern<float, 128>::launch(prm, ctas, s);
     return WarpKern<float, 64>::launch(prm, ctas, s);
   }
-  return dispatch(dtype, D, [&](auto k) { return decltype(k)::launch(prm, pairs, splits, s); });
+  return dispatch(dtype, D, splits, [&](auto k) { return decltype(k)::launch(prm, pairs, splits, s); });
 }
 
-int decode_threads() { return 160; }
+int decode_threads(int splits) { return (consumer_warps(splits) + 1) * 32; }
 
 }  // namespace h2o

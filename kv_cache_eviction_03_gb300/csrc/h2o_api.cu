@@ -444,7 +444,8 @@ int h2o_cache_set_decode_shape(h2o_cache* c, int splits, int stages) {
     if (s == c->shape_auto.splits)
       n = c->shape_auto.stages;
     else
-      n = s == h2o::kDecodeWarpPerPair ? h2o::decode_warp_default_stages(c->dtype, c->D, c->C, c->P) : 4;
+      n = s == h2o::kDecodeWarpPerPair ? h2o::decode_warp_default_stages(c->dtype, c->D, c->C, c->P)
+                                      : h2o::decode_stage_multiple(s);
   }
   if (s == h2o::kDecodeWarpPerPair) {
     if (c->C > h2o::decode_warp_max_slots())
@@ -456,9 +457,9 @@ int h2o_cache_set_decode_shape(h2o_cache* c, int splits, int stages) {
     if (h2o::decode_warp_resident(c->dtype, c->D, n, c->C) <= 0)
       return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: warp per pair with %d stages cannot be scheduled", n);
   } else {
-    if (n < 0 || n > h2o::decode_max_stages() || n % h2o::decode_stage_multiple() != 0)
+    if (n < 0 || n > h2o::decode_max_stages() || n % h2o::decode_stage_multiple(s) != 0)
       return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: stages must be a multiple of %d in 0..%d",
-                  h2o::decode_stage_multiple(), h2o::decode_max_stages());
+                  h2o::decode_stage_multiple(s), h2o::decode_max_stages());
     if (chunk_for(c->C, s) > h2o::decode_max_chunk())
       return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: %d splits leave more than %d slots per CTA", s,
                   h2o::decode_max_chunk());
@@ -481,7 +482,7 @@ int h2o_cache_info(const h2o_cache* c, int32_t* info) {
   info[5] = c->dtype;
   info[6] = splits_in_use(c);
   info[7] = stages_in_use(c);
-  info[8] = splits_in_use(c) == h2o::kDecodeWarpPerPair ? 128 : h2o::decode_threads();
+  info[8] = splits_in_use(c) == h2o::kDecodeWarpPerPair ? 128 : h2o::decode_threads(splits_in_use(c));
   info[9] = 0;
   return H2O_OK;
 }

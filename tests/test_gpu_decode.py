@@ -155,23 +155,29 @@ def test_splits_agree(splits):
     assert rep.pairs > 0
 
 
-@pytest.mark.parametrize("splits,stages", [(1, 4), (1, 12), (1, 16), (2, 4), (4, 16)])
+@pytest.mark.parametrize("splits,stages", [(1, 6), (1, 12), (1, 18), (2, 4), (2, 8), (4, 16)])
 def test_ring_depths_agree(splits, stages):
-    """Every legal ring depth (a multiple of the four consumer warps) gives
-    the oracle's result, with more tiles than stages so stages are reused."""
+    """Every legal ring depth (a multiple of the consumer warps: six for one
+    CTA per pair, four in a cluster) gives the oracle's result, with more
+    tiles than stages so stages are reused."""
     w = W.Workload("ring", 1, 3, 128, "f16", 600, 12, 300, 200, 1.1)
     cache_check = set(range(12))
     rep = run_stepwise(w, 23, check=cache_check, splits=splits, stages=stages)
     assert rep.pairs == w.pairs * 12
 
 
-def test_ring_depth_must_be_a_multiple_of_four():
+def test_ring_depth_must_be_a_multiple_of_the_consumer_warps():
     cache = B.h2o_cache_create(1, 2, 128, 40, 40, B.H2O_F16)
-    for bad in (1, 3, 6, 10, 20):
+    for bad in (1, 3, 4, 8, 16, 24):  # one CTA per pair: six consumer warps
         with pytest.raises(B.H2OError):
             B.h2o_cache_set_decode_shape(cache, 1, bad)
+    for bad in (1, 3, 6, 10, 18, 20):  # a cluster: four consumer warps
+        with pytest.raises(B.H2OError):
+            B.h2o_cache_set_decode_shape(cache, 2, bad)
     B.h2o_cache_set_decode_shape(cache, 1, 12)
-    assert B.h2o_cache_info(cache)[6:8] == [1, 12]
+    assert B.h2o_cache_info(cache)[6:9] == [1, 12, 224]
+    B.h2o_cache_set_decode_shape(cache, 2, 8)
+    assert B.h2o_cache_info(cache)[6:9] == [2, 8, 160]
     B.h2o_cache_destroy(cache)
 
 
