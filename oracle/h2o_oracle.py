@@ -21,6 +21,9 @@ order the method states it.  Sources (page title, then section):
 * same page, section 2.3, and "H2O" (phantomic12 inference-research notes):
   the score is the running sum of the attention probability each token
   receives, lowest-scoring entry evicted when full, recent window kept.
+* same page, section 2.3 (its Figure 2(d) comparison): the online ("local")
+  rule set against a global one that may use the whole sequence's attention,
+  future rows included (global_select_pair, heavy_overlap).
 
 Readings taken where the pages are loose (each also listed in the design
 notes): the score is the column sum of attention probabilities (the report's
@@ -141,6 +144,40 @@ def prefill_pair(q, k, v, heavy, recent, scale):
             st.ring[r] = keep.index(r)
         st.head = L
     return st, colsum, out
+
+
+# --------------------------------------------------------------------------- global selector
+def global_select_pair(q, k, heavy, recent, scale):
+    """Global (offline) heavy hitters of one pair's whole sequence.
+
+    Section 2.3 compares the online rule, which only ever sums the attention
+    each token has received so far, with a global rule that may look at the
+    whole sequence.  Reading: token j's global score is the attention it
+    receives from every row of the sequence, sum_{i >= j} softmax_i(s_ij)
+    over all N rows (the prefill column sum taken over the whole sequence),
+    and the global kept set is the prefill keep rule applied to those
+    scores: the last `recent` positions plus the `heavy` largest keys
+    (score, position) before them.  q, k: float64 [N, D].
+    Returns (kept positions in ascending order, scores [N]).
+    """
+    N = q.shape[0]
+    if N == 0:
+        return [], np.zeros((0,))
+    _, colsum, _ = causal_attention_stats(q, k, np.zeros((N, 1)), scale)
+    return sorted(select_prefill(colsum, N, heavy, recent)), colsum
+
+
+def heavy_overlap(local_pos, global_pos, n, recent):
+    """Share of the global heavy hitters that a local run also kept.
+
+    Both sets hold the same recent window (positions n-recent..n-1); the heavy
+    hitters are the kept positions before it.  Returns (shared, of): `of` is
+    the number of global heavy hitters, `shared` how many of them the local
+    set holds too (1.0 drift-free when shared == of).
+    """
+    lh = {int(x) for x in local_pos if 0 <= x < n - recent}
+    gh = {int(x) for x in global_pos if 0 <= x < n - recent}
+    return len(lh & gh), len(gh)
 
 
 # --------------------------------------------------------------------------- decode

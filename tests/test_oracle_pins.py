@@ -321,3 +321,82 @@ def test_kv_cache_size_worked_example():
     b = kv_cache_bytes(int(fields["layers"]), int(fields["hidden"]), int(fields["batch"]),
                        int(fields["seq"]), int(fields["bytes_per_elem"]))
     assert round(b / 1e9) == int(fields["approx_gb"])
+
+
+# ------------------------------------------------------------------ global selector
+def _brute_force_global(q, k, heavy, recent, scale):
+    """Global kept set by explicit loops: each row's softmax over its causal
+    prefix, scores as sums down each column, and a candidate kept when fewer
+    than `heavy` other candidates have a larger (score, position) key."""
+    N = len(q)
+    score = [0.0] * N
+    for i in range(N):
+        s = [scale * sum(a * b for a, b in zip(q[i], k[j])) for j in range(i + 1)]
+        mx = max(s)
+        e = [math.exp(x - mx) for x in s]
+        z = sum(e)
+        for j in range(i + 1):
+            score[j] += e[j] / z
+    if N <= heavy + recent:
+        return list(range(N)), score
+    n = N - recent
+    f32 = [float(np.float32(x)) for x in score]
+    kept = [j for j in range(n) if sum(1 for o in range(n) if (f32[o], o) > (f32[j], j)) < heavy]
+    return kept + list(range(n, N)), score
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_global_select_brute_force(seed):
+    rng = np.random.default_rng(300 + seed)
+    N = int(rng.integers(1, 14))
+    heavy, recent = int(rng.integers(0, 5)), int(rng.integers(1, 4))
+    D = 3
+    q, k, _ = rand_seq(rng, N, D, key_mean=rng.standard_normal(D))
+    k[rng.integers(0, N, 3)] = k[0]  # repeated keys: heavy hitters and near ties
+    kept, score = O.global_select_pair(q, k, heavy, recent, 0.8)
+    bf_kept, bf_score = _brute_force_global(q.tolist(), k.tolist(), heavy, recent, 0.8)
+    np.testing.assert_allclose(score, bf_score, rtol=1e-12)
+    assert kept == bf_kept
+
+
+def test_global_select_uniform_attention_keeps_the_earliest():
+    """Equal keys: row i gives 1/(i+1) to every j <= i, so the scores are
+    H_N - H_j (harmonic numbers), decreasing in j, and the global heavy
+    hitters are the first `heavy` positions."""
+    N, D, heavy, recent = 40, 4, 6, 5
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal((N, D))
+    k = np.tile(rng.standard_normal(D), (N, 1))
+    kept, score = O.global_select_pair(q, k, heavy, recent, 0.5)
+    H = np.concatenate([[0.0], np.cumsum(1.0 / np.arange(1, N + 1))])
+    np.testing.assert_allclose(score, H[N] - H[np.arange(N)], rtol=1e-12)
+    assert kept == list(range(heavy)) + list(range(N - recent, N))
+
+
+@pytest.mark.parametrize("N,heavy,recent", [(0, 2, 2), (7, 4, 3), (5, 4, 3), (9, 0, 9)])
+def test_global_select_within_budget_keeps_all(N, heavy, recent):
+    rng = np.random.default_rng(N)
+    q, k, _ = rand_seq(rng, N, 3)
+    kept, _ = O.global_select_pair(q, k, heavy, recent, 0.7)
+    assert kept == list(range(N))
+
+
+def test_local_run_matches_global_under_uniform_attention():
+    """Equal keys make every kept token receive the same probability each
+    step, so the local rule never reorders the prompt's heavy hitters
+    (scores H_L - H_j) and ends with the global set: full overlap."""
+    L, T, D, heavy, recent = 30, 25, 4, 5, 4
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((L + T, D))
+    k = np.tile(rng.standard_normal(D), (L + T, 1))
+    v = rng.standard_normal((L + T, D))
+    st, _, _, _ = run_pair(q, k, v, L, heavy, recent, 0.6)
+    kept, _ = O.global_select_pair(q, k, heavy, recent, 0.6)
+    local = sorted(int(x) for x in st.pos if x >= 0)
+    assert local == kept == list(range(heavy)) + list(range(L + T - recent, L + T))
+    assert O.heavy_overlap(local, kept, L + T, recent) == (heavy, heavy)
+
+
+def test_heavy_overlap_counts_only_heavy_positions():
+    assert O.heavy_overlap([0, 3, 5, 8, 9], [0, 4, 5, 8, 9], 10, 2) == (2, 3)
+    assert O.heavy_overlap([8, 9], [8, 9], 10, 2) == (0, 0)
