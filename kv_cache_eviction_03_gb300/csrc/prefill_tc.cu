@@ -655,8 +655,24 @@ __global__ void __launch_bounds__(NT, 2) colsum_tc(const __grid_constant__ TcArg
 
 // ------------------------------------------------- column sums from partials
 // colsum_j = sum over query blocks qb >= j / 128 and the four TMEM lane
-// quarters of the output pass's partial column sums, in that fixed order, in
-// float64 (each partial is a float32 sum over 32 rows).
+// quarters of the output pass's partial column sums (each a float32 sum over
+// 32 rows), added in a fixed order (query blocks ascending, quarters 0..3)
+// with Neumaier's compensated summation in float32 ("Rundungsfehleranalyse
+// einiger Verfahren zur Summation endlicher Summen", 1974): the result is
+// within about one float32 ulp of the exact sum of the partials.  GB300's
+// float64 rate is a small fraction of its float32 rate, so plain float64
+// accumulation made this kernel arithmetic-bound.  Four query blocks' loads
+// are issued before they are added.
+struct Neumaier {
+  float s = 0.f, c = 0.f;  // running sum, accumulated rounding errors
+  __device__ __forceinline__ void add(float x) {
+    const float t = s + x;
+    c += fabsf(s) >= fabsf(x) ? (s - t) + x : (x - t) + s;
+    s = t;
+  }
+  __device__ __forceinline__ float value() const { return s + c; }
+};
+
 __global__ void __launch_bounds__(BLK) colsum_reduce_kernel(const PrefillParams prm) {
   griddep_wait();
   const int pair = blockIdx.y, kb = blockIdx.x, col = threadIdx.x;
@@ -665,17 +681,31 @@ __global__ void __launch_bounds__(BLK) colsum_reduce_kernel(const PrefillParams 
   const int nbp = (Lp + BLK - 1) / BLK;  // query blocks the output pass ran for this pair
   if (kb >= nbp) return;
   const float* part = prm.cs_part + static_cast<size_t>(pair) * colsum_partial_floats(L, 1) + col;
-  double acc = 0.0;
-  for (int qb = kb; qb < nbp; ++qb) {
-    const float* row = part + (static_cast<size_t>(qb) * (qb + 1) / 2 + kb) * (4 * BLK);
-    acc += static_cast<double>(row[0]);
-    acc += static_cast<double>(row[BLK]);
-    acc += static_cast<double>(row[2 * BLK]);
-    acc += static_cast<double>(row[3 * BLK]);
+  auto row = [&](int qb) { return part + (static_cast<size_t>(qb) * (qb + 1) / 2 + kb) * (4 * BLK); };
+  Neumaier acc;
+  int qb = kb;
+  for (; qb + 4 <= nbp; qb += 4) {
+    float v[16];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float* r = row(qb + u);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) v[4 * u + h] = __ldg(r + h * BLK);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc.add(v[i]);
+  }
+  for (; qb < nbp; ++qb) {
+    const float* r = row(qb);
+    float v[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) v[h] = __ldg(r + h * BLK);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) acc.add(v[h]);
   }
   griddep_launch();
   const int key = kb * BLK + col;
-  if (key < Lp) prm.colsum[static_cast<size_t>(pair) * L + key] = static_cast<float>(acc);
+  if (key < Lp) prm.colsum[static_cast<size_t>(pair) * L + key] = acc.value();
 }
 
 // ------------------------------------------------------------------ host
