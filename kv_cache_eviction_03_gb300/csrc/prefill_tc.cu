@@ -302,8 +302,9 @@ struct OutCfg {
   static constexpr size_t q = 0, k = Tile<D>::BYTES;
   static constexpr size_t v = k + NK * static_cast<size_t>(Tile<D>::BYTES);
   static constexpr size_t bars = v + NV * static_cast<size_t>(Tile<D>::BYTES);
-  // qfull, kfull[3], kempty[3], vfull[3], vempty[3], sfull[2], pfull[2], pempty[2], ofull, drain
-  static constexpr int NB = 21;
+  // qfull, kfull[3], kempty[3], vfull[3], vempty[3], sfull[2], pfull[2], pempty[2], ofull, drain,
+  // sempty[2]
+  static constexpr int NB = 23;
   static constexpr size_t tslot = bars + 8 * NB;
   static constexpr size_t bytes = tslot + 16 + 1024;
 };
@@ -340,7 +341,8 @@ __global__ void __launch_bounds__(NT_O, 1) out_tc(const __grid_constant__ TcArgs
   uint64_t* pempty = sfull + 4;
   uint64_t* ofull = sfull + 6;
   uint64_t* drain = sfull + 7;
-  static_assert(1 + 2 * NK + 2 * NV + 8 == Cfg::NB, "barrier count");
+  uint64_t* sempty = sfull + 8;
+  static_assert(1 + 2 * NK + 2 * NV + 10 == Cfg::NB, "barrier count");
   const PrefillParams& prm = a.prm;
   int* err = prm.err;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -348,10 +350,13 @@ __global__ void __launch_bounds__(NT_O, 1) out_tc(const __grid_constant__ TcArgs
   const int qb = gridDim.x - 1 - blockIdx.x;  // longest rows first
   const int n = qb + 1;
   // qfull, K full/empty, V full/empty, sfull[2]: one arrival (TMA or commit);
-  // pfull[2]: one per compute warp; pempty[2], ofull, drain: a commit
+  // pfull[2], sempty[2]: one per compute warp; pempty[2], ofull, drain: a commit
   uint32_t counts[Cfg::NB];
 #pragma unroll
-  for (int i = 0; i < Cfg::NB; ++i) counts[i] = (i == 1 + 2 * NK + 2 * NV + 2 || i == 1 + 2 * NK + 2 * NV + 3) ? NCOMP_O : 1;
+  for (int i = 0; i < Cfg::NB; ++i) {
+    const int r = i - (1 + 2 * NK + 2 * NV);  // index from sfull[0]
+    counts[i] = (r == 2 || r == 3 || r == 8 || r == 9) ? NCOMP_O : 1;
+  }
 
   if (threadIdx.x == 0) {
     tc::prefetch_tensormap(&a.q);
@@ -366,7 +371,7 @@ __global__ void __launch_bounds__(NT_O, 1) out_tc(const __grid_constant__ TcArgs
       setup(warp, bars, counts, Cfg::NB, reinterpret_cast<uint32_t*>(smem + Cfg::tslot), kOutTmemCols);
   const uint32_t o_tmem = tbase + kOcol;
   if (warp == 0) {
-    if (lane == 0) {  // TMA producer, in the order the MMAs consume: K0 K1 V0 K2 V1 K3 ...
+    if (lane == 0) {  // TMA producer, in the order the MMAs consume: K0 K1 K2 V0 K3 V1 ...
       mbar_arrive_expect_tx(qfull, TB);
       tma_tile<D>(sQ, &a.q, qb * BLK, pair, qfull);
       int uk = 0, uv = 0;
@@ -385,13 +390,13 @@ __global__ void __launch_bounds__(NT_O, 1) out_tc(const __grid_constant__ TcArgs
         return true;
       };
       bool ok = issue_k(0) && (n < 2 || issue_k(1));
-      for (int j = 0; ok && j < n; ++j) ok = issue_v(j) && (j + 2 >= n || issue_k(j + 2));
+      for (int j = 0; ok && j < n; ++j) ok = (j + 2 >= n || issue_k(j + 2)) && issue_v(j);
       kr.drain(uk, err);
       vr.drain(uv, err);
       wait1(qfull, 0, err);
     }
   } else if (warp == 1) {
-    if (lane == 0) {  // MMA issuer: S0 S1 O0 S2 O1 S3 ...
+    if (lane == 0) {  // MMA issuer: S0 S1, then per block j: S(j+2) once S(j) is read, O(j) once P(j) is in
       bool ok = wait1(qfull, 0, err);
       for (int j = 0; ok && j < 2 && j < n; ++j) {
         ok = wait1(kr.full_of(j), kr.parity(j), err);
@@ -403,19 +408,21 @@ __global__ void __launch_bounds__(NT_O, 1) out_tc(const __grid_constant__ TcArgs
       }
       for (int j = 0; ok && j < n; ++j) {
         const int b = j & 1;
-        ok = wait1(&pfull[b], static_cast<uint32_t>((j >> 1) & 1), err) && wait1(vr.full_of(j), vr.parity(j), err);
+        const uint32_t ph = static_cast<uint32_t>((j >> 1) & 1);
+        if (j + 2 < n) {  // every compute warp has loaded S(j): accumulator b takes S(j+2)
+          ok = wait1(&sempty[b], ph, err) && wait1(kr.full_of(j + 2), kr.parity(j + 2), err);
+          if (!ok) break;
+          tc::fence_after_sync();
+          issue_block<D>(tbase + b * BLK, sQ, sK + ((j + 2) % NK) * TB);
+          tc::mma_commit(&sfull[b]);
+          tc::mma_commit(&kr.empty[(j + 2) % NK]);
+        }
+        ok = wait1(&pfull[b], ph, err) && wait1(vr.full_of(j), vr.parity(j), err);
         if (!ok) break;
         tc::fence_after_sync();
         issue_pv_t<D>(o_tmem, tbase + kPcol + b * 64, sV + (j % NV) * TB, j > 0);
         tc::mma_commit(&pempty[b]);
         tc::mma_commit(&vr.empty[j % NV]);
-        if (j + 2 < n) {  // the compute warps are done with accumulator b (they have written P(j))
-          ok = wait1(kr.full_of(j + 2), kr.parity(j + 2), err);
-          if (!ok) break;
-          issue_block<D>(tbase + b * BLK, sQ, sK + ((j + 2) % NK) * TB);
-          tc::mma_commit(&sfull[b]);
-          tc::mma_commit(&kr.empty[(j + 2) % NK]);
-        }
       }
       if (ok) tc::mma_commit(ofull);
     }
@@ -436,6 +443,11 @@ __global__ void __launch_bounds__(NT_O, 1) out_tc(const __grid_constant__ TcArgs
       tc::fence_after_sync();
       float v[32];
       tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + col0), v);
+      // accumulator b may take the next logit block as soon as every compute
+      // warp has its slice in registers
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_plain(&sempty[b]);
       if (j == qb) {  // diagonal block: key col0 + e is visible to row rl if it is <= rl
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] = col0 + e <= rl ? ex2(fmaf(v[e], prm.qscale, -lse)) : 0.f;
