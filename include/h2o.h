@@ -191,6 +191,18 @@ H2O_API int h2o_cache_info(const h2o_cache* cache, int32_t* info);
 H2O_API int h2o_prefill_colsum_static(const void* q, const void* k, int batch, int heads, int head_dim,
                                       int prompt_len, int kv_dtype, float scale, float* colsum, void* stream);
 
+/* Self-test of the bounded waits every kernel of the library uses (they are
+ * how a device-side stall becomes an H2O_EDEVICE status instead of a hang).
+ * Launches one warp that waits, `polls` times (each poll suspends at most
+ * about 1 us), on an mbarrier nothing arrives at: once with the CTA-scope
+ * wait the stage rings use, once with the cluster-scope wait the decode
+ * cluster exchange uses.  Synchronous.  On return gave_up[0] and gave_up[1]
+ * are 1 if the respective wait gave up (the expected result) and elapsed_ns
+ * holds the device time the two waits took together.  polls must be in
+ * 1..1000000 (at most about 2 s); other values return H2O_EINVAL.  The device
+ * stays usable afterwards: nothing is left waiting. */
+H2O_API int h2o_selftest_wait_timeout(unsigned polls, int* gave_up, unsigned long long* elapsed_ns);
+
 /* Thread-local message describing the last error returned on this thread. */
 H2O_API const char* h2o_last_error(void);
 

@@ -45,6 +45,7 @@ SIGNATURES = {
     "h2o_cache_info": (_c_int, [_c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     "h2o_prefill_colsum_static": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
                                            _c_void_p, _c_void_p]),
+    "h2o_selftest_wait_timeout": (_c_int, [ctypes.c_uint, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_ulonglong)]),
     "h2o_last_error": (ctypes.c_char_p, []),
 }
 
@@ -235,6 +236,15 @@ def h2o_cache_info(cache: Cache) -> list[int]:
     info = (ctypes.c_int32 * 10)()
     _check(lib().h2o_cache_info(cache.handle, info))
     return list(info)
+
+
+def h2o_selftest_wait_timeout(polls: int) -> tuple[list[int], int]:
+    """Run the bounded-wait self-test; returns ([CTA-scope gave up, cluster-scope
+    gave up], elapsed device nanoseconds)."""
+    gave_up = (ctypes.c_int * 2)()
+    ns = ctypes.c_ulonglong(0)
+    _check(lib().h2o_selftest_wait_timeout(int(polls), gave_up, ctypes.byref(ns)))
+    return list(gave_up), int(ns.value)
 
 
 def h2o_prefill_colsum_static(q, k, scale, colsum, kv_dtype=None, stream=None):

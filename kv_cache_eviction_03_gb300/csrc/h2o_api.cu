@@ -13,6 +13,7 @@
 
 #include "h2o.h"
 #include "h2o_internal.cuh"
+#include "ptx.cuh"
 
 namespace {
 
@@ -104,6 +105,26 @@ cudaError_t kernel_attrs(const void* kern, size_t smem_bytes, bool nonportable_c
   return cudaSuccess;
 }
 }  // namespace h2o
+
+namespace {
+// One warp; lane 0 waits on an mbarrier that no thread or copy will ever
+// complete, first with the CTA-scope bounded wait, then with the
+// cluster-scope one, and records whether each gave up.
+__global__ void wait_timeout_probe(unsigned polls, int* out, unsigned long long* ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  h2o::mbar_init(&bar, 1);
+  h2o::fence_mbar_init();
+  unsigned long long t0, t1;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  const bool a = h2o::mbar_wait_bounded(&bar, 0u, polls);
+  const bool b = h2o::mbar_wait_cluster_bounded(&bar, 0u, polls);
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+  out[0] = a ? 0 : 1;
+  out[1] = b ? 0 : 1;
+  *ns = t1 - t0;
+}
+}  // namespace
 
 extern "C" {
 
@@ -484,6 +505,29 @@ int h2o_cache_info(const h2o_cache* c, int32_t* info) {
   info[7] = stages_in_use(c);
   info[8] = splits_in_use(c) == h2o::kDecodeWarpPerPair ? 128 : h2o::decode_threads(splits_in_use(c));
   info[9] = 0;
+  return H2O_OK;
+}
+
+int h2o_selftest_wait_timeout(unsigned polls, int* gave_up, unsigned long long* elapsed_ns) {
+  if (polls < 1 || polls > 1000000u || gave_up == nullptr || elapsed_ns == nullptr)
+    return fail(H2O_EINVAL, "h2o_selftest_wait_timeout: polls must be 1..1000000 and the outputs non-null");
+  void* buf = nullptr;
+  cudaError_t e = cudaMalloc(&buf, 16);
+  if (e != cudaSuccess) return cuda_fail(e, "h2o_selftest_wait_timeout: cudaMalloc");
+  int* flags = static_cast<int*>(buf);
+  unsigned long long* ns = reinterpret_cast<unsigned long long*>(static_cast<char*>(buf) + 8);
+  wait_timeout_probe<<<1, 32>>>(polls, flags, ns);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  int host_flags[2] = {0, 0};
+  unsigned long long host_ns = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(host_flags, flags, sizeof(host_flags), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(&host_ns, ns, sizeof(host_ns), cudaMemcpyDeviceToHost);
+  cudaFree(buf);
+  if (e != cudaSuccess) return cuda_fail(e, "h2o_selftest_wait_timeout");
+  gave_up[0] = host_flags[0];
+  gave_up[1] = host_flags[1];
+  *elapsed_ns = host_ns;
   return H2O_OK;
 }
 

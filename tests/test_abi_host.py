@@ -74,3 +74,14 @@ def test_state_layout_arithmetic():
     P, C = 6, 9
     assert lay["K"] == (64, P * C * 64 * 2)
     assert lay["total"] == 64 + 2 * P * C * 64 * 2 + P * C * 8 + P * 4 * 4 + P * 16
+
+
+def test_selftest_rejects_bad_poll_counts():
+    lib = B.lib()
+    gave_up = (ctypes.c_int * 2)()
+    ns = ctypes.c_ulonglong(0)
+    for polls in (0, 1_000_001):
+        assert lib.h2o_selftest_wait_timeout(polls, gave_up, ctypes.byref(ns)) == -1
+        assert lib.h2o_last_error().decode().startswith("h2o_selftest_wait_timeout")
+    assert lib.h2o_selftest_wait_timeout(10, None, ctypes.byref(ns)) == -1
+
