@@ -429,63 +429,104 @@ __global__ void __launch_bounds__(NT_O, 1) out_tc(const __grid_constant__ TcArgs
     __syncwarp();
   } else {  // compute warps: lane quarter (warp % 4) x column part (32 of the 128)
     const int quarter = warp & 3, part = (warp - 2) >> 2;
-    const int rl = quarter * 32 + lane;  // TMEM lane = query row qb * BLK + rl
+    const int rl = quarter * 32 + lane;  // O readout: TMEM lane = query row qb * BLK + rl
     const int col0 = part * 32;          // this warp's keys in a block / its O columns
     const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
-    const float lse = lse_at(prm.lse2 + static_cast<size_t>(pair) * L, qb * BLK, rl, Lp);
+    // Logits are read in the 16x256b shape, two loads per block (lane halves
+    // h = 0, 1 of the quarter): element e of repetition k of half h holds
+    // row r4 + 16h + 8(e >> 1) and key k4 + 8k + (e & 1).  Each thread thus
+    // holds 4 rows x 8 keys, and a key's 32 rows of the quarter sit in the 8
+    // lanes that share lane % 4.
+    const int r4 = quarter * 32 + (lane >> 2);
+    const int k4 = col0 + 2 * (lane & 3);
+    float nlse[4];  // -lse of row r4 + 8i, i = 2h + (e >> 1)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) nlse[i] = -lse_at(prm.lse2 + static_cast<size_t>(pair) * L, qb * BLK, r4 + 8 * i, Lp);
     // this pair's column-sum partials: one 4 x 128-float row per (query block, key block <= it)
     float* cs_part = prm.cs_part ? prm.cs_part + static_cast<size_t>(pair) * colsum_partial_floats(L, 1) : nullptr;
+    const uint64_t qs2 = f2_pack(prm.qscale, prm.qscale);
+    const uint32_t half_hi = 16u << 16;  // TMEM lane offset of the upper half
     bool ok = true;
     for (int j = 0; ok && j < n; ++j) {
       const int b = j & 1;
       ok = wait_warp(&sfull[b], static_cast<uint32_t>((j >> 1) & 1), lane, err);
       if (!ok) break;
       tc::fence_after_sync();
-      float v[32];
-      tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + col0), v);
+      uint32_t raw[2][16];
+      const uint32_t sa = lane_addr + static_cast<uint32_t>(b * BLK + col0);
+      tc::tmem_ld_16x256b_x4_pair(sa, sa + half_hi, raw[0], raw[1]);
       // accumulator b may take the next logit block as soon as every compute
       // warp has its slice in registers
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_plain(&sempty[b]);
-      if (j == qb) {  // diagonal block: key col0 + e is visible to row rl if it is <= rl
+      float v[2][16];  // probabilities, same element order as raw
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = col0 + e <= rl ? ex2(fmaf(v[e], prm.qscale, -lse)) : 0.f;
-      } else {
-        const uint64_t qs2 = f2_pack(prm.qscale, prm.qscale), nl2 = f2_pack(-lse, -lse);
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(v[2 * e], v[2 * e + 1]), qs2, nl2), x0, x1);
-          v[2 * e] = ex2(x0);
-          v[2 * e + 1] = ex2(x1);
-        }
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            const int i = 2 * h + g, e = 4 * k + 2 * g;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(raw[h][e]), __uint_as_float(raw[h][e + 1])), qs2,
+                             f2_pack(nlse[i], nlse[i])),
+                      x0, x1);
+            v[h][e] = ex2(x0);
+            v[h][e + 1] = ex2(x1);
+          }
+      if (j == qb) {  // diagonal block: key k is visible to row r if k <= r
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (k4 + 8 * k + (e & 1) > r4 + 16 * h + 8 * (e >> 1)) v[h][4 * k + e] = 0.f;
       }
-      uint32_t ph[16];  // this thread's 32 probabilities as fp16 pairs
+      // probability block b (TMEM) was last read by O(j-2).  Keys k4 + 8k and
+      // k4 + 8k + 1 of a row are one fp16 pair, packed column col0/2 + 4k +
+      // lane % 4: the 16x128b store puts element g of repetition k there, in
+      // row r4 + 16h + 8g.
+      uint32_t ph[2][8];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) ph[e] = tc::cvt_half2(v[2 * e], v[2 * e + 1]);
-      // probability block b (TMEM) was last read by O(j-2); this thread's 32
-      // keys go to its lane's 16 packed columns of that block
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int g = 0; g < 2; ++g) ph[h][2 * k + g] = tc::cvt_half2(v[h][4 * k + 2 * g], v[h][4 * k + 2 * g + 1]);
       if (j >= 2 && !(ok = wait_warp(&pempty[b], static_cast<uint32_t>(((j - 2) >> 1) & 1), lane, err))) break;
-      tc::tmem_st16(lane_addr + kPcol + static_cast<uint32_t>(b * 64 + part * 16), ph);
+      const uint32_t pa = lane_addr + kPcol + static_cast<uint32_t>(b * 64 + col0 / 2);
+      tc::tmem_st_16x128b_x4(pa, ph[0]);
+      tc::tmem_st_16x128b_x4(pa + half_hi, ph[1]);
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_plain(&pfull[b]);
       if (cs_part) {
-        // while the tensor core works on P V: column sums over this warp's 32
-        // rows (a reduce-scatter: after it lane t holds column col0 + t), one
-        // 128-byte store per warp
+        // while the tensor core works on P V: column sums over the quarter's
+        // 32 rows.  Each thread adds its 4 rows of its 8 keys (c[2k + x] for
+        // key k4 + 8k + x), then a reduce-scatter over the lanes sharing
+        // lane % 4 leaves key index (lane >> 2) & 7 in each lane; one
+        // 128-byte store per warp.
+        float c[8];
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int x = 0; x < 2; ++x)
+            c[2 * k + x] = (v[0][4 * k + x] + v[0][4 * k + 2 + x]) + (v[1][4 * k + x] + v[1][4 * k + 2 + x]);
+#pragma unroll
+        for (int off = 16, w = 4; off >= 4; off >>= 1, w >>= 1) {
           const bool hi = (lane & off) != 0;
 #pragma unroll
-          for (int i = 0; i < off; ++i) {
-            const float keep = hi ? v[i + off] : v[i];
-            const float send = hi ? v[i] : v[i + off];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+          for (int i = 0; i < w; ++i) {
+            const float keep = hi ? c[i + w] : c[i];
+            const float send = hi ? c[i] : c[i + w];
+            c[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
           }
         }
-        cs_part[(static_cast<size_t>(qb) * (qb + 1) / 2 + j) * (4 * BLK) + quarter * BLK + col0 + lane] = v[0];
+        const int c8 = (lane >> 2) & 7;
+        cs_part[(static_cast<size_t>(qb) * (qb + 1) / 2 + j) * (4 * BLK) + quarter * BLK + k4 + 8 * (c8 >> 1) +
+                (c8 & 1)] = c[0];
       }
     }
     ok = ok && wait_warp(ofull, 0, lane, err);
