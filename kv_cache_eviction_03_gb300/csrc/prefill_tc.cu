@@ -248,6 +248,11 @@ __global__ void __launch_bounds__(NT, 2) stats_tc(const __grid_constant__ TcArgs
         const int col0 = half * 64 + c * 32;
         float v[32];
         tc::tmem_ld32(lane_addr + static_cast<uint32_t>(b * BLK + col0), v);
+        if (c == 1) {  // both loads of block j are done: accumulator b may take S(j+2)
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive_plain(&sempty[b]);
+        }
         if (j == qb) {  // diagonal block: key col0 + e is visible to row rl if it is <= rl
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = col0 + e <= rl ? v[e] : -INFINITY;
@@ -278,9 +283,6 @@ __global__ void __launch_bounds__(NT, 2) stats_tc(const __grid_constant__ TcArgs
         l = l * ex2(m - mn) + ((a0 + a1) + (a2 + a3));
         m = mn;
       }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive_plain(&sempty[b]);  // accumulator b may be overwritten
     }
     // merge the two column halves of each row
     if (half == 1) red[rl] = make_float2(m, l);
