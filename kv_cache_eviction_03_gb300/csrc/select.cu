@@ -54,24 +54,80 @@ __device__ __forceinline__ unsigned block_scan(bool flag, Scan& sh, unsigned* to
   return r;
 }
 
-// copy `n` rows listed in (src_pos, dst_slot) from the prompt into the slot store
+// copy `n` rows listed in (src_pos, dst_slot) from the prompt into the slot
+// store; each thread loads its 16-byte pieces of four rows before storing
+// them, so four rows' loads are in flight at once
 template <int ROWB>
 __device__ __forceinline__ void copy_rows(const unsigned char* srcK, const unsigned char* srcV, unsigned char* dstK,
                                           unsigned char* dstV, const int* src_pos, const int* dst_slot, int n) {
   constexpr int LPR = ROWB / 16;
   constexpr int RPI = 32 / LPR;
+  constexpr int STEP = NW * RPI, UNROLL = 4;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int grp = lane / LPR, lig = lane % LPR;
-  for (int i = warp * RPI + grp; i < n; i += NW * RPI) {
-    const size_t so = static_cast<size_t>(src_pos[i]) * ROWB + lig * 16;
-    const size_t dofs = static_cast<size_t>(dst_slot[i]) * ROWB + lig * 16;
-    *reinterpret_cast<uint4*>(dstK + dofs) = *reinterpret_cast<const uint4*>(srcK + so);
-    *reinterpret_cast<uint4*>(dstV + dofs) = *reinterpret_cast<const uint4*>(srcV + so);
+  for (int i0 = warp * RPI + grp; i0 < n; i0 += UNROLL * STEP) {
+    uint4 kv[UNROLL], vv[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int i = i0 + u * STEP;
+      if (i < n) {
+        const size_t so = static_cast<size_t>(src_pos[i]) * ROWB + lig * 16;
+        kv[u] = *reinterpret_cast<const uint4*>(srcK + so);
+        vv[u] = *reinterpret_cast<const uint4*>(srcV + so);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int i = i0 + u * STEP;
+      if (i < n) {
+        const size_t dofs = static_cast<size_t>(dst_slot[i]) * ROWB + lig * 16;
+        *reinterpret_cast<uint4*>(dstK + dofs) = kv[u];
+        *reinterpret_cast<uint4*>(dstV + dofs) = vv[u];
+      }
+    }
+  }
+}
+
+// The digit d of this radix pass: the largest d >= 1 whose bins d..255 hold
+// at least k keys (d = 0 if none does), with cum = the keys in bins above d.
+// Warp 0 does it: lane l sums bins 255-8l .. 248-8l, a shuffle scan finds
+// the lane where the running count reaches k, and that lane walks its bins
+// and publishes prefix | d << shift, k - cum and the count in bin d.
+__device__ __forceinline__ void pick_digit(const unsigned* hist, unsigned k, unsigned prefix, int shift,
+                                           unsigned* s_prefix, unsigned* s_k, unsigned* s_eq) {
+  const int lane = threadIdx.x & 31;
+  const int top = 255 - 8 * lane;
+  unsigned loc = 0;
+#pragma unroll
+  for (int x = 0; x < 8; ++x) loc += hist[top - x];
+  unsigned inc = loc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  const unsigned exc = inc - loc;
+  const unsigned who = __ballot_sync(0xffffffffu, exc < k && inc >= k);
+  const int owner = who ? __ffs(who) - 1 : 31;
+  if (lane == owner) {
+    unsigned cum = exc, d = 0;
+    for (int x = 0; x < 8; ++x) {
+      const int dd = top - x;
+      if (dd == 0) break;
+      if (cum + hist[dd] >= k) {
+        d = static_cast<unsigned>(dd);
+        break;
+      }
+      cum += hist[dd];
+    }
+    *s_prefix = prefix | (d << shift);
+    *s_k = k - cum;
+    *s_eq = hist[d];
   }
 }
 
 template <int ROWB>
-__global__ void __launch_bounds__(NT, 1) select_kernel(const SelectParams prm) {
+__global__ void __launch_bounds__(NT, 2) select_kernel(const SelectParams prm) {
   __shared__ unsigned hist[256];
   __shared__ Scan scan;
   __shared__ int list_pos[NT];
@@ -121,17 +177,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const SelectParams prm) {
           if ((bits & mask) == prefix) atomicAdd(&hist[(bits >> shift) & 255u], 1u);
         }
         __syncthreads();
-        if (tid == 0) {
-          unsigned cum = 0;
-          int d = 255;
-          for (; d > 0; --d) {
-            if (cum + hist[d] >= k) break;
-            cum += hist[d];
-          }
-          s_prefix = prefix | (static_cast<unsigned>(d) << shift);
-          s_k = k - cum;
-          s_eq = hist[d];
-        }
+        if (tid < 32) pick_digit(hist, k, prefix, shift, &s_prefix, &s_k, &s_eq);
         __syncthreads();
         prefix = s_prefix;
         k = s_k;
