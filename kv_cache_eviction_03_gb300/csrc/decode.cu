@@ -524,13 +524,15 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
     prm.out[static_cast<size_t>(pair) * D + tid] = acc * inv;
   }
 
-  // probabilities -> accumulated scores; local minimum candidate key
+  // probabilities -> accumulated scores, stored at once (the evicted slot's
+  // score is overwritten with the newcomer's below, after the block barrier
+  // that orders the two stores); local minimum candidate key
   const int limit = p - R;  // candidates: kept positions <= p - R
   unsigned long long kmin = ~0ull;
   int smin = -1;
   for (int j = tid; j < nrows; j += NT) {
     const float ns = sc[j] + exp2f(lg[j] - M) * inv;
-    sc[j] = ns;
+    prm.score[slot0 + j] = ns;
     if (full && ps[j] <= limit) {
       const unsigned long long key =
           (static_cast<unsigned long long>(__float_as_uint(ns)) << 32) | static_cast<uint32_t>(ps[j]);
@@ -595,8 +597,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
   // reads another's shared memory, so the CTAs of a cluster leave without a
   // cluster barrier.
 
-  // write back: scores of this CTA's slots, the new token into slot u
-  for (int j = tid; j < nrows; j += NT) prm.score[slot0 + j] = (lo + j == u) ? p_self : sc[j];
+  // the new token into slot u
   if (u >= lo && u < lo + prm.chunk && u >= 0) {
     const size_t us = static_cast<size_t>(pair) * C + u;
     if (tid < 2 * LPR) {
@@ -605,7 +606,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
     }
     if (tid == 0) {
       prm.pos[us] = p;
-      if (u >= lo + nrows) prm.score[us] = p_self;  // fill phase: slot was empty
+      prm.score[us] = p_self;
     }
   }
   if (rank == 0 && tid == 0) {
@@ -807,8 +808,10 @@ __global__ void __launch_bounds__(kWarpNW * 32, 1) decode_warp_kernel(const Deco
       for (int e = 0; e < EPV; e += 4)
         *reinterpret_cast<float4*>(dst + e) = make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
     }
-    // probabilities -> accumulated scores; the lowest candidate key (score
-    // bits, position) among kept positions <= p - R
+    // probabilities -> accumulated scores, stored at once (after a failed
+    // wait nothing is stored; the evicted slot's score is overwritten with
+    // the newcomer's below, in program order after a warp barrier); the
+    // lowest candidate key (score bits, position) among kept positions <= p - R
     cp_async_wait<0>();
     __syncwarp();
     const bool fullc = count >= C;
@@ -817,7 +820,7 @@ __global__ void __launch_bounds__(kWarpNW * 32, 1) decode_warp_kernel(const Deco
     int smin = -1;
     for (int j = lane; j < count; j += 32) {
       const float ns = sc[j] + exp2f(lg[j] - m) * inv;
-      sc[j] = ns;
+      if (ok) prm.score[slot0 + j] = ns;
       if (fullc && ps[j] <= limit) {
         const unsigned long long key =
             (static_cast<unsigned long long>(__float_as_uint(ns)) << 32) | static_cast<uint32_t>(ps[j]);
@@ -839,7 +842,6 @@ __global__ void __launch_bounds__(kWarpNW * 32, 1) decode_warp_kernel(const Deco
     __syncwarp();
     if (ok) {
       if (fullc && u < 0 && lane == 0) atomicOr(prm.err, ERR_NO_CANDIDATE);
-      for (int j = lane; j < count; j += 32) prm.score[slot0 + j] = (j == u) ? p_self : sc[j];
       if (u >= 0) {
         // the new row from the slices already in registers: row group 0
         // writes K, group 1 writes V (one group covering the row: both)
@@ -848,7 +850,7 @@ __global__ void __launch_bounds__(kWarpNW * 32, 1) decode_warp_kernel(const Deco
         if (grp == (LPR == 32 ? 0 : 1)) *reinterpret_cast<uint4*>(static_cast<unsigned char*>(prm.V) + us) = v4;
         if (lane == 0) {
           prm.pos[slot0 + u] = p;
-          if (u >= count) prm.score[slot0 + u] = p_self;  // fill phase: the slot was empty
+          prm.score[slot0 + u] = p_self;
         }
       }
       if (lane == 0) {
