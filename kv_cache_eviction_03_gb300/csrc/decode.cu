@@ -1113,9 +1113,7 @@ int warp_grid(int dtype, int D, int nstage, int C, int pairs) {
 }
 }  // namespace
 
-cudaError_t launch_decode(const DecodeParams& prm, int dtype, int D, int pairs, int splits, int threads,
-                          cudaStream_t s) {
-  (void)threads;
+cudaError_t launch_decode(const DecodeParams& prm, int dtype, int D, int pairs, int splits, cudaStream_t s) {
   if ((dtype != 0 && dtype != 1) || (D != 64 && D != 128)) return cudaErrorInvalidValue;
   if (splits == kDecodeWarpPerPair) {
     if (prm.C > kWarpMaxSlots || prm.nstage < 2 || prm.nstage > kWarpMaxStages) return cudaErrorInvalidValue;

@@ -346,7 +346,7 @@ int h2o_decode_step(h2o_cache* c, const void* q, const void* k_new, const void* 
   dp.qscale = scale * 1.4426950408889634f;
   dp.prefetch = touch_stream(c, stream) ? 1 : 0;
   dp.pairs = c->P;
-  cudaError_t e = h2o::launch_decode(dp, c->dtype, c->D, c->P, splits, 128, as_stream(stream));
+  cudaError_t e = h2o::launch_decode(dp, c->dtype, c->D, c->P, splits, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "h2o_decode_step: launch");
   c->host_next_p += 1;
   return H2O_OK;

@@ -42,7 +42,7 @@ struct DecodeParams {
   int C, R;
   int chunk;          // slots per CTA of a pair's cluster (multiple of 4)
   float qscale;       // scale * log2(e): logits kept in the base-2 domain
-  int nstage;         // depth of the shared-memory stage ring (1..16)
+  int nstage;         // stage ring depth: a multiple of the cluster kernel's consumer warps (<= 18), or 2..8 per warp (warp per pair)
   int prefetch;       // 1: the previous kernel on the stream did not touch
                       // this cache, so its slot store may be read before the
                       // grid-dependency wait
@@ -107,8 +107,7 @@ int set_error(int code, const char* fmt, ...);
 cudaError_t kernel_attrs(const void* kern, size_t smem_bytes, bool nonportable_cluster);
 
 // Launchers (return the launch error; they do not synchronise).
-cudaError_t launch_decode(const DecodeParams& prm, int dtype, int D, int pairs, int splits, int threads,
-                          cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& prm, int dtype, int D, int pairs, int splits, cudaStream_t s);
 // splits value selecting the warp-per-pair decode kernel (one warp streams
 // a whole pair, each CTA's warps work through several pairs in turn)
 constexpr int kDecodeWarpPerPair = -1;
