@@ -24,6 +24,10 @@ order the method states it.  Sources (page title, then section):
 * same page, section 2.3 (its Figure 2(d) comparison): the online ("local")
   rule set against a global one that may use the whole sequence's attention,
   future rows included (global_select_pair, heavy_overlap).
+* same page, section 4.4 (Q1, infinite streaming "with position rolling"):
+  rotary position embedding applied with positions counted inside the cache
+  rather than in the text (rope_rotate, cache_ranks, decode_step_pair with
+  rope_base).
 
 Readings taken where the pages are loose (each also listed in the design
 notes): the score is the column sum of attention probabilities (the report's
@@ -180,6 +184,34 @@ def heavy_overlap(local_pos, global_pos, n, recent):
     return len(lh & gh), len(gh)
 
 
+# --------------------------------------------------------------------------- position rolling
+def rope_rotate(x, positions, base):
+    """Rotary position embedding (Su et al., RoFormer, 2021): the element pair
+    (2i, 2i+1) of each row is rotated by the angle position * base^(-2i/D).
+    x: [n, D] float64, positions: [n]."""
+    x = np.asarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    theta = base ** (-2.0 * np.arange(D // 2) / D)
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * theta[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    out = np.empty_like(x)
+    out[:, 0::2] = x[:, 0::2] * c - x[:, 1::2] * s
+    out[:, 1::2] = x[:, 0::2] * s + x[:, 1::2] * c
+    return out
+
+
+def cache_ranks(pos):
+    """Position inside the cache of every kept slot: its rank among the kept
+    tokens ordered by their position in the text (-1 for an empty slot).
+    Reading of "position rolling" (section 4.4): the kept tokens are numbered
+    0..n-1 in text order, the token being generated gets n."""
+    pos = np.asarray(pos)
+    ranks = np.full(pos.shape, -1, dtype=np.int64)
+    kept = np.nonzero(pos >= 0)[0]
+    ranks[kept[np.argsort(pos[kept], kind="stable")]] = np.arange(kept.size)
+    return ranks
+
+
 # --------------------------------------------------------------------------- decode
 @dataclass
 class StepResult:
@@ -189,8 +221,13 @@ class StepResult:
     prob: np.ndarray  # [count + 1] probabilities (kept slots, then self)
 
 
-def decode_step_pair(st: PairState, q, k_new, v_new, scale, heavy, recent) -> StepResult:
+def decode_step_pair(st: PairState, q, k_new, v_new, scale, heavy, recent, rope_base=None) -> StepResult:
     """One decode step of one pair, in place on `st` (sections 3.1, 3.3, 3.4).
+
+    With rope_base (position rolling, section 4.4) the logits are taken
+    between rotary-embedded vectors, each kept key at its rank inside the
+    cache (cache_ranks) and the query and the new key at n, the number of
+    kept tokens; the cache stores the keys as given (not rotated).
 
     1. attend over the kept slots and the new token itself; the softmax
        normaliser covers only those entries;
@@ -206,8 +243,14 @@ def decode_step_pair(st: PairState, q, k_new, v_new, scale, heavy, recent) -> St
     n = st.count
     p = st.p
     logits = np.empty(n + 1)
-    logits[:n] = scale * (st.K[:n] @ q)
-    logits[n] = scale * float(k_new @ q)
+    if rope_base is None:
+        logits[:n] = scale * (st.K[:n] @ q)
+        logits[n] = scale * float(k_new @ q)
+    else:
+        qr = rope_rotate(np.asarray(q)[None, :], [n], rope_base)[0]
+        kr = rope_rotate(st.K[:n], cache_ranks(st.pos[:n]), rope_base)
+        logits[:n] = scale * (kr @ qr)
+        logits[n] = scale * float(rope_rotate(np.asarray(k_new)[None, :], [n], rope_base)[0] @ qr)
     m = logits.max()
     e = np.exp(logits - m)
     prob = e / e.sum()
@@ -291,16 +334,17 @@ def prefill(q, k, v, heavy, recent, scale):
     return CacheState.stack(states), np.stack(colsums), np.stack(outs)
 
 
-def decode_step(state: CacheState, q, k_new, v_new, heavy, recent, scale):
+def decode_step(state: CacheState, q, k_new, v_new, heavy, recent, scale, rope_base=None):
     """One decode step for every pair.  q, k_new, v_new: [B, H, D].
 
     Returns (new_state, out [P, D], evicted [P], gap [P]); `state` is untouched.
+    rope_base: position rolling (see decode_step_pair), None for none.
     """
     q, k_new, v_new = _pairs(q), _pairs(k_new), _pairs(v_new)
     new_pairs, outs, ev, gaps = [], [], [], []
     for i in range(q.shape[0]):
         st = state.pair(i)
-        r = decode_step_pair(st, q[i], k_new[i], v_new[i], scale, heavy, recent)
+        r = decode_step_pair(st, q[i], k_new[i], v_new[i], scale, heavy, recent, rope_base)
         new_pairs.append(st)
         outs.append(r.out)
         ev.append(r.evicted)

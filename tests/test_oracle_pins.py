@@ -400,3 +400,54 @@ def test_local_run_matches_global_under_uniform_attention():
 def test_heavy_overlap_counts_only_heavy_positions():
     assert O.heavy_overlap([0, 3, 5, 8, 9], [0, 4, 5, 8, 9], 10, 2) == (2, 3)
     assert O.heavy_overlap([8, 9], [8, 9], 10, 2) == (0, 0)
+
+
+# ------------------------------------------------------------------ position rolling
+def test_rope_rotation_closed_form_and_relative_property():
+    """D = 2: the pair is rotated by exactly `position` radians (theta_0 = 1).
+    Any D: rotations keep norms, and <R(m) q, R(n) k> = <q, R(n - m) k>."""
+    x = np.array([[1.0, 0.0], [0.6, -0.8]])
+    got = O.rope_rotate(x, [0.5, 2.0], 10000.0)
+    want = np.array([[math.cos(0.5), math.sin(0.5)],
+                     [0.6 * math.cos(2.0) + 0.8 * math.sin(2.0), 0.6 * math.sin(2.0) - 0.8 * math.cos(2.0)]])
+    np.testing.assert_allclose(got, want, atol=1e-15)
+    rng = np.random.default_rng(7)
+    q, k = rng.standard_normal((2, 16))
+    for m, n in [(0, 0), (3, 11), (40, 7), (1000, 1003)]:
+        a = float(O.rope_rotate(q[None], [m], 500.0)[0] @ O.rope_rotate(k[None], [n], 500.0)[0])
+        b = float(q @ O.rope_rotate(k[None], [n - m], 500.0)[0])
+        assert abs(a - b) < 1e-12
+    np.testing.assert_allclose(np.linalg.norm(O.rope_rotate(q[None], [123], 500.0)), np.linalg.norm(q), rtol=1e-14)
+
+
+def test_cache_ranks_count_smaller_positions():
+    rng = np.random.default_rng(9)
+    for _ in range(30):
+        C = int(rng.integers(1, 20))
+        pos = rng.permutation(100)[:C].astype(np.int64)
+        pos[rng.random(C) < 0.3] = -1
+        ranks = O.cache_ranks(pos)
+        for j in range(C):
+            want = -1 if pos[j] < 0 else int(np.sum((pos >= 0) & (pos < pos[j])))
+            assert ranks[j] == want
+
+
+def test_rolling_without_eviction_is_rotary_attention():
+    """From an empty cache that never fills, every kept token's rank is its
+    position, so each step is causal attention over rotary-embedded q and k
+    at their text positions: checked against torch's fp64 attention on vectors
+    rotated here as complex numbers."""
+    T, D, heavy, recent, base = 14, 8, 10, 8, 100.0
+    rng = np.random.default_rng(11)
+    q, k, v = rng.standard_normal((3, T, D))
+    st = O.empty_pair(heavy + recent, recent, D)
+    outs = [O.decode_step_pair(st, q[t], k[t], v[t], 0.7, heavy, recent, rope_base=base).out for t in range(T)]
+
+    def rotate(x):
+        xc = torch.from_numpy(x[:, 0::2] + 1j * x[:, 1::2])
+        ang = torch.arange(T, dtype=torch.float64)[:, None] * base ** (-2.0 * torch.arange(D // 2) / D)[None, :]
+        r = xc * torch.exp(1j * ang)
+        return torch.stack([r.real, r.imag], dim=-1).reshape(T, D).numpy()
+
+    ref = sdpa_causal(rotate(q), rotate(k), v, 0.7)
+    np.testing.assert_allclose(np.stack(outs), ref, atol=1e-12)
