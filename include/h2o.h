@@ -164,6 +164,21 @@ H2O_API int h2o_cache_check(h2o_cache* cache, void* stream);
 #define H2O_DECODE_WARP_PER_PAIR (-1)
 H2O_API int h2o_cache_set_decode_shape(h2o_cache* cache, int splits, int stages);
 
+/* Position rolling for long or endless streams ("... 深度解读报告", section
+ * 4.4: H2O with position rolling on 4-million-token streams).  With
+ * rope_base > 0 every decode step takes its logits between rotary-embedded
+ * vectors (RoFormer: element pair (2i, 2i+1) rotated by position *
+ * rope_base^(-2i/D)) whose positions count inside the cache: the kept tokens
+ * are numbered 0..n-1 in text order and the new token gets n.  q, k_new and
+ * the cached keys are given, and kept, unrotated.  rope_base = 0 turns it
+ * off.  Synchronous: waits for the device and reads the positions back to
+ * rank the kept tokens.  While it is on, h2o_prefill, h2o_prefill_ex and
+ * h2o_prefill_ragged return H2O_ESTATE (they apply no rotary embedding;
+ * decode from an empty or reset cache), and decode runs on the cluster
+ * kernel (a warp-per-pair shape is refused; turning it on resets the shape
+ * to automatic).  Returns H2O_EINVAL for a negative or non-finite base. */
+H2O_API int h2o_cache_set_position_rolling(h2o_cache* cache, float rope_base);
+
 /* info[0..9] = {batch, heads, head_dim, heavy, recent, kv_dtype,
  *               decode splits in use (-1: warp per pair), decode stages in
  *               use, decode threads per CTA, 0}. */

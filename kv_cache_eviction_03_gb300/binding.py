@@ -45,6 +45,7 @@ SIGNATURES = {
     "h2o_cache_info": (_c_int, [_c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     "h2o_prefill_colsum_static": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
                                            _c_void_p, _c_void_p]),
+    "h2o_cache_set_position_rolling": (_c_int, [_c_void_p, _c_float]),
     "h2o_selftest_wait_timeout": (_c_int, [ctypes.c_uint, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_ulonglong)]),
     "h2o_last_error": (ctypes.c_char_p, []),
 }
@@ -230,6 +231,11 @@ def h2o_cache_check(cache: Cache, stream=None):
 
 def h2o_cache_set_decode_shape(cache: Cache, splits: int = 0, stages: int = 0):
     _check(lib().h2o_cache_set_decode_shape(cache.handle, splits, stages))
+
+
+def h2o_cache_set_position_rolling(cache: Cache, rope_base: float):
+    """Rotary embedding at positions inside the cache (0 turns it off)."""
+    _check(lib().h2o_cache_set_position_rolling(cache.handle, float(rope_base)))
 
 
 def h2o_cache_info(cache: Cache) -> list[int]:

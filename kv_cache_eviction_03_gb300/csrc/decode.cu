@@ -97,16 +97,34 @@ struct DecodeCfg : RowGeom<T, D> {
 // copies of each), and the probabilities go through the warp's shared buffer
 // wb to the lanes that weight V.  After the call the warp no longer reads the
 // stage.
-template <typename T, int D, int TILE>
+// Position rolling: rotate this lane's EPV/2 element pairs (2i, 2i+1) of a
+// row by the angles whose (cos, sin) sit at `cs` (the row's rank in the
+// table, the lane's pairs), as in the rotary embedding.
+template <int EPV>
+__device__ __forceinline__ void rope_rotate_lane(float (&x)[EPV], const float2* cs) {
+#pragma unroll
+  for (int h = 0; h < EPV / 4; ++h) {
+    const float4 t = __ldg(reinterpret_cast<const float4*>(cs) + h);  // (cos, sin) of two pairs
+    const float a0 = x[4 * h], a1 = x[4 * h + 1], b0 = x[4 * h + 2], b1 = x[4 * h + 3];
+    x[4 * h] = a0 * t.x - a1 * t.y;
+    x[4 * h + 1] = a0 * t.y + a1 * t.x;
+    x[4 * h + 2] = b0 * t.z - b1 * t.w;
+    x[4 * h + 3] = b0 * t.w + b1 * t.z;
+  }
+}
+
+template <typename T, int D, int TILE, bool ROPE = false>
 __device__ __forceinline__ void attend_tile(const unsigned char* sK, const unsigned char* sV, int rows,
                                             const float (&qv)[RowGeom<T, D>::EPV], float& m, float& l,
-                                            float (&o)[RowGeom<T, D>::EPV], float* wb, float* lg, int lane) {
+                                            float (&o)[RowGeom<T, D>::EPV], float* wb, float* lg, int lane,
+                                            const int* rk = nullptr, const float2* rope = nullptr) {
   using Gm = RowGeom<T, D>;
   constexpr int EPV = Gm::EPV, LPR = Gm::LPR, ROWB = Gm::ROWB;
   constexpr int G = Gm::RPI;      // row groups per warp
   constexpr int RG = TILE / G;    // rows per group per stage
   constexpr int DUP = LPR / RG;   // lanes holding each row's total
   static_assert(RG >= 1 && RG <= LPR && LPR % RG == 0, "butterfly shape");
+  static_assert(!ROPE || EPV % 4 == 0, "a lane holds whole pairs of pairs");
   const int grp = lane / LPR, lig = lane % LPR;
   float acc[RG];
 #pragma unroll
@@ -114,6 +132,9 @@ __device__ __forceinline__ void attend_tile(const unsigned char* sK, const unsig
     const int row = grp * RG + r;
     float kf[EPV];
     Vec16<T>::unpack(*reinterpret_cast<const uint4*>(sK + row * ROWB + lig * 16), kf);
+    if constexpr (ROPE) {  // key rotated to its rank inside the cache (lg, rk: this stage's rows)
+      if (row < rows) rope_rotate_lane<EPV>(kf, rope + static_cast<size_t>(rk[row]) * (D / 2) + lig * (EPV / 2));
+    }
     float a = 0.f;
 #pragma unroll
     for (int e = 0; e < EPV; ++e) a = fmaf(qv[e], kf[e], a);
@@ -201,8 +222,9 @@ struct __align__(16) Xch {
 
 // Shared-memory layout (bytes); identical on host and device.  The stage ring
 // depth, the CTA's slot count and the cluster size are launch parameters.
-template <int D, int NCW, int TILE, int STAGE>
+template <int D, int NCW, int TILE, int STAGE, bool ROPE>
 struct Layout {
+  static constexpr int PER_SLOT = ROPE ? 16 : 12;  // logit, score, position (, rank)
   static constexpr size_t full = 0;                            // kMaxStages mbarriers
   static constexpr size_t empty = 8 * kMaxStages;              // kMaxStages mbarriers
   static constexpr size_t xbar = 16 * kMaxStages;              // mbarrier: the peers' partials have landed
@@ -217,7 +239,7 @@ struct Layout {
   // after the logits, scores and positions of the CTA's slots: rank 0's
   // copies of the other ranks' partial output rows (rank r at r - 1)
   __host__ __device__ static size_t rows_in(int nstage, int chunk) {
-    return (tail(nstage) + static_cast<size_t>(chunk) * 12 + 15) / 16 * 16;
+    return (tail(nstage) + static_cast<size_t>(chunk) * PER_SLOT + 15) / 16 * 16;
   }
   __host__ __device__ static size_t bytes(int nstage, int chunk, int splits) {
     return rows_in(nstage, chunk) + (splits > 1 ? static_cast<size_t>(splits - 1) * D * 4 : 0);
@@ -237,10 +259,10 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-template <typename T, int D, int NCW, int TILE>
+template <typename T, int D, int NCW, int TILE, bool ROPE>
 __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel(const DecodeParams prm) {
   using Cfg = DecodeCfg<T, D, NCW, TILE>;
-  using Lay = Layout<D, NCW, TILE, Cfg::STAGE>;
+  using Lay = Layout<D, NCW, TILE, Cfg::STAGE, ROPE>;
   // Stage s is always consumed by warp s % NCW: with a ring depth that is a
   // multiple of NCW a warp never waits two phases ahead on a stage another
   // warp still owns, so mbarrier parity waits cannot alias.  Other depths
@@ -269,6 +291,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
   float* lg = reinterpret_cast<float*>(smem + Lay::tail(NSTAGE));
   float* sc = lg + prm.chunk;
   int* ps = reinterpret_cast<int*>(sc + prm.chunk);
+  int* rk = ps + prm.chunk;  // slot ranks inside the cache (position rolling only)
   float* xo_in = reinterpret_cast<float*>(smem + Lay::rows_in(NSTAGE, prm.chunk));
 
   cg::cluster_group cluster = cg::this_cluster();
@@ -361,6 +384,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
       for (int j = tid; j < nrows; j += NCW * 32) {
         sc[j] = prm.score[slot0 + j];
         ps[j] = prm.pos[slot0 + j];
+        if constexpr (ROPE) rk[j] = prm.rank[slot0 + j];
       }
     };
     // warm L2 with this pair's q, k_new and v_new rows while waiting
@@ -401,10 +425,18 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
     Vec16<T>::unpack(q4, qv);
 #pragma unroll
     for (int e = 0; e < EPV; ++e) qv[e] *= prm.qscale;  // exp2(logit) is the softmax numerator
+    // position rolling: the query (and the new key) sit at rank `count`, after
+    // every kept token
+    const float2* rope_cs = nullptr;
+    if constexpr (ROPE) {
+      rope_cs = prm.rope + static_cast<size_t>(count) * (D / 2) + lig * (EPV / 2);
+      rope_rotate_lane<EPV>(qv, rope_cs);
+    }
     if (rank == 0 && warp == 0) {
       // the new token attends to itself: row group 0 of warp 0 starts from it
       float kf[EPV];
       Vec16<T>::unpack(k4, kf);
+      if constexpr (ROPE) rope_rotate_lane<EPV>(kf, rope_cs);
       float acc = 0.f;
 #pragma unroll
       for (int e = 0; e < EPV; ++e) acc = fmaf(qv[e], kf[e], acc);
@@ -424,6 +456,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
     // prefetch now; triggering only after this step's inputs are loaded keeps
     // those small loads ahead of the next step's bulk traffic.
     griddep_launch();
+    if constexpr (ROPE) consumer_sync(NCW * 32);  // every rank in rk[] is in place
     bool ok = true;
     for (int t = warp; t < ntiles; t += NCW) {
       const int s = t % NSTAGE;
@@ -433,7 +466,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
       }
       const unsigned char* sK = stage_base + static_cast<size_t>(s) * Cfg::STAGE;
       const int rows = ok ? min(TILE, nrows - t * TILE) : 0;
-      attend_tile<T, D, TILE>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lg + t * TILE, lane);
+      attend_tile<T, D, TILE, ROPE>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lg + t * TILE, lane, rk + t * TILE,
+                                    prm.rope);
       // stage s may be refilled; after a timeout the stage is not released,
       // so no new copy can target memory an unfinished copy still writes
       if (lane == 0 && ok) mbar_arrive(&empty_bar[s]);
@@ -564,14 +598,17 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
       bk = blk_key[w];
       bslot = blk_slot[w];
     }
+  // position rolling: the candidate's rank inside the cache travels with it
+  int brank = -1;
+  if constexpr (ROPE) brank = bslot >= 0 ? rk[bslot - lo] : -1;
 
-  int u;
+  int u, urank = brank;
   if (clustered) {
     // every thread holds this CTA's candidate (bk, bslot): thread r pushes it
     // into peer r's kin[rank]; each CTA waits for its peers' candidates
     if (tid < S && tid != rank) {
       const uint4 v = make_uint4(static_cast<uint32_t>(bk), static_cast<uint32_t>(bk >> 32),
-                                 static_cast<uint32_t>(bslot), 0u);
+                                 static_cast<uint32_t>(bslot), static_cast<uint32_t>(brank));
       st_async_v4(mapa_shared(smem_u32(&kin[rank]), tid), v, mapa_shared(smem_u32(kbar), tid));
     }
     if (!mbar_wait_cluster_bounded(kbar, 0, kWaitLimit) && tid == 0) atomicOr(prm.err, ERR_XCH_TIMEOUT);
@@ -584,6 +621,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
         if (key < best) {
           best = key;
           u = r == rank ? bslot : static_cast<int>(c.z);
+          urank = r == rank ? brank : static_cast<int>(c.w);
         }
       }
     } else {
@@ -597,6 +635,18 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
   // reads another's shared memory, so the CTAs of a cluster leave without a
   // cluster barrier.
 
+  // position rolling: after an eviction the kept tokens ranked above the
+  // victim move down one place and the newcomer takes the last rank, C - 1;
+  // while filling, every rank stays and the newcomer takes rank `count`
+  if constexpr (ROPE) {
+    if (full && u >= 0)
+      for (int j = tid; j < nrows; j += NT) {
+        int r = rk[j];
+        if (r > urank) --r;
+        if (lo + j == u) r = C - 1;
+        prm.rank[slot0 + j] = r;
+      }
+  }
   // the new token into slot u
   if (u >= lo && u < lo + prm.chunk && u >= 0) {
     const size_t us = static_cast<size_t>(pair) * C + u;
@@ -607,6 +657,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
     if (tid == 0) {
       prm.pos[us] = p;
       prm.score[us] = p_self;
+      if constexpr (ROPE) {
+        if (!full) prm.rank[us] = count;
+      }
     }
   }
   if (rank == 0 && tid == 0) {
@@ -906,12 +959,12 @@ struct WarpKern {
   }
 };
 
-template <typename T, int D, int NCW>
+template <typename T, int D, int NCW, bool ROPE>
 struct Kern {
   static constexpr int TILE = 16;
   using Cfg = DecodeCfg<T, D, NCW, TILE>;
-  using Lay = Layout<D, NCW, TILE, Cfg::STAGE>;
-  static constexpr auto fn = decode_kernel<T, D, NCW, TILE>;
+  using Lay = Layout<D, NCW, TILE, Cfg::STAGE, ROPE>;
+  static constexpr auto fn = decode_kernel<T, D, NCW, TILE, ROPE>;
 
   static size_t smem(int nstage, int chunk, int splits) { return Lay::bytes(nstage, chunk, splits); }
 
@@ -974,18 +1027,19 @@ int chunk_for(int C, int splits) {
   return (ch + 3) / 4 * 4;
 }
 
-template <int NCW, typename F>
-auto dispatch_ncw(int dtype, int D, F&& f) -> decltype(f(Kern<__half, 128, NCW>{})) {
-  if (dtype == 0 && D == 128) return f(Kern<__half, 128, NCW>{});
-  if (dtype == 0 && D == 64) return f(Kern<__half, 64, NCW>{});
-  if (dtype == 1 && D == 128) return f(Kern<float, 128, NCW>{});
-  return f(Kern<float, 64, NCW>{});
+template <int NCW, bool ROPE, typename F>
+auto dispatch_ncw(int dtype, int D, F&& f) -> decltype(f(Kern<__half, 128, NCW, ROPE>{})) {
+  if (dtype == 0 && D == 128) return f(Kern<__half, 128, NCW, ROPE>{});
+  if (dtype == 0 && D == 64) return f(Kern<__half, 64, NCW, ROPE>{});
+  if (dtype == 1 && D == 128) return f(Kern<float, 128, NCW, ROPE>{});
+  return f(Kern<float, 64, NCW, ROPE>{});
 }
-// the kernel instance for a dtype, head width and cluster size
+// the kernel instance for a dtype, head width, cluster size and position rolling
 template <typename F>
-auto dispatch(int dtype, int D, int splits, F&& f) -> decltype(f(Kern<__half, 128, 4>{})) {
-  if (consumer_warps(splits) == 4) return dispatch_ncw<4>(dtype, D, f);
-  return dispatch_ncw<6>(dtype, D, f);
+auto dispatch(int dtype, int D, int splits, bool rope, F&& f) -> decltype(f(Kern<__half, 128, 4, false>{})) {
+  if (consumer_warps(splits) == 4)
+    return rope ? dispatch_ncw<4, true>(dtype, D, f) : dispatch_ncw<4, false>(dtype, D, f);
+  return rope ? dispatch_ncw<6, true>(dtype, D, f) : dispatch_ncw<6, false>(dtype, D, f);
 }
 
 }  // namespace
@@ -1007,10 +1061,10 @@ int device_sms() {
   return sms;
 }
 
-int decode_resident(int dtype, int D, int splits, int nstage, int chunk, int pairs) {
+int decode_resident(int dtype, int D, int splits, int nstage, int chunk, int pairs, bool rope) {
   const int sms = device_sms();
   const int r =
-      dispatch(dtype, D, splits, [&](auto k) { return decltype(k)::resident(splits, nstage, chunk, pairs, sms); });
+      dispatch(dtype, D, splits, rope, [&](auto k) { return decltype(k)::resident(splits, nstage, chunk, pairs, sms); });
   cudaGetLastError();
   return r;
 }
@@ -1035,9 +1089,10 @@ int decode_warp_default_stages(int dtype, int D, int C, int pairs) {
   return 2;
 }
 
-DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C) {
+DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C, bool rope) {
   const int sms = device_sms();
-  if (sms > 0 && C <= kWarpMaxSlots && pairs >= 4 * sms && decode_warp_resident(dtype, D, 2, C) > 0) {
+  // position rolling runs on the cluster kernel only
+  if (!rope && sms > 0 && C <= kWarpMaxSlots && pairs >= 4 * sms && decode_warp_resident(dtype, D, 2, C) > 0) {
     DecodeShape w;
     w.splits = kDecodeWarpPerPair;
     w.stages = decode_warp_default_stages(dtype, D, C, pairs);
@@ -1061,7 +1116,7 @@ DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C) {
   if (ctas <= 2LL * sms) {
     const int ch = chunk_for(C, sh.splits);
     for (int st : {12, ncw == 6 ? 6 : 8}) {
-      const int res = decode_resident(dtype, D, sh.splits, st, ch, pairs);
+      const int res = decode_resident(dtype, D, sh.splits, st, ch, pairs, rope);
       if (res >= 2 * sms || static_cast<long long>(res) >= ctas) {
         sh.stages = st;
         break;
@@ -1116,6 +1171,7 @@ int warp_grid(int dtype, int D, int nstage, int C, int pairs) {
 cudaError_t launch_decode(const DecodeParams& prm, int dtype, int D, int pairs, int splits, cudaStream_t s) {
   if ((dtype != 0 && dtype != 1) || (D != 64 && D != 128)) return cudaErrorInvalidValue;
   if (splits == kDecodeWarpPerPair) {
+    if (prm.rope != nullptr) return cudaErrorInvalidValue;  // position rolling: cluster kernel only
     if (prm.C > kWarpMaxSlots || prm.nstage < 2 || prm.nstage > kWarpMaxStages) return cudaErrorInvalidValue;
     const int ctas = warp_grid(dtype, D, prm.nstage, prm.C, pairs);
     if (ctas <= 0) return cudaErrorInvalidConfiguration;
@@ -1124,7 +1180,9 @@ cudaError_t launch_decode(const DecodeParams& prm, int dtype, int D, int pairs, 
     if (dtype == 1 && D == 128) return WarpKern<float, 128>::launch(prm, ctas, s);
     return WarpKern<float, 64>::launch(prm, ctas, s);
   }
-  return dispatch(dtype, D, splits, [&](auto k) { return decltype(k)::launch(prm, pairs, splits, s); });
+  if (prm.rope != nullptr && prm.rank == nullptr) return cudaErrorInvalidValue;
+  return dispatch(dtype, D, splits, prm.rope != nullptr,
+                  [&](auto k) { return decltype(k)::launch(prm, pairs, splits, s); });
 }
 
 int decode_threads(int splits) { return (consumer_warps(splits) + 1) * 32; }

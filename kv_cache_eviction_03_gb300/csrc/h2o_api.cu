@@ -2,7 +2,9 @@
 // stream-ordered launches of the decode / prefill kernels.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
+#include <cmath>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -10,12 +12,30 @@
 #include <cstdio>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "h2o.h"
 #include "h2o_internal.cuh"
 #include "ptx.cuh"
 
 namespace {
+// Position rolling: the rank of every kept slot among its pair's kept tokens
+// in text order (-1 for an empty slot).  pos: [P, C] host array.
+void ranks_from_positions(const int* pos, int P, int C, std::vector<int>& out) {
+  out.assign(static_cast<size_t>(P) * C, -1);
+  std::vector<std::pair<int, int>> kept;
+  kept.reserve(C);
+  for (int i = 0; i < P; ++i) {
+    kept.clear();
+    for (int j = 0; j < C; ++j) {
+      const int x = pos[static_cast<size_t>(i) * C + j];
+      if (x >= 0) kept.emplace_back(x, j);
+    }
+    std::sort(kept.begin(), kept.end());
+    for (size_t r = 0; r < kept.size(); ++r) out[static_cast<size_t>(i) * C + kept[r].second] = static_cast<int>(r);
+  }
+}
+
 
 thread_local char g_msg[512] = "";
 
@@ -200,6 +220,8 @@ void h2o_cache_destroy(h2o_cache* c) {
   cudaFree(c->err);
   cudaFree(c->ws);
   cudaFree(c->wsp);
+  cudaFree(c->rank);
+  cudaFree(c->rope);
   delete c;
 }
 
@@ -220,6 +242,9 @@ static int prefill_impl(h2o_cache* c, const void* q, const void* k, const void* 
   if (!c) return fail(H2O_EINVAL, "h2o_prefill: cache is NULL");
   if (prompt_len < 0) return fail(H2O_EINVAL, "h2o_prefill: prompt_len must be >= 0");
   if (prompt_len == 0) return h2o_cache_reset(c, stream);
+  if (c->rope)
+    return fail(H2O_ESTATE, "h2o_prefill: position rolling is on and the prefill applies no rotary embedding "
+                            "(decode from an empty cache instead)");
   if (!q || !k || !v) return fail(H2O_EINVAL, "h2o_prefill: q, k and v are required");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (out_or_null && !aligned16(out_or_null)))
     return fail(H2O_EINVAL, "h2o_prefill: device pointers must be 16-byte aligned");
@@ -346,6 +371,8 @@ int h2o_decode_step(h2o_cache* c, const void* q, const void* k_new, const void* 
   dp.qscale = scale * 1.4426950408889634f;
   dp.prefetch = touch_stream(c, stream) ? 1 : 0;
   dp.pairs = c->P;
+  dp.rank = c->rank;
+  dp.rope = c->rope;
   cudaError_t e = h2o::launch_decode(dp, c->dtype, c->D, c->P, splits, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "h2o_decode_step: launch");
   c->host_next_p += 1;
@@ -428,6 +455,14 @@ int h2o_cache_import_state(h2o_cache* c, const void* host_buf, size_t bytes, voi
       return cuda_fail(e, "h2o_cache_import_state: copy");
     p += part.n;
   }
+  std::vector<int> ranks;  // position rolling: ranks follow from the imported positions
+  if (c->rope) {
+    const int* pos = reinterpret_cast<const int*>(static_cast<const unsigned char*>(host_buf) +
+                                                  kHeaderInts * sizeof(int) + 2 * kv_bytes(c) + nslot * 4);
+    ranks_from_positions(pos, c->P, c->C, ranks);
+    if ((e = cudaMemcpyAsync(c->rank, ranks.data(), nslot * sizeof(int), cudaMemcpyHostToDevice, s)) != cudaSuccess)
+      return cuda_fail(e, "h2o_cache_import_state: ranks");
+  }
   if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "h2o_cache_import_state: sync");
   c->host_next_p = maxp;
   return H2O_OK;
@@ -469,6 +504,8 @@ int h2o_cache_set_decode_shape(h2o_cache* c, int splits, int stages) {
                                       : h2o::decode_stage_multiple(s);
   }
   if (s == h2o::kDecodeWarpPerPair) {
+    if (c->rope)
+      return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: position rolling runs on the cluster kernel only");
     if (c->C > h2o::decode_warp_max_slots())
       return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: warp per pair takes at most %d slots per pair",
                   h2o::decode_warp_max_slots());
@@ -484,7 +521,7 @@ int h2o_cache_set_decode_shape(h2o_cache* c, int splits, int stages) {
     if (chunk_for(c->C, s) > h2o::decode_max_chunk())
       return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: %d splits leave more than %d slots per CTA", s,
                   h2o::decode_max_chunk());
-    if (h2o::decode_resident(c->dtype, c->D, s, n, chunk_for(c->C, s), c->P) < s)
+    if (h2o::decode_resident(c->dtype, c->D, s, n, chunk_for(c->C, s), c->P, c->rope != nullptr) < s)
       return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: %d CTAs per pair with %d stages cannot be scheduled", s,
                   n);
   }
@@ -505,6 +542,51 @@ int h2o_cache_info(const h2o_cache* c, int32_t* info) {
   info[7] = stages_in_use(c);
   info[8] = splits_in_use(c) == h2o::kDecodeWarpPerPair ? 128 : h2o::decode_threads(splits_in_use(c));
   info[9] = 0;
+  return H2O_OK;
+}
+
+int h2o_cache_set_position_rolling(h2o_cache* c, float rope_base) {
+  if (!c) return fail(H2O_EINVAL, "h2o_cache_set_position_rolling: cache is NULL");
+  if (!(rope_base >= 0.f) || !std::isfinite(rope_base))
+    return fail(H2O_EINVAL, "h2o_cache_set_position_rolling: rope_base must be finite and >= 0 (0 = off)");
+  cudaError_t e = cudaDeviceSynchronize();  // the positions are read back below
+  if (e != cudaSuccess) return cuda_fail(e, "h2o_cache_set_position_rolling: synchronise");
+  if (rope_base == 0.f) {
+    cudaFree(c->rank);
+    cudaFree(c->rope);
+    c->rank = nullptr;
+    c->rope = nullptr;
+    c->rope_base = 0.f;
+    c->shape_auto = h2o::decode_pick_shape(c->dtype, c->D, c->P, c->C, false);
+    return H2O_OK;
+  }
+  const size_t nslot = static_cast<size_t>(c->P) * c->C;
+  const size_t ntab = static_cast<size_t>(c->C + 1) * (c->D / 2);
+  if (!c->rank && (e = cudaMalloc(&c->rank, nslot * sizeof(int))) != cudaSuccess)
+    return cuda_fail(e, "h2o_cache_set_position_rolling: cudaMalloc");
+  if (!c->rope && (e = cudaMalloc(&c->rope, ntab * sizeof(float2))) != cudaSuccess)
+    return cuda_fail(e, "h2o_cache_set_position_rolling: cudaMalloc");
+  // (cos, sin) of rank * base^(-2i/D) for ranks 0..C, in double, stored as float
+  std::vector<float2> tab(ntab);
+  for (int r = 0; r <= c->C; ++r)
+    for (int i = 0; i < c->D / 2; ++i) {
+      const double ang = r * std::pow(static_cast<double>(rope_base), -2.0 * i / c->D);
+      tab[static_cast<size_t>(r) * (c->D / 2) + i] = make_float2(static_cast<float>(std::cos(ang)),
+                                                                 static_cast<float>(std::sin(ang)));
+    }
+  std::vector<int> pos(nslot), ranks;
+  if ((e = cudaMemcpy(pos.data(), c->pos, nslot * sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "h2o_cache_set_position_rolling: read positions");
+  ranks_from_positions(pos.data(), c->P, c->C, ranks);
+  if ((e = cudaMemcpy(c->rope, tab.data(), ntab * sizeof(float2), cudaMemcpyHostToDevice)) != cudaSuccess ||
+      (e = cudaMemcpy(c->rank, ranks.data(), nslot * sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess)
+    return cuda_fail(e, "h2o_cache_set_position_rolling: upload");
+  c->rope_base = rope_base;
+  // the cluster kernel with one more int of shared memory per slot; a
+  // warp-per-pair or explicit shape goes back to the automatic one
+  c->shape_auto = h2o::decode_pick_shape(c->dtype, c->D, c->P, c->C, true);
+  c->splits_override = 0;
+  c->stages_override = 0;
   return H2O_OK;
 }
 

@@ -47,6 +47,11 @@ struct DecodeParams {
                       // this cache, so its slot store may be read before the
                       // grid-dependency wait
   int pairs;          // P
+  // position rolling (rotary embedding at positions inside the cache), or
+  // both nullptr: the rank of each slot among the kept tokens in text order,
+  // and cos / sin of rank * base^(-2i/D) for ranks 0..C and pairs i < D/2
+  int* rank;           // [P, C]
+  const float2* rope;  // [C + 1, D / 2]
 };
 
 struct PrefillParams {
@@ -115,9 +120,11 @@ struct DecodeShape {
   int splits;  // CTAs (one cluster) per pair, or kDecodeWarpPerPair
   int stages;  // shared-memory ring depth per CTA (per warp in warp-per-pair mode)
 };
-DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C);
+// rope: the cache uses position rolling (cluster kernel only, one more int
+// of shared memory per slot)
+DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C, bool rope = false);
 // CTAs of this shape that fit on the device at once (0: cannot launch)
-int decode_resident(int dtype, int D, int splits, int nstage, int chunk, int pairs);
+int decode_resident(int dtype, int D, int splits, int nstage, int chunk, int pairs, bool rope = false);
 int decode_chunk(int C, int splits);
 int decode_max_stages();
 int decode_stage_multiple(int splits);  // ring depths for this cluster size must be multiples of this
@@ -165,4 +172,9 @@ struct h2o_cache {
   int splits_override, stages_override;
   h2o::DecodeShape shape_auto;
   long long host_next_p;  // host mirror of the next position (overflow check)
+  // position rolling: slot ranks [P, C] and the (cos, sin) table [C + 1, D/2];
+  // nullptr when off
+  int* rank;
+  float2* rope;
+  float rope_base;
 };
