@@ -28,6 +28,11 @@ order the method states it.  Sources (page title, then section):
   rotary position embedding applied with positions counted inside the cache
   rather than in the text (rope_rotate, cache_ranks, decode_step_pair with
   rope_base).
+* same page, section 4.5 (Table 2: Sparse Transformer strided / fixed
+  patterns combined with heavy hitters): positions chosen by a fixed pattern
+  are kept for good, the heavy hitters fill the rest of the heavy budget
+  (StaticPattern, the `pattern` argument of select_prefill, prefill_pair and
+  decode_step_pair).
 
 Readings taken where the pages are loose (each also listed in the design
 notes): the score is the column sum of attention probabilities (the report's
@@ -80,7 +85,42 @@ def causal_attention_stats(q, k, v, scale):
     return lse, colsum, out
 
 
-def select_prefill(colsum, L, heavy, recent):
+# --------------------------------------------------------------------------- static pattern
+@dataclass(frozen=True)
+class StaticPattern:
+    """Positions a fixed sparse pattern keeps for good (section 4.5, Table 2:
+    Sparse Transformer strided / fixed patterns plus heavy hitters).
+
+    Reading (the pages give the combination's accuracy only, not how the two
+    share a budget): the protected positions are offset, offset + stride, ...,
+    offset + (count - 1) * stride.  They occupy heavy-budget slots (count <=
+    heavy) and are never eviction candidates; the heavy hitters take the
+    remaining heavy slots.  offset 0 gives the strided lattice, offset
+    stride - 1 the fixed pattern's block-summary positions (the last position
+    of each block of `stride`), stride 1 the first `count` tokens.
+    """
+
+    offset: int
+    stride: int
+    count: int
+
+    def __post_init__(self):
+        if self.offset < 0 or self.stride < 1 or self.count < 0:
+            raise ValueError("static pattern needs offset >= 0, stride >= 1, count >= 0")
+
+    def protects(self, pos):
+        """Boolean array: which of the positions `pos` are protected."""
+        pos = np.asarray(pos, dtype=np.int64)
+        d = pos - self.offset
+        return (self.count > 0) & (d >= 0) & (d % self.stride == 0) & (d // self.stride < self.count)
+
+
+def _protected(pattern, pos):
+    pos = np.asarray(pos, dtype=np.int64)
+    return np.zeros(pos.shape, dtype=bool) if pattern is None else pattern.protects(pos)
+
+
+def select_prefill(colsum, L, heavy, recent, pattern=None):
     """Positions kept after a prompt of length L, in slot order (section 3.4).
 
     L <= heavy + recent: every position, slot j holds position j.
@@ -88,14 +128,20 @@ def select_prefill(colsum, L, heavy, recent):
     are the `heavy` largest keys (score, position) among positions < L-recent,
     where score is colsum as stored in the float32 buffer.  Slots 0..heavy-1
     hold the heavy hitters in ascending position, then the recent window.
+    With a static pattern (section 4.5) its positions below L-recent are kept
+    first and the heavy hitters fill the remaining heavy slots.
     """
     C = heavy + recent
     if L <= C:
         return list(range(L))
     n = L - recent
     score = to_f32(colsum[:n])
-    ascending = np.lexsort((np.arange(n), score))  # by score, then position
-    heavy_pos = sorted(ascending[n - heavy:].tolist()) if heavy else []
+    prot = _protected(pattern, np.arange(n))
+    free = np.nonzero(~prot)[0]
+    take = heavy - int(prot.sum())
+    assert take >= 0, "a static pattern holds at most `heavy` positions"
+    ascending = free[np.lexsort((free, score[free]))]  # by score, then position
+    heavy_pos = sorted(np.nonzero(prot)[0].tolist() + (ascending[free.size - take:].tolist() if take else []))
     return heavy_pos + list(range(n, L))
 
 
@@ -122,7 +168,7 @@ def empty_pair(C, R, D) -> PairState:
                      np.full(C, -1, dtype=np.int64), np.full(R, -1, dtype=np.int64), 0, 0, 0)
 
 
-def prefill_pair(q, k, v, heavy, recent, scale):
+def prefill_pair(q, k, v, heavy, recent, scale, pattern=None):
     """Prefill one pair: attention stats, keep rule, cache laid out in slots."""
     L, D = k.shape
     C = heavy + recent
@@ -130,7 +176,7 @@ def prefill_pair(q, k, v, heavy, recent, scale):
     if L == 0:
         return st, np.zeros((0,)), np.zeros((0, D))
     lse, colsum, out = causal_attention_stats(q, k, v, scale)
-    keep = select_prefill(colsum, L, heavy, recent)
+    keep = select_prefill(colsum, L, heavy, recent, pattern)
     n = len(keep)
     st.K[:n] = k[keep]
     st.V[:n] = v[keep]
@@ -221,13 +267,15 @@ class StepResult:
     prob: np.ndarray  # [count + 1] probabilities (kept slots, then self)
 
 
-def decode_step_pair(st: PairState, q, k_new, v_new, scale, heavy, recent, rope_base=None) -> StepResult:
+def decode_step_pair(st: PairState, q, k_new, v_new, scale, heavy, recent, rope_base=None,
+                     pattern=None) -> StepResult:
     """One decode step of one pair, in place on `st` (sections 3.1, 3.3, 3.4).
 
     With rope_base (position rolling, section 4.4) the logits are taken
     between rotary-embedded vectors, each kept key at its rank inside the
     cache (cache_ranks) and the query and the new key at n, the number of
     kept tokens; the cache stores the keys as given (not rotated).
+    With a static pattern (section 4.5) its positions are never candidates.
 
     1. attend over the kept slots and the new token itself; the softmax
        normaliser covers only those entries;
@@ -264,7 +312,7 @@ def decode_step_pair(st: PairState, q, k_new, v_new, scale, heavy, recent, rope_
         evicted = -1
         st.count = n + 1
     else:
-        cand = np.nonzero(st.pos[:C] <= p - recent)[0]
+        cand = np.nonzero((st.pos[:C] <= p - recent) & ~_protected(pattern, st.pos[:C]))[0]
         ranked = cand[np.lexsort((st.pos[cand], st.score[cand]))]  # by score, then position
         u = int(ranked[0])
         evicted = u
@@ -322,29 +370,30 @@ def empty_cache(pairs, heavy, recent, head_dim) -> CacheState:
     return CacheState.stack([empty_pair(heavy + recent, recent, head_dim) for _ in range(pairs)])
 
 
-def prefill(q, k, v, heavy, recent, scale):
+def prefill(q, k, v, heavy, recent, scale, pattern=None):
     """Prefill every pair.  q, k, v: [B, H, L, D].  Returns (state, colsum, O)."""
     q, k, v = _pairs(q), _pairs(k), _pairs(v)
     states, colsums, outs = [], [], []
     for i in range(q.shape[0]):
-        st, cs, o = prefill_pair(q[i], k[i], v[i], heavy, recent, scale)
+        st, cs, o = prefill_pair(q[i], k[i], v[i], heavy, recent, scale, pattern)
         states.append(st)
         colsums.append(cs)
         outs.append(o)
     return CacheState.stack(states), np.stack(colsums), np.stack(outs)
 
 
-def decode_step(state: CacheState, q, k_new, v_new, heavy, recent, scale, rope_base=None):
+def decode_step(state: CacheState, q, k_new, v_new, heavy, recent, scale, rope_base=None, pattern=None):
     """One decode step for every pair.  q, k_new, v_new: [B, H, D].
 
     Returns (new_state, out [P, D], evicted [P], gap [P]); `state` is untouched.
     rope_base: position rolling (see decode_step_pair), None for none.
+    pattern: a StaticPattern (see decode_step_pair), None for none.
     """
     q, k_new, v_new = _pairs(q), _pairs(k_new), _pairs(v_new)
     new_pairs, outs, ev, gaps = [], [], [], []
     for i in range(q.shape[0]):
         st = state.pair(i)
-        r = decode_step_pair(st, q[i], k_new[i], v_new[i], scale, heavy, recent, rope_base)
+        r = decode_step_pair(st, q[i], k_new[i], v_new[i], scale, heavy, recent, rope_base, pattern)
         new_pairs.append(st)
         outs.append(r.out)
         ev.append(r.evicted)

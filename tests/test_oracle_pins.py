@@ -27,13 +27,13 @@ def rand_seq(rng, L, D, key_mean=None):
     return q, k, v
 
 
-def run_pair(q_all, k_all, v_all, L, heavy, recent, scale):
+def run_pair(q_all, k_all, v_all, L, heavy, recent, scale, rope_base=None, pattern=None):
     """Prefill positions < L, then decode the rest; returns per-step results."""
-    st, colsum, out_prefill = O.prefill_pair(q_all[:L], k_all[:L], v_all[:L], heavy, recent, scale)
+    st, colsum, out_prefill = O.prefill_pair(q_all[:L], k_all[:L], v_all[:L], heavy, recent, scale, pattern)
     steps = []
     for p in range(L, q_all.shape[0]):
         before = st.copy()
-        r = O.decode_step_pair(st, q_all[p], k_all[p], v_all[p], scale, heavy, recent)
+        r = O.decode_step_pair(st, q_all[p], k_all[p], v_all[p], scale, heavy, recent, rope_base, pattern)
         steps.append((before, r, st.copy()))
     return st, colsum, out_prefill, steps
 
@@ -42,6 +42,26 @@ def sdpa_causal(q, k, v, scale):
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a))[None, None]
     o = torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v), is_causal=True, scale=scale)
     return o[0, 0].numpy()
+
+
+def sdpa_masked(q, k, v, scale, allowed):
+    """torch fp64 attention where query row i sees key j only if allowed[i, j]."""
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))[None, None]
+    mask = torch.from_numpy(np.ascontiguousarray(allowed))[None, None]
+    o = torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v), attn_mask=mask, scale=scale)
+    return o[0, 0].numpy()
+
+
+def rotary_at(x, positions, base):
+    """Rotary embedding computed as complex rotations in torch (independent of
+    the oracle's rope_rotate): pair (2i, 2i+1) as one complex number, times
+    exp(i * position * base^(-2i/D))."""
+    n, D = x.shape
+    xc = torch.from_numpy(x[:, 0::2] + 1j * x[:, 1::2])
+    theta = base ** (-2.0 * torch.arange(D // 2, dtype=torch.float64) / D)
+    ang = torch.as_tensor(positions, dtype=torch.float64)[:, None] * theta[None, :]
+    r = xc * torch.exp(1j * ang)
+    return torch.stack([r.real, r.imag], dim=-1).reshape(n, D).numpy()
 
 
 # ------------------------------------------------------------------ library routine
@@ -190,19 +210,34 @@ def test_score_mass_conservation():
 
 
 # ------------------------------------------------------------------ brute force
-def brute_force_run(q, k, v, L, heavy, recent, scale):
+def brute_force_run(q, k, v, L, heavy, recent, scale, protected=frozenset(), rope_base=None):
     """Independent restatement on position sets with pure-Python arithmetic.
 
     Prefill: colsum by explicit double sums; the heavy set is found by evicting
     the lowest (score, position) candidate one at a time.  Decode: Algorithm 1
     taken literally, u = argmax_v F(S + {p} - {v}) with F the sum of scores,
     enumerated over every candidate v outside the recent window (ties: lowest
-    position evicted).
+    position evicted).  `protected`: positions of a static pattern, never
+    candidates (kept first at prefill).  `rope_base`: position rolling, every
+    key rotated by its rank in the cache (counted here as the number of kept
+    positions below it) and the query by the number of kept tokens, element
+    pair (2i, 2i+1) by the angle rank * base^(-2i/D).
     """
     C = heavy + recent
     D = len(q[0])
     f32 = lambda x: float(np.float32(x))
     dot = lambda a, b: sum(a[d] * b[d] for d in range(D))
+
+    def rot(x, r):
+        if rope_base is None:
+            return x
+        y = list(x)
+        for i in range(D // 2):
+            a = r * rope_base ** (-2.0 * i / D)
+            y[2 * i] = x[2 * i] * math.cos(a) - x[2 * i + 1] * math.sin(a)
+            y[2 * i + 1] = x[2 * i] * math.sin(a) + x[2 * i + 1] * math.cos(a)
+        return y
+
     score = {}
     if L:
         colsum = [0.0] * L
@@ -217,13 +252,15 @@ def brute_force_run(q, k, v, L, heavy, recent, scale):
         else:
             cand = set(range(L - recent))
             while len(cand) > heavy:
-                cand.remove(min(cand, key=lambda j: (f32(colsum[j]), j)))
+                cand.remove(min(cand - set(protected), key=lambda j: (f32(colsum[j]), j)))
             kept = cand | set(range(L - recent, L))
         score = {j: f32(colsum[j]) for j in kept}
     outs, kept_sets, evictions = [], [], []
     for p in range(L, len(q)):
         S = sorted(score) + [p]
-        s = [scale * dot(q[p], k[j]) for j in S]
+        n = len(S) - 1
+        qr = rot(q[p], n)
+        s = [scale * dot(qr, rot(k[j], sum(1 for i in S[:-1] if i < j) if j != p else n)) for j in S]
         mx = max(s)
         z = sum(math.exp(x - mx) for x in s)
         pr = [math.exp(x - mx) / z for x in s]
@@ -232,7 +269,7 @@ def brute_force_run(q, k, v, L, heavy, recent, scale):
             score[j] = f32(score[j] + pr[a])
         ev = None
         if len(S) - 1 == C:
-            cand = [j for j in S[:-1] if j <= p - recent]
+            cand = [j for j in S[:-1] if j <= p - recent and j not in protected]
             total = sum(score.values())
             best = max(total - score[j] for j in cand)
             ev = min(j for j in cand if total - score[j] == best)
@@ -443,11 +480,149 @@ def test_rolling_without_eviction_is_rotary_attention():
     st = O.empty_pair(heavy + recent, recent, D)
     outs = [O.decode_step_pair(st, q[t], k[t], v[t], 0.7, heavy, recent, rope_base=base).out for t in range(T)]
 
-    def rotate(x):
-        xc = torch.from_numpy(x[:, 0::2] + 1j * x[:, 1::2])
-        ang = torch.arange(T, dtype=torch.float64)[:, None] * base ** (-2.0 * torch.arange(D // 2) / D)[None, :]
-        r = xc * torch.exp(1j * ang)
-        return torch.stack([r.real, r.imag], dim=-1).reshape(T, D).numpy()
-
-    ref = sdpa_causal(rotate(q), rotate(k), v, 0.7)
+    ref = sdpa_causal(rotary_at(q, np.arange(T), base), rotary_at(k, np.arange(T), base), v, 0.7)
     np.testing.assert_allclose(np.stack(outs), ref, atol=1e-12)
+
+
+@pytest.mark.parametrize("recent", [1, 5, 9])
+def test_rolling_without_heavy_is_rotary_sliding_window(recent):
+    """heavy = 0 with rolling on: past the fill the cache holds exactly the
+    window p-recent..p-1 at ranks 0..recent-1 and the query sits at rank
+    `recent`.  Rotary logits depend only on rank differences, which then equal
+    text-position differences, so every step must be sliding-window attention
+    over q and k rotated at their text positions (torch fp64, masked).  A
+    query placed at its text position p, or keys at theirs, fails this once
+    p > recent."""
+    T, D, base = 40, 8, 50.0
+    rng = np.random.default_rng(12)
+    q, k, v = rng.standard_normal((3, T, D))
+    st = O.empty_pair(recent, recent, D)
+    outs = [O.decode_step_pair(st, q[t], k[t], v[t], 0.8, 0, recent, rope_base=base).out for t in range(T)]
+    i, j = np.arange(T)[:, None], np.arange(T)[None, :]
+    allowed = (j <= i) & (j >= i - recent)
+    ref = sdpa_masked(rotary_at(q, np.arange(T), base), rotary_at(k, np.arange(T), base), v, 0.8, allowed)
+    np.testing.assert_allclose(np.stack(outs), ref, atol=1e-12)
+
+
+@pytest.mark.parametrize("seed", range(5))
+@pytest.mark.parametrize("heavy,recent", [(3, 2), (4, 1), (2, 4)])
+def test_rolling_after_evictions_brute_force(seed, heavy, recent):
+    """heavy > 0 with rolling on, far past the fill (ranks and positions
+    differ): outputs, kept sets and victims against the position-set brute
+    force, which ranks every kept key by counting the kept positions below it
+    and rotates with its own cos / sin loops."""
+    rng = np.random.default_rng(300 + seed)
+    T, D, base = 45, 4, 30.0
+    q, k, v = rand_seq(rng, T, D, key_mean=rng.standard_normal(D))
+    k[rng.integers(0, T, 5)] = k[1]
+    _, _, _, steps = run_pair(q, k, v, 0, heavy, recent, 0.9, rope_base=base)
+    outs, kept_sets, evictions = brute_force_run(q.tolist(), k.tolist(), v.tolist(), 0, heavy, recent, 0.9,
+                                                 rope_base=base)
+    moved = 0
+    for t, (before, r, after) in enumerate(steps):
+        assert set(after.pos[after.pos >= 0].tolist()) == kept_sets[t]
+        ev_pos = None if r.evicted < 0 else int(before.pos[r.evicted])
+        assert ev_pos == evictions[t]
+        np.testing.assert_allclose(r.out, outs[t], atol=1e-12)
+        moved += int(before.count < t)  # the query's rank n differs from its position t
+    assert moved > 20
+
+
+# ------------------------------------------------------------------ static pattern + heavy hitters
+def test_static_pattern_positions():
+    """Closed form of the three pattern families."""
+    pos = np.arange(40)
+    strided = O.StaticPattern(0, 4, 5)
+    assert np.nonzero(strided.protects(pos))[0].tolist() == [0, 4, 8, 12, 16]
+    fixed = O.StaticPattern(7, 8, 3)  # last position of each block of 8
+    assert np.nonzero(fixed.protects(pos))[0].tolist() == [7, 15, 23]
+    first = O.StaticPattern(0, 1, 4)
+    assert np.nonzero(first.protects(pos))[0].tolist() == [0, 1, 2, 3]
+    assert not O.StaticPattern(3, 2, 0).protects(pos).any()
+    assert not strided.protects([-1]).any()
+    with pytest.raises(ValueError):
+        O.StaticPattern(0, 0, 3)
+
+
+@pytest.mark.parametrize("pattern,L,recent", [((0, 5, 6), 40, 6), ((4, 5, 4), 33, 4), ((0, 1, 3), 20, 2)])
+def test_static_pattern_filling_the_heavy_budget_is_sparse_attention(pattern, L, recent):
+    """heavy == count with every pattern position inside the prompt's
+    candidate region: the heavy budget holds only the pattern, so the cache is
+    exactly the pattern plus the recent window at every step (the Sparse
+    Transformer baseline of section 4.5 without heavy hitters), and each decode
+    output equals torch fp64 attention over that key set plus the token
+    itself."""
+    sp = O.StaticPattern(*pattern)
+    heavy = sp.count
+    T, D = 30, 6
+    rng = np.random.default_rng(21)
+    q, k, v = rand_seq(rng, L + T, D, key_mean=rng.standard_normal(D))
+    lattice = set(np.nonzero(sp.protects(np.arange(L + T)))[0].tolist())
+    assert max(lattice) < L - recent
+    st, _, _, steps = run_pair(q, k, v, L, heavy, recent, 0.7, pattern=sp)
+    i, j = np.arange(L + T)[:, None], np.arange(L + T)[None, :]
+    allowed = (j <= i) & ((j >= i - recent) | sp.protects(np.arange(L + T))[None, :])
+    ref = sdpa_masked(q, k, v, 0.7, allowed)
+    for t, (before, r, after) in enumerate(steps):
+        p = L + t
+        assert set(before.pos[before.pos >= 0].tolist()) == lattice | set(range(p - recent, p))
+        np.testing.assert_allclose(r.out, ref[p], atol=1e-12)
+
+
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("pattern,L,heavy,recent", [((0, 3, 2), 12, 3, 2), ((2, 3, 3), 9, 4, 2),
+                                                    ((0, 1, 2), 0, 3, 2), ((1, 4, 4), 14, 4, 1)])
+def test_static_pattern_against_position_set_brute_force(seed, pattern, L, heavy, recent):
+    """Static pattern + heavy hitters against the brute force with protected
+    positions (never candidates, kept first at prefill); pattern positions
+    also arrive during decode and become protected once they leave the
+    recent window."""
+    sp = O.StaticPattern(*pattern)
+    rng = np.random.default_rng(200 + seed)
+    T, D = 40, 3
+    q, k, v = rand_seq(rng, L + T, D, key_mean=rng.standard_normal(D))
+    k[rng.integers(0, L + T, 6)] = k[0]
+    _, _, _, steps = run_pair(q, k, v, L, heavy, recent, 0.9, pattern=sp)
+    prot = frozenset(np.nonzero(sp.protects(np.arange(L + T)))[0].tolist())
+    outs, kept_sets, evictions = brute_force_run(q.tolist(), k.tolist(), v.tolist(), L, heavy, recent, 0.9,
+                                                 protected=prot)
+    for t, (before, r, after) in enumerate(steps):
+        assert set(after.pos[after.pos >= 0].tolist()) == kept_sets[t]
+        assert prot & set(range(L + t + 1)) <= kept_sets[t]  # a pattern position is never evicted
+        ev_pos = None if r.evicted < 0 else int(before.pos[r.evicted])
+        assert ev_pos == evictions[t]
+        np.testing.assert_allclose(r.out, outs[t], atol=1e-12)
+
+
+def test_static_pattern_prefill_selection_brute_force():
+    """Pattern positions below L-recent are all kept; the rest of the heavy
+    budget goes to the top keys (score, position) of the other positions,
+    which also equals iterated lowest-key evictions among non-pattern ones."""
+    rng = np.random.default_rng(18)
+    for trial in range(30):
+        L = int(rng.integers(10, 150))
+        heavy = int(rng.integers(0, 12))
+        recent = int(rng.integers(1, 12))
+        sp = O.StaticPattern(int(rng.integers(0, 6)), int(rng.integers(1, 9)), int(rng.integers(0, heavy + 1)))
+        colsum = rng.integers(0, 5, size=L).astype(np.float64) / 4  # many exact ties
+        keep = O.select_prefill(colsum, L, heavy, recent, sp)
+        if L <= heavy + recent:
+            assert keep == list(range(L))
+            continue
+        n = L - recent
+        prot = set(np.nonzero(sp.protects(np.arange(n)))[0].tolist())
+        cand = list(range(n))
+        while len(cand) > heavy:
+            cand.remove(min((j for j in cand if j not in prot), key=lambda j: (colsum[j], j)))
+        assert keep[:heavy] == cand and prot <= set(cand)
+        assert keep[heavy:] == list(range(n, L))
+
+
+def test_empty_static_pattern_is_plain_h2o():
+    rng = np.random.default_rng(4)
+    L, T, D, heavy, recent = 30, 25, 4, 5, 4
+    q, k, v = rand_seq(rng, L + T, D, key_mean=rng.standard_normal(D))
+    a = run_pair(q, k, v, L, heavy, recent, 0.8)[3]
+    b = run_pair(q, k, v, L, heavy, recent, 0.8, pattern=O.StaticPattern(0, 3, 0))[3]
+    for (_, ra, sa), (_, rb, sb) in zip(a, b):
+        assert ra.evicted == rb.evicted and np.array_equal(ra.out, rb.out) and np.array_equal(sa.pos, sb.pos)
