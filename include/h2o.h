@@ -179,6 +179,22 @@ H2O_API int h2o_cache_set_decode_shape(h2o_cache* cache, int splits, int stages)
  * to automatic).  Returns H2O_EINVAL for a negative or non-finite base. */
 H2O_API int h2o_cache_set_position_rolling(h2o_cache* cache, float rope_base);
 
+/* Static sparse pattern combined with heavy hitters ("... 深度解读报告",
+ * section 4.5, Table 2: Sparse Transformer strided / fixed patterns plus H2).
+ * Positions offset, offset + stride, ..., offset + (count - 1) * stride are
+ * kept for good: h2o_prefill keeps those below L - recent before choosing
+ * heavy hitters, and h2o_decode_step never evicts them (they are not
+ * eviction candidates once outside the recent window).  They occupy
+ * heavy-budget slots, so count <= heavy; the heavy hitters fill the remaining
+ * heavy slots.  offset 0 and stride s give the strided lattice 0, s, 2s, ...;
+ * offset l - 1 and stride l the fixed pattern's block-summary positions (the
+ * last position of each block of l); stride 1 the first `count` tokens.
+ * count = 0 (the default) turns it off.  Host-side and immediate: it applies
+ * to the prefill and decode calls made after it.  It is configuration, not
+ * state: export/import do not carry it.  Returns H2O_EINVAL for offset < 0,
+ * stride < 1, count < 0, count > heavy, or a last position beyond int32. */
+H2O_API int h2o_cache_set_static_pattern(h2o_cache* cache, int offset, int stride, int count);
+
 /* info[0..9] = {batch, heads, head_dim, heavy, recent, kv_dtype,
  *               decode splits in use (-1: warp per pair), decode stages in
  *               use, decode threads per CTA, 0}. */
@@ -188,8 +204,11 @@ H2O_API int h2o_cache_info(const h2o_cache* cache, int32_t* info);
  * no counterpart: this exists for callers that cannot call cudaMalloc, such
  * as engines that hand out all device memory from their own pools and forbid
  * allocation after start-up, or loops that cannot afford the device-wide
- * synchronisation a cudaMalloc implies.  It computes exactly what
- * h2o_prefill_ex returns in colsum_or_null (same kernels, same order):
+ * synchronisation a cudaMalloc implies.  It runs the same kernels as
+ * h2o_prefill_ex without an attention output and returns the same values,
+ * bit for bit, as that call's colsum_or_null (with an attention output,
+ * h2o_prefill_ex takes its column sums from the output pass instead, and
+ * they agree within 1e-5 relative):
  *   colsum[b,h,j] = sum_{i>=j} softmax_i(scale * q_i . k_j)    (causal rows)
  * q, k: [B, H, L, D] device pointers in kv_dtype (16-byte aligned); colsum:
  * [B, H, L] float32 device output.  No cache is involved and nothing is kept.
@@ -202,9 +221,19 @@ H2O_API int h2o_cache_info(const h2o_cache* cache, int32_t* info);
  * kernels overlap on the GPU (different streams, or several host threads)
  * race and corrupt each other's results, so serialise them.  Each call
  * writes every scratch entry it reads, so stale contents from a previous
- * call do no harm.  Asynchronous on `stream`. */
+ * call do no harm, unless one of the call's bounded device waits gave up:
+ * the call then leaves some entries unwritten and latches an error word
+ * (also a fixed library array, cleared with cudaMemsetAsync at the start of
+ * every call) that h2o_prefill_colsum_static_check reports.  Asynchronous
+ * on `stream`. */
 H2O_API int h2o_prefill_colsum_static(const void* q, const void* k, int batch, int heads, int head_dim,
                                       int prompt_len, int kv_dtype, float scale, float* colsum, void* stream);
+
+/* Synchronous.  Wait for `stream`, then report H2O_EDEVICE if the kernels of
+ * the last h2o_prefill_colsum_static call on the current device latched a
+ * device error (its column sums are then not valid), else H2O_OK.  Allocates
+ * nothing.  Call it on the stream of that call, before the next one. */
+H2O_API int h2o_prefill_colsum_static_check(void* stream);
 
 /* Self-test of the bounded waits every kernel of the library uses (they are
  * how a device-side stall becomes an H2O_EDEVICE status instead of a hang).
@@ -217,6 +246,14 @@ H2O_API int h2o_prefill_colsum_static(const void* q, const void* k, int batch, i
  * 1..1000000 (at most about 2 s); other values return H2O_EINVAL.  The device
  * stays usable afterwards: nothing is left waiting. */
 H2O_API int h2o_selftest_wait_timeout(unsigned polls, int* gave_up, unsigned long long* elapsed_ns);
+
+/* Fault injection for tests of the callers' error paths: after `after`
+ * more successful device allocations made by this library (from any
+ * thread), the next one fails as if the device were out of memory (the call
+ * that makes it returns H2O_ENOMEM and frees what it had allocated), and the
+ * hook disarms itself.  after = -1 disarms it.  Host-side only: no kernel
+ * and no device is involved.  Returns H2O_EINVAL for after < -1. */
+H2O_API int h2o_debug_fail_alloc(int after);
 
 /* Thread-local message describing the last error returned on this thread. */
 H2O_API const char* h2o_last_error(void);

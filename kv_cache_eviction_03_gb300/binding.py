@@ -45,8 +45,11 @@ SIGNATURES = {
     "h2o_cache_info": (_c_int, [_c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     "h2o_prefill_colsum_static": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
                                            _c_void_p, _c_void_p]),
+    "h2o_prefill_colsum_static_check": (_c_int, [_c_void_p]),
     "h2o_cache_set_position_rolling": (_c_int, [_c_void_p, _c_float]),
+    "h2o_cache_set_static_pattern": (_c_int, [_c_void_p, _c_int, _c_int, _c_int]),
     "h2o_selftest_wait_timeout": (_c_int, [ctypes.c_uint, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_ulonglong)]),
+    "h2o_debug_fail_alloc": (_c_int, [_c_int]),
     "h2o_last_error": (ctypes.c_char_p, []),
 }
 
@@ -238,6 +241,11 @@ def h2o_cache_set_position_rolling(cache: Cache, rope_base: float):
     _check(lib().h2o_cache_set_position_rolling(cache.handle, float(rope_base)))
 
 
+def h2o_cache_set_static_pattern(cache: Cache, offset: int, stride: int, count: int):
+    """Protect positions offset, offset + stride, ... (count of them, count <= heavy)."""
+    _check(lib().h2o_cache_set_static_pattern(cache.handle, int(offset), int(stride), int(count)))
+
+
 def h2o_cache_info(cache: Cache) -> list[int]:
     info = (ctypes.c_int32 * 10)()
     _check(lib().h2o_cache_info(cache.handle, info))
@@ -266,6 +274,17 @@ def h2o_prefill_colsum_static(q, k, scale, colsum, kv_dtype=None, stream=None):
     _check(lib().h2o_prefill_colsum_static(
         _ptr(q, dt, (B, H, L, D), "q"), _ptr(k, dt, (B, H, L, D), "k"), B, H, D, L, code, float(scale),
         _ptr(colsum, torch.float32, (B, H, L), "colsum"), _stream(stream)))
+
+
+def h2o_prefill_colsum_static_check(stream=None):
+    """Raise H2OError if the last h2o_prefill_colsum_static call's kernels
+    latched a device error (synchronises the stream)."""
+    _check(lib().h2o_prefill_colsum_static_check(_stream(stream)))
+
+
+def h2o_debug_fail_alloc(after: int):
+    """Make the library's device allocation number after+1 from now fail (-1: off)."""
+    _check(lib().h2o_debug_fail_alloc(int(after)))
 
 
 def h2o_last_error() -> str:

@@ -561,13 +561,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
   // probabilities -> accumulated scores, stored at once (the evicted slot's
   // score is overwritten with the newcomer's below, after the block barrier
   // that orders the two stores); local minimum candidate key
-  const int limit = p - R;  // candidates: kept positions <= p - R
+  const int limit = p - R;  // candidates: kept positions <= p - R outside the static pattern
   unsigned long long kmin = ~0ull;
   int smin = -1;
   for (int j = tid; j < nrows; j += NT) {
     const float ns = sc[j] + exp2f(lg[j] - M) * inv;
     prm.score[slot0 + j] = ns;
-    if (full && ps[j] <= limit) {
+    if (full && ps[j] <= limit && !is_protected(prm.sp, ps[j])) {
       const unsigned long long key =
           (static_cast<unsigned long long>(__float_as_uint(ns)) << 32) | static_cast<uint32_t>(ps[j]);
       if (key < kmin) {
@@ -874,7 +874,7 @@ __global__ void __launch_bounds__(kWarpNW * 32, 1) decode_warp_kernel(const Deco
     for (int j = lane; j < count; j += 32) {
       const float ns = sc[j] + exp2f(lg[j] - m) * inv;
       if (ok) prm.score[slot0 + j] = ns;
-      if (fullc && ps[j] <= limit) {
+      if (fullc && ps[j] <= limit && !is_protected(prm.sp, ps[j])) {
         const unsigned long long key =
             (static_cast<unsigned long long>(__float_as_uint(ns)) << 32) | static_cast<uint32_t>(ps[j]);
         if (key < kmin) {

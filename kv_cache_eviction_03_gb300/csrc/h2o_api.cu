@@ -1,8 +1,10 @@
 // C ABI of the H2O library: cache object, argument checks, error reporting and
 // stream-ordered launches of the decode / prefill kernels.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <map>
@@ -38,6 +40,39 @@ void ranks_from_positions(const int* pos, int P, int C, std::vector<int>& out) {
 
 
 thread_local char g_msg[512] = "";
+
+// NVTX range around an ABI call (visible in Nsight Systems / Compute; a
+// no-op when no tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+
+// Allocation-failure injection (h2o_debug_fail_alloc): the number of device
+// allocations still allowed before the next one fails, or -1 when disarmed.
+std::atomic<long long> g_alloc_budget{-1};
+
+// Every device allocation of the library goes through here.
+cudaError_t dev_alloc(void** p, size_t bytes) {
+  long long b = g_alloc_budget.load();
+  while (b >= 0) {
+    if (g_alloc_budget.compare_exchange_weak(b, b - 1)) {
+      if (b == 0) {  // this is the allocation that fails; the hook disarms
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+      }
+      break;
+    }
+  }
+  return cudaMalloc(p, bytes);
+}
+template <typename T>
+cudaError_t dev_alloc(T** p, size_t bytes) {
+  void* v = nullptr;
+  cudaError_t e = dev_alloc(&v, bytes);
+  *p = static_cast<T*>(v);
+  return e;
+}
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -152,6 +187,7 @@ const char* h2o_last_error(void) { return g_msg; }
 
 int h2o_cache_create(int batch, int heads, int head_dim, int heavy_budget, int recent_budget, int kv_dtype,
                      h2o_cache** out) {
+  NvtxRange nvtx("h2o_cache_create");
   if (!out) return fail(H2O_EINVAL, "h2o_cache_create: out is NULL");
   *out = nullptr;
   if (batch < 1 || heads < 1) return fail(H2O_EINVAL, "h2o_cache_create: batch and heads must be >= 1");
@@ -176,6 +212,7 @@ int h2o_cache_create(int batch, int heads, int head_dim, int heavy_budget, int r
   c->dtype = kv_dtype;
   c->elem = kv_dtype == H2O_F16 ? 2 : 4;
   c->P = static_cast<int>(P);
+  c->sp = h2o::StaticPattern{0, 1, 0};
   cudaError_t e = cudaGetDevice(&c->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
   if (e != cudaSuccess) {
@@ -184,12 +221,12 @@ int h2o_cache_create(int batch, int heads, int head_dim, int heavy_budget, int r
   }
   const size_t nslot = static_cast<size_t>(c->P) * c->C;
   const size_t nring = static_cast<size_t>(c->P) * c->recent;
-  if ((e = cudaMalloc(&c->K, kv_bytes(c))) != cudaSuccess || (e = cudaMalloc(&c->V, kv_bytes(c))) != cudaSuccess ||
-      (e = cudaMalloc(&c->score, nslot * sizeof(float))) != cudaSuccess ||
-      (e = cudaMalloc(&c->pos, nslot * sizeof(int))) != cudaSuccess ||
-      (e = cudaMalloc(&c->ring, nring * sizeof(int))) != cudaSuccess ||
-      (e = cudaMalloc(&c->ctr, static_cast<size_t>(c->P) * sizeof(h2o::PairCtr))) != cudaSuccess ||
-      (e = cudaMalloc(&c->err, sizeof(int))) != cudaSuccess) {
+  if ((e = dev_alloc(&c->K, kv_bytes(c))) != cudaSuccess || (e = dev_alloc(&c->V, kv_bytes(c))) != cudaSuccess ||
+      (e = dev_alloc(&c->score, nslot * sizeof(float))) != cudaSuccess ||
+      (e = dev_alloc(&c->pos, nslot * sizeof(int))) != cudaSuccess ||
+      (e = dev_alloc(&c->ring, nring * sizeof(int))) != cudaSuccess ||
+      (e = dev_alloc(&c->ctr, static_cast<size_t>(c->P) * sizeof(h2o::PairCtr))) != cudaSuccess ||
+      (e = dev_alloc(&c->err, sizeof(int))) != cudaSuccess) {
     h2o_cache_destroy(c);
     return cuda_fail(e, "h2o_cache_create: cudaMalloc");
   }
@@ -226,6 +263,7 @@ void h2o_cache_destroy(h2o_cache* c) {
 }
 
 int h2o_cache_reset(h2o_cache* c, void* stream) {
+  NvtxRange nvtx("h2o_cache_reset");
   if (!c) return fail(H2O_EINVAL, "h2o_cache_reset: cache is NULL");
   touch_stream(c, stream);
   cudaError_t e = h2o::launch_reset(c->ctr, c->pos, c->score, c->ring, c->P, c->C, c->recent, as_stream(stream));
@@ -239,6 +277,7 @@ int h2o_cache_reset(h2o_cache* c, void* stream) {
 static int prefill_impl(h2o_cache* c, const void* q, const void* k, const void* v, int prompt_len,
                         const int32_t* lens, float scale, float* out_or_null, float* colsum_or_null,
                         float* lse_or_null, void* stream) {
+  NvtxRange nvtx("h2o_prefill");
   if (!c) return fail(H2O_EINVAL, "h2o_prefill: cache is NULL");
   if (prompt_len < 0) return fail(H2O_EINVAL, "h2o_prefill: prompt_len must be >= 0");
   if (prompt_len == 0) return h2o_cache_reset(c, stream);
@@ -259,7 +298,7 @@ static int prefill_impl(h2o_cache* c, const void* q, const void* k, const void* 
       c->ws = nullptr;
       c->ws_len = 0;
     }
-    if ((e = cudaMalloc(&c->ws, 2 * need * c->P * sizeof(float))) != cudaSuccess)
+    if ((e = dev_alloc(&c->ws, 2 * need * c->P * sizeof(float))) != cudaSuccess)
       return cuda_fail(e, "h2o_prefill: workspace cudaMalloc");
     c->ws_len = need;
   }
@@ -275,7 +314,7 @@ static int prefill_impl(h2o_cache* c, const void* q, const void* k, const void* 
       c->wsp = nullptr;
       c->wsp_len = 0;
     }
-    if ((e = cudaMalloc(&c->wsp, need_p * sizeof(float))) != cudaSuccess)
+    if ((e = dev_alloc(&c->wsp, need_p * sizeof(float))) != cudaSuccess)
       return cuda_fail(e, "h2o_prefill: partials workspace cudaMalloc");
     c->wsp_len = need_p;
   }
@@ -316,6 +355,7 @@ static int prefill_impl(h2o_cache* c, const void* q, const void* k, const void* 
   sp.C = c->C;
   sp.lens = lens;
   sp.heads = c->H;
+  sp.sp = c->sp;
   if ((e = h2o::launch_prefill_select(sp, c->dtype, c->D, c->P, s)) != cudaSuccess)
     return cuda_fail(e, "h2o_prefill: select launch");
   if (lse_or_null && (e = h2o::launch_lse_export(pp.lse2, lse_or_null, plen, s)) != cudaSuccess)
@@ -344,6 +384,7 @@ int h2o_prefill(h2o_cache* c, const void* q, const void* k, const void* v, int p
 
 int h2o_decode_step(h2o_cache* c, const void* q, const void* k_new, const void* v_new, float scale, float* out,
                     int32_t* evicted_or_null, void* stream) {
+  NvtxRange nvtx("h2o_decode_step");
   if (!c) return fail(H2O_EINVAL, "h2o_decode_step: cache is NULL");
   if (!q || !k_new || !v_new || !out) return fail(H2O_EINVAL, "h2o_decode_step: q, k_new, v_new and out are required");
   if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out))
@@ -373,6 +414,7 @@ int h2o_decode_step(h2o_cache* c, const void* q, const void* k_new, const void* 
   dp.pairs = c->P;
   dp.rank = c->rank;
   dp.rope = c->rope;
+  dp.sp = c->sp;
   cudaError_t e = h2o::launch_decode(dp, c->dtype, c->D, c->P, splits, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "h2o_decode_step: launch");
   c->host_next_p += 1;
@@ -387,6 +429,7 @@ size_t h2o_cache_state_bytes(const h2o_cache* c) {
 }
 
 int h2o_cache_export_state(const h2o_cache* c, void* host_buf, size_t bytes, void* stream) {
+  NvtxRange nvtx("h2o_cache_export_state");
   if (!c || !host_buf) return fail(H2O_EINVAL, "h2o_cache_export_state: NULL argument");
   if (bytes < h2o_cache_state_bytes(c)) return fail(H2O_EINVAL, "h2o_cache_export_state: buffer too small");
   int* hdr = static_cast<int*>(host_buf);
@@ -422,6 +465,7 @@ int h2o_cache_export_state(const h2o_cache* c, void* host_buf, size_t bytes, voi
 }
 
 int h2o_cache_import_state(h2o_cache* c, const void* host_buf, size_t bytes, void* stream) {
+  NvtxRange nvtx("h2o_cache_import_state");
   if (!c || !host_buf) return fail(H2O_EINVAL, "h2o_cache_import_state: NULL argument");
   if (bytes < h2o_cache_state_bytes(c)) return fail(H2O_EINVAL, "h2o_cache_import_state: buffer too small");
   const int* hdr = static_cast<const int*>(host_buf);
@@ -469,6 +513,7 @@ int h2o_cache_import_state(h2o_cache* c, const void* host_buf, size_t bytes, voi
 }
 
 int h2o_cache_check(h2o_cache* c, void* stream) {
+  NvtxRange nvtx("h2o_cache_check");
   if (!c) return fail(H2O_EINVAL, "h2o_cache_check: cache is NULL");
   cudaError_t e = cudaStreamSynchronize(as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "h2o_cache_check: stream");
@@ -530,6 +575,18 @@ int h2o_cache_set_decode_shape(h2o_cache* c, int splits, int stages) {
   return H2O_OK;
 }
 
+int h2o_cache_set_static_pattern(h2o_cache* c, int offset, int stride, int count) {
+  if (!c) return fail(H2O_EINVAL, "h2o_cache_set_static_pattern: cache is NULL");
+  if (offset < 0 || stride < 1 || count < 0)
+    return fail(H2O_EINVAL, "h2o_cache_set_static_pattern: need offset >= 0, stride >= 1, count >= 0");
+  if (count > c->heavy)
+    return fail(H2O_EINVAL, "h2o_cache_set_static_pattern: count %d exceeds the heavy budget %d", count, c->heavy);
+  if (count > 0 && static_cast<long long>(offset) + static_cast<long long>(count - 1) * stride > INT_MAX)
+    return fail(H2O_EINVAL, "h2o_cache_set_static_pattern: pattern positions exceed int32");
+  c->sp = h2o::StaticPattern{offset, stride, count};
+  return H2O_OK;
+}
+
 int h2o_cache_info(const h2o_cache* c, int32_t* info) {
   if (!c || !info) return fail(H2O_EINVAL, "h2o_cache_info: NULL argument");
   info[0] = c->B;
@@ -546,6 +603,7 @@ int h2o_cache_info(const h2o_cache* c, int32_t* info) {
 }
 
 int h2o_cache_set_position_rolling(h2o_cache* c, float rope_base) {
+  NvtxRange nvtx("h2o_cache_set_position_rolling");
   if (!c) return fail(H2O_EINVAL, "h2o_cache_set_position_rolling: cache is NULL");
   if (!(rope_base >= 0.f) || !std::isfinite(rope_base))
     return fail(H2O_EINVAL, "h2o_cache_set_position_rolling: rope_base must be finite and >= 0 (0 = off)");
@@ -562,10 +620,18 @@ int h2o_cache_set_position_rolling(h2o_cache* c, float rope_base) {
   }
   const size_t nslot = static_cast<size_t>(c->P) * c->C;
   const size_t ntab = static_cast<size_t>(c->C + 1) * (c->D / 2);
-  if (!c->rank && (e = cudaMalloc(&c->rank, nslot * sizeof(int))) != cudaSuccess)
-    return cuda_fail(e, "h2o_cache_set_position_rolling: cudaMalloc");
-  if (!c->rope && (e = cudaMalloc(&c->rope, ntab * sizeof(float2))) != cudaSuccess)
-    return cuda_fail(e, "h2o_cache_set_position_rolling: cudaMalloc");
+  // Everything is built into new buffers and swapped in only once it is
+  // complete, so a failure leaves the cache exactly as it was.
+  int* rank = nullptr;
+  float2* rope = nullptr;
+  auto give_up = [&](cudaError_t err, const char* what) {
+    cudaFree(rank);
+    cudaFree(rope);
+    return cuda_fail(err, what);
+  };
+  if ((e = dev_alloc(&rank, nslot * sizeof(int))) != cudaSuccess ||
+      (e = dev_alloc(&rope, ntab * sizeof(float2))) != cudaSuccess)
+    return give_up(e, "h2o_cache_set_position_rolling: cudaMalloc");
   // (cos, sin) of rank * base^(-2i/D) for ranks 0..C, in double, stored as float
   std::vector<float2> tab(ntab);
   for (int r = 0; r <= c->C; ++r)
@@ -576,11 +642,15 @@ int h2o_cache_set_position_rolling(h2o_cache* c, float rope_base) {
     }
   std::vector<int> pos(nslot), ranks;
   if ((e = cudaMemcpy(pos.data(), c->pos, nslot * sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
-    return cuda_fail(e, "h2o_cache_set_position_rolling: read positions");
+    return give_up(e, "h2o_cache_set_position_rolling: read positions");
   ranks_from_positions(pos.data(), c->P, c->C, ranks);
-  if ((e = cudaMemcpy(c->rope, tab.data(), ntab * sizeof(float2), cudaMemcpyHostToDevice)) != cudaSuccess ||
-      (e = cudaMemcpy(c->rank, ranks.data(), nslot * sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess)
-    return cuda_fail(e, "h2o_cache_set_position_rolling: upload");
+  if ((e = cudaMemcpy(rope, tab.data(), ntab * sizeof(float2), cudaMemcpyHostToDevice)) != cudaSuccess ||
+      (e = cudaMemcpy(rank, ranks.data(), nslot * sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess)
+    return give_up(e, "h2o_cache_set_position_rolling: upload");
+  cudaFree(c->rank);
+  cudaFree(c->rope);
+  c->rank = rank;
+  c->rope = rope;
   c->rope_base = rope_base;
   // the cluster kernel with one more int of shared memory per slot; a
   // warp-per-pair or explicit shape goes back to the automatic one
@@ -590,11 +660,17 @@ int h2o_cache_set_position_rolling(h2o_cache* c, float rope_base) {
   return H2O_OK;
 }
 
+int h2o_debug_fail_alloc(int after) {
+  if (after < -1) return fail(H2O_EINVAL, "h2o_debug_fail_alloc: after must be >= -1");
+  g_alloc_budget.store(after);
+  return H2O_OK;
+}
+
 int h2o_selftest_wait_timeout(unsigned polls, int* gave_up, unsigned long long* elapsed_ns) {
   if (polls < 1 || polls > 1000000u || gave_up == nullptr || elapsed_ns == nullptr)
     return fail(H2O_EINVAL, "h2o_selftest_wait_timeout: polls must be 1..1000000 and the outputs non-null");
   void* buf = nullptr;
-  cudaError_t e = cudaMalloc(&buf, 16);
+  cudaError_t e = dev_alloc(&buf, 16);
   if (e != cudaSuccess) return cuda_fail(e, "h2o_selftest_wait_timeout: cudaMalloc");
   int* flags = static_cast<int*>(buf);
   unsigned long long* ns = reinterpret_cast<unsigned long long*>(static_cast<char*>(buf) + 8);

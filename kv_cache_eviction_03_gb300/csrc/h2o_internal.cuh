@@ -17,6 +17,25 @@ enum : int {
   ERR_XCH_TIMEOUT = 32,  // a wait for the partial results a peer CTA pushes gave up
 };
 
+// Static sparse pattern combined with heavy hitters ("H2O ... 深度解读报告",
+// section 4.5, Table 2): positions offset, offset + stride, ...,
+// offset + (count - 1) * stride are kept for good.  They take heavy-budget
+// slots (count <= heavy), the prefill keeps them first and decode never
+// evicts them.  count = 0: no pattern.
+struct StaticPattern {
+  int offset;
+  int stride;
+  int count;
+};
+
+__host__ __device__ __forceinline__ bool is_protected(const StaticPattern& sp, int pos) {
+  if (sp.count <= 0) return false;
+  const int d = pos - sp.offset;
+  if (d < 0) return false;
+  const int k = d / sp.stride;
+  return k < sp.count && k * sp.stride == d;
+}
+
 // Per-pair counters kept on the device so decode steps can be replayed from
 // a CUDA graph: next absolute position, occupied slots, ring head.
 struct PairCtr {
@@ -52,6 +71,7 @@ struct DecodeParams {
   // and cos / sin of rank * base^(-2i/D) for ranks 0..C and pairs i < D/2
   int* rank;           // [P, C]
   const float2* rope;  // [C + 1, D / 2]
+  StaticPattern sp;    // protected positions, never eviction candidates
 };
 
 struct PrefillParams {
@@ -91,6 +111,7 @@ struct SelectParams {
   int L, heavy, recent, C;    // L: row stride of the inputs (the longest prompt)
   const int* lens = nullptr;  // [B] per-batch-row prompt lengths (device), or nullptr: all L
   int heads = 1;
+  StaticPattern sp = {0, 1, 0};  // protected positions: kept before any heavy hitter
 };
 
 // Prompt length of pair `pair`: its batch row's length, clamped to [0, L],
@@ -177,4 +198,5 @@ struct h2o_cache {
   int* rank;
   float2* rope;
   float rope_base;
+  h2o::StaticPattern sp;  // static sparse pattern (count 0: none)
 };

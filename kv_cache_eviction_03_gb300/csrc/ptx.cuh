@@ -1,5 +1,5 @@
 // Inline-PTX helpers for sm_103a: mbarriers, bulk async copies, cp.async,
-// ldmatrix / mma.sync fragments, programmatic dependent launch.
+// tcgen05 / TMEM, programmatic dependent launch.
 #pragma once
 #include <cstdint>
 #include <cuda_fp16.h>
@@ -117,13 +117,8 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
-// ---------------------------------------------------------------- cp.async (16 B)
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
-  const int n = valid ? 16 : 0;  // 0 source bytes: zero-fill
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(n)
-               : "memory");
-}
-// 4-byte variant (dst and src 4-byte aligned).
+// ---------------------------------------------------------------- cp.async
+// 4-byte asynchronous copy global -> shared (dst and src 4-byte aligned).
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
@@ -133,26 +128,6 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// ---------------------------------------------------------------- ldmatrix / mma
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-// D = A(16x16, row) * B(16x8, col) + D, fp16 inputs, fp32 accumulators.
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 // 2^x by the SFU's approximate exponential (PTX ex2.approx.ftz.f32: relative
 // error a few units in the last place; results below 2^-126 flush to zero).
 __device__ __forceinline__ float ex2(float x) {

@@ -8,7 +8,9 @@
 //
 // Heavy hitters are the `heavy` largest keys (colsum_j, j) among positions
 // j < L - recent (larger position kept on equal scores, i.e. the same total
-// order under which decode evicts the minimum).  One CTA per pair finds the
+// order under which decode evicts the minimum).  Positions of a static
+// pattern (section 4.5, Table 2; at most `heavy` of them) rank above every
+// score, so they are kept first and the heavy hitters fill the rest.  One CTA per pair finds the
 // threshold with an MSB-first radix select on the float bits (non-negative
 // floats order like their bit patterns), then compacts the kept positions in
 // ascending order with block-wide ballot scans and gathers their K/V rows
@@ -126,6 +128,12 @@ __device__ __forceinline__ void pick_digit(const unsigned* hist, unsigned k, uns
   }
 }
 
+// Selection key of position j: the bits of its (non-negative) column sum, or
+// those of +infinity for a protected position, above every finite score.
+__device__ __forceinline__ unsigned key_bits(const float* colsum, const StaticPattern& sp, int j) {
+  return is_protected(sp, j) ? 0x7F800000u : __float_as_uint(colsum[j]);
+}
+
 template <int ROWB>
 __global__ void __launch_bounds__(NT, 2) select_kernel(const SelectParams prm) {
   __shared__ unsigned hist[256];
@@ -173,7 +181,7 @@ __global__ void __launch_bounds__(NT, 2) select_kernel(const SelectParams prm) {
         for (int b = tid; b < 256; b += NT) hist[b] = 0;
         __syncthreads();
         for (int j = tid; j < n; j += NT) {
-          const unsigned bits = __float_as_uint(colsum[j]);
+          const unsigned bits = key_bits(colsum, prm.sp, j);
           if ((bits & mask) == prefix) atomicAdd(&hist[(bits >> shift) & 255u], 1u);
         }
         __syncthreads();
@@ -189,7 +197,7 @@ __global__ void __launch_bounds__(NT, 2) select_kernel(const SelectParams prm) {
       unsigned base_eq = 0, base_keep = 0;
       for (int j0 = 0; j0 < n; j0 += NT) {
         const int j = j0 + tid;
-        const unsigned bits = j < n ? __float_as_uint(colsum[j]) : 0u;
+        const unsigned bits = j < n ? key_bits(colsum, prm.sp, j) : 0u;
         const bool is_eq = j < n && bits == prefix;
         unsigned tot_eq, tot_keep;
         const unsigned eq_rank = base_eq + block_scan(is_eq, scan, &tot_eq);

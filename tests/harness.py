@@ -54,21 +54,36 @@ class StepReport:
     notes: list = field(default_factory=list)
 
 
-def candidate_near_ties(before: O.PairState, prob, recent) -> set:
-    """Slots whose updated score is within NEAR_TIE of the lowest candidate."""
+def candidate_near_ties(before: O.PairState, prob, recent, pattern=None) -> set:
+    """Slots whose updated score is within NEAR_TIE of the lowest candidate
+    (candidates: kept positions <= p - recent outside the static pattern)."""
     n = before.count
     new = O.to_f32(before.score[:n] + prob[:n])
-    cand = [j for j in range(n) if before.pos[j] <= before.p - recent]
+    prot = pattern.protects(before.pos[:n]) if pattern is not None else np.zeros(n, dtype=bool)
+    cand = [j for j in range(n) if before.pos[j] <= before.p - recent and not prot[j]]
     lo = min(new[j] for j in cand)
     return {j for j in cand if new[j] - lo <= NEAR_TIE}
 
 
+def check_other_victim(before: O.PairState, q, k_new, v_new, scale, heavy, recent, gpu_victim, ref_victim, gap,
+                       rope_base=None, pattern=None, where=""):
+    """A GPU victim that differs from the oracle's is accepted only at a near
+    tie (the oracle's two lowest candidates within NEAR_TIE) and only if the
+    GPU's victim is itself one of the candidates within NEAR_TIE of the
+    lowest updated score (any of them is a correct choice)."""
+    assert gap <= NEAR_TIE, f"{where}: evicted slot {gpu_victim} != oracle {ref_victim} (gap {gap})"
+    r = O.decode_step_pair(before.copy(), q, k_new, v_new, scale, heavy, recent, rope_base, pattern)
+    assert int(gpu_victim) in candidate_near_ties(before, r.prob, recent, pattern), \
+        f"{where}: GPU victim {gpu_victim} is not a near tie"
+
+
 def compare_decode_step(cache: B.Cache, gpu_after: dict, gpu_out, gpu_ev, ref_before: O.CacheState,
                         ref_after: O.CacheState, ref_out, ref_ev, ref_gap, rep: StepReport, inputs, scale,
-                        pairs=None):
+                        pairs=None, rope_base=None, pattern=None):
     """Compare one decode step (identical pre-step state) pair by pair.
 
-    inputs = (q, k_new, v_new) as float64 [P, D] arrays of this step."""
+    inputs = (q, k_new, v_new) as float64 [P, D] arrays of this step;
+    rope_base / pattern: position rolling and static pattern of the step."""
     tol = out_tol(cache.kv_dtype)
     R = cache.recent
     pairs = range(ref_out.shape[0]) if pairs is None else pairs
@@ -82,11 +97,8 @@ def compare_decode_step(cache: B.Cache, gpu_after: dict, gpu_out, gpu_ev, ref_be
             rep.near_ties += 1
         if ge != re_:
             # accepted only at a near tie, and only for an equally good victim
-            assert ref_gap[i] <= NEAR_TIE, f"pair {i}: evicted slot {ge} != oracle {re_} (gap {ref_gap[i]})"
-            before = ref_before.pair(i)
-            r = O.decode_step_pair(before.copy(), inputs[0][i], inputs[1][i], inputs[2][i], scale,
-                                   cache.heavy, cache.recent)
-            assert ge in candidate_near_ties(before, r.prob, R), f"pair {i}: GPU victim {ge} is not a near tie"
+            check_other_victim(ref_before.pair(i), inputs[0][i], inputs[1][i], inputs[2][i], scale, cache.heavy,
+                               R, ge, re_, ref_gap[i], rope_base, pattern, where=f"pair {i}")
             rep.tie_mismatch += 1
             rep.notes.append((i, ge, re_))
             continue
@@ -106,9 +118,59 @@ def compare_decode_step(cache: B.Cache, gpu_after: dict, gpu_out, gpu_ev, ref_be
         assert np.array_equal(gpu_after["V"][i][used], ref_after.V[i][used].astype(kd)), f"pair {i}: V slots"
 
 
-def heavy_boundary_gap(colsum_f32: np.ndarray, L: int, heavy: int, recent: int) -> float:
-    """Gap between the heavy-th and (heavy+1)-th largest candidate scores."""
-    if L <= heavy + recent or heavy == 0:
+def heavy_boundary_gap(colsum_f32: np.ndarray, L: int, heavy: int, recent: int, pattern=None) -> float:
+    """Gap between the last kept and the first dropped candidate score at the
+    heavy boundary (candidates: positions < L - recent outside the pattern)."""
+    if L <= heavy + recent:
         return np.inf
-    c = np.sort(colsum_f32[:L - recent])[::-1]
-    return float(c[heavy - 1] - c[heavy]) if heavy < c.size else np.inf
+    n = L - recent
+    prot = pattern.protects(np.arange(n)) if pattern is not None else np.zeros(n, dtype=bool)
+    take = heavy - int(prot.sum())
+    c = np.sort(colsum_f32[:n][~prot])[::-1]
+    if take == 0 or take >= c.size:
+        return np.inf
+    return float(c[take - 1] - c[take])
+
+
+def check_prefill_pair(g: dict, i: int, st: O.PairState, colsum_ref, k_pair, v_pair, L: int, heavy: int,
+                       recent: int, kv_np_dtype, pattern=None) -> bool:
+    """Pair i of an exported GPU state after the prefill, against the oracle.
+
+    Equal kept sets: slots, K/V, scores (1e-5 relative to the oracle's column
+    sums), ring and counters are compared.  Different kept sets are accepted
+    only at the heavy boundary: every position kept by one side and not the
+    other must be a non-pattern candidate whose float32 column sum lies within
+    NEAR_TIE of the boundary score, and the GPU's own set must still be laid
+    out correctly (heavy hitters ascending below L - recent with every pattern
+    position among them, the recent window after them, each slot's K/V row,
+    score, the ring and the counters).  Returns True when the sets are equal.
+    """
+    C = heavy + recent
+    gp = g["pos"][i].astype(np.int64)
+    count = int(g["count"][i])
+    assert (int(g["p"][i]), count, int(g["head"][i])) == (st.p, st.count, st.head), f"pair {i}: counters"
+    assert np.array_equal(g["ring"][i], st.ring.astype(np.int32)), f"pair {i}: ring"
+    same = np.array_equal(gp, st.pos)
+    if not same:
+        assert L > C, f"pair {i}: a prompt within the budget keeps every position"
+        cs32 = O.to_f32(colsum_ref)
+        n = L - recent
+        gh, rh = gp[:heavy], st.pos[:heavy]
+        assert np.all(np.diff(gh) > 0) and gh.max() < n, f"pair {i}: heavy slots not ascending below L-recent"
+        assert np.array_equal(gp[heavy:C], np.arange(n, L)), f"pair {i}: recent window"
+        prot = pattern.protects(np.arange(n)) if pattern is not None else np.zeros(n, dtype=bool)
+        assert set(np.nonzero(prot)[0].tolist()) <= set(gh.tolist()), f"pair {i}: pattern position dropped"
+        free = np.nonzero(~prot)[0]
+        take = heavy - int(prot.sum())
+        boundary = np.sort(cs32[free])[::-1][take - 1]
+        for j in set(gh.tolist()) ^ set(rh.tolist()):
+            assert not prot[j] and abs(cs32[j] - boundary) <= NEAR_TIE, \
+                f"pair {i}: position {j} (score {cs32[j]}) differs away from the heavy boundary {boundary}"
+    used = gp[:count]
+    gs = g["score"][i][:count].astype(np.float64)
+    rs = colsum_ref[used]
+    assert count == 0 or np.max(np.abs(gs - rs) / rs) <= SCORE_RTOL, f"pair {i}: slot scores"
+    assert np.array_equal(g["K"][i][:count], k_pair[used].astype(kv_np_dtype)), f"pair {i}: K slots"
+    assert np.array_equal(g["V"][i][:count], v_pair[used].astype(kv_np_dtype)), f"pair {i}: V slots"
+    assert np.all(g["pos"][i][count:] == -1)
+    return same

@@ -85,3 +85,27 @@ def test_selftest_rejects_bad_poll_counts():
         assert lib.h2o_last_error().decode().startswith("h2o_selftest_wait_timeout")
     assert lib.h2o_selftest_wait_timeout(10, None, ctypes.byref(ns)) == -1
 
+
+
+def test_static_pattern_and_alloc_hook_reject_bad_arguments():
+    lib = B.lib()
+    assert lib.h2o_cache_set_static_pattern(None, 0, 1, 0) == -1
+    assert lib.h2o_last_error().decode().startswith("h2o_cache_set_static_pattern")
+    assert lib.h2o_debug_fail_alloc(-2) == -1
+    assert lib.h2o_debug_fail_alloc(-1) == 0  # disarm: always accepted
+
+
+def test_alloc_hook_fails_the_chosen_allocation_on_the_host():
+    """Host-side fault injection: with the hook armed at 0 the very next
+    device allocation fails.  Without a GPU, create fails first on the
+    missing device, so this runs the hook path only where a device exists;
+    the hook itself is a host counter and is disarmed after the test."""
+    lib = B.lib()
+    out = ctypes.c_void_p(1234)
+    try:
+        assert lib.h2o_debug_fail_alloc(0) == 0
+        code = lib.h2o_cache_create(1, 2, 64, 4, 4, 0, ctypes.byref(out))
+        assert code in (-2, -3)  # ENOMEM from the hook, or ECUDA without a device
+        assert out.value is None
+    finally:
+        lib.h2o_debug_fail_alloc(-1)

@@ -11,7 +11,7 @@ trajectory on their own and are compared step by step.
 import numpy as np
 import pytest
 
-from harness import StepReport, compare_decode_step, oracle_image, out_tol, NEAR_TIE
+from harness import StepReport, check_other_victim, compare_decode_step, oracle_image, out_tol
 from kv_cache_eviction_03_gb300 import binding as B
 from kv_cache_eviction_03_gb300 import workload as W
 from oracle import h2o_oracle as O
@@ -30,26 +30,30 @@ def flat(a):
     return a.reshape((-1,) + a.shape[2:])
 
 
-def oracle_start(w, seed):
+def oracle_start(w, seed, pattern=None):
     if w.prompt:
         q, k, v = W.prefill_inputs(w, seed)
-        st, _, _ = O.prefill(q, k, v, w.heavy, w.recent, w.scale)
+        st, _, _ = O.prefill(q, k, v, w.heavy, w.recent, w.scale, pattern)
         return st
     return O.empty_cache(w.pairs, w.heavy, w.recent, w.head_dim)
 
 
-def run_stepwise(w, seed, check=None, splits=None, stages=0):
+def run_stepwise(w, seed, check=None, splits=None, stages=0, pattern=None):
+    """Every checked step starts both sides from the oracle's state.
+    pattern: an oracle StaticPattern, also set on the cache."""
     cache = B.h2o_cache_create(w.batch, w.heads, w.head_dim, w.heavy, w.recent, dtype_code(w))
     if splits or stages:
         B.h2o_cache_set_decode_shape(cache, splits or 0, stages)
-    st = oracle_start(w, seed)
+    if pattern is not None:
+        B.h2o_cache_set_static_pattern(cache, pattern.offset, pattern.stride, pattern.count)
+    st = oracle_start(w, seed, pattern)
     out = torch.empty((w.batch, w.heads, w.head_dim), dtype=torch.float32, device="cuda")
     ev = torch.empty((w.batch, w.heads), dtype=torch.int32, device="cuda")
     rep = StepReport()
     P, D = w.pairs, w.head_dim
     for t in range(w.decode):
         qd, kd, vd = W.decode_inputs(w, w.prompt + t, seed)
-        nxt, r_out, r_ev, gap = O.decode_step(st, qd, kd, vd, w.heavy, w.recent, w.scale)
+        nxt, r_out, r_ev, gap = O.decode_step(st, qd, kd, vd, w.heavy, w.recent, w.scale, pattern=pattern)
         if check is None or t in check:
             B.h2o_cache_import_state(cache, oracle_image(cache, st))
             B.h2o_decode_step(cache, torch.from_numpy(qd).cuda(), torch.from_numpy(kd).cuda(),
@@ -58,19 +62,23 @@ def run_stepwise(w, seed, check=None, splits=None, stages=0):
             after = B.unpack_state(cache, B.h2o_cache_export_state(cache))
             compare_decode_step(cache, after, out.cpu().numpy().reshape(P, D), ev.cpu().numpy().reshape(P),
                                 st, nxt, r_out, r_ev, gap, rep, inputs=(flat(qd), flat(kd), flat(vd)),
-                                scale=w.scale)
+                                scale=w.scale, pattern=pattern)
         st = nxt
     B.h2o_cache_destroy(cache)
     return rep
 
 
-def run_free(w, seed, splits=None):
-    """Both sides run prefill + every decode step on their own."""
+def run_free(w, seed, splits=None, pattern=None):
+    """Both sides run prefill + every decode step on their own.  A different
+    victim is accepted only for an equally good candidate (near tie); the
+    pair's trajectories then part and it is no longer compared."""
     cache = B.h2o_cache_create(w.batch, w.heads, w.head_dim, w.heavy, w.recent, dtype_code(w))
+    if pattern is not None:
+        B.h2o_cache_set_static_pattern(cache, pattern.offset, pattern.stride, pattern.count)
     if splits:
         B.h2o_cache_set_decode_shape(cache, splits)
     P, D = w.pairs, w.head_dim
-    st = oracle_start(w, seed)
+    st = oracle_start(w, seed, pattern)
     if w.prompt:
         q, k, v = W.prefill_inputs(w, seed)
         B.h2o_prefill(cache, torch.from_numpy(q).cuda(), torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(),
@@ -88,7 +96,8 @@ def run_free(w, seed, splits=None):
         qd, kd, vd = W.decode_inputs(w, w.prompt + t, seed)
         B.h2o_decode_step(cache, torch.from_numpy(qd).cuda(), torch.from_numpy(kd).cuda(),
                           torch.from_numpy(vd).cuda(), w.scale, out, ev)
-        st, r_out, r_ev, gap = O.decode_step(st, qd, kd, vd, w.heavy, w.recent, w.scale)
+        before = st
+        st, r_out, r_ev, gap = O.decode_step(st, qd, kd, vd, w.heavy, w.recent, w.scale, pattern=pattern)
         g_out = out.cpu().numpy().reshape(P, D)
         g_ev = ev.cpu().numpy().reshape(P)
         for i in np.nonzero(alive)[0]:
@@ -96,7 +105,9 @@ def run_free(w, seed, splits=None):
             worst = max(worst, err)
             assert err <= tol, f"step {t} pair {i}: out err {err}"
             if g_ev[i] != r_ev[i]:
-                assert gap[i] <= NEAR_TIE, f"step {t} pair {i}: evicted {g_ev[i]} != {r_ev[i]}"
+                f64 = lambda a: flat(a)[i]
+                check_other_victim(before.pair(i), f64(qd), f64(kd), f64(vd), w.scale, w.heavy, w.recent, g_ev[i],
+                                   r_ev[i], gap[i], pattern=pattern, where=f"step {t} pair {i}")
                 alive[i] = False  # trajectories legitimately part at a near tie
     B.h2o_cache_check(cache)
     g = B.unpack_state(cache, B.h2o_cache_export_state(cache))

@@ -5,7 +5,7 @@ import math
 import numpy as np
 import pytest
 
-from harness import NEAR_TIE, heavy_boundary_gap, out_tol
+from harness import check_prefill_pair, out_tol
 from kv_cache_eviction_03_gb300 import binding as B
 from kv_cache_eviction_03_gb300 import workload as W
 from oracle import h2o_oracle as O
@@ -15,10 +15,13 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 
-def check_prefill(w, seed, pairs=None, with_out=True):
-    """Run the GPU prefill on the full shape, compare `pairs` (default all)."""
+def check_prefill(w, seed, pairs=None, with_out=True, pattern=None):
+    """Run the GPU prefill on the full shape, compare `pairs` (default all).
+    pattern: an oracle StaticPattern, also set on the cache."""
     dt = B.H2O_F16 if w.dtype == "f16" else B.H2O_F32
     cache = B.h2o_cache_create(w.batch, w.heads, w.head_dim, w.heavy, w.recent, dt)
+    if pattern is not None:
+        B.h2o_cache_set_static_pattern(cache, pattern.offset, pattern.stride, pattern.count)
     q, k, v = W.prefill_inputs(w, seed)
     L, P, D = w.prompt, w.pairs, w.head_dim
     dev = lambda a: torch.from_numpy(a).cuda()
@@ -35,7 +38,7 @@ def check_prefill(w, seed, pairs=None, with_out=True):
     tol = out_tol(dt)
     stats = {"colsum_rel": 0.0, "out_err": 0.0, "lse_err": 0.0, "ties": 0}
     for i in (range(P) if pairs is None else pairs):
-        st, cs, o = O.prefill_pair(qf[i], kf[i], vf[i], w.heavy, w.recent, w.scale)
+        st, cs, o = O.prefill_pair(qf[i], kf[i], vf[i], w.heavy, w.recent, w.scale, pattern)
         lse_ref, _, _ = O.causal_attention_stats(qf[i], kf[i], vf[i], w.scale) if L <= 4096 else (None, 0, 0)
         rel = float(np.max(np.abs(g_cs[i] - cs) / cs))
         stats["colsum_rel"] = max(stats["colsum_rel"], rel)
@@ -49,19 +52,9 @@ def check_prefill(w, seed, pairs=None, with_out=True):
             e = float(np.max(np.abs(g_out[i] - o)))
             stats["out_err"] = max(stats["out_err"], e)
             assert e <= tol, f"pair {i}: out err {e}"
-        gap = heavy_boundary_gap(O.to_f32(cs), L, w.heavy, w.recent)
-        if not np.array_equal(g["pos"][i], st.pos):
-            assert gap <= NEAR_TIE, f"pair {i}: kept positions differ (boundary gap {gap})"
-            stats["ties"] += 1
-            continue
-        used = st.pos >= 0
-        assert np.array_equal(g["score"][i][used], st.score[used].astype(np.float32)) or \
-            np.max(np.abs(g["score"][i][used] - st.score[used]) / st.score[used]) <= 1e-5
         kd = np.float16 if w.dtype == "f16" else np.float32
-        assert np.array_equal(g["K"][i][used], st.K[used].astype(kd))
-        assert np.array_equal(g["V"][i][used], st.V[used].astype(kd))
-        assert np.array_equal(g["ring"][i], st.ring)
-        assert (g["p"][i], g["count"][i], g["head"][i]) == (st.p, st.count, st.head)
+        if not check_prefill_pair(g, i, st, cs, kf[i], vf[i], L, w.heavy, w.recent, kd, pattern):
+            stats["ties"] += 1
     B.h2o_cache_destroy(cache)
     return stats
 
@@ -165,13 +158,12 @@ def test_long_prompt_output_with_separate_column_pass():
     scale = 1 / math.sqrt(D)
     B.h2o_prefill_ex(cache, q, k, v, scale, out=out, colsum=cs)
     B.h2o_cache_check(cache)
-    g_pos = B.unpack_state(cache, B.h2o_cache_export_state(cache))["pos"]
+    g = B.unpack_state(cache, B.h2o_cache_export_state(cache))
     for i in (0, 1, 2047, Bn * H - 1):
         b, h = divmod(i, H)
         qf, kf, vf = (x[b, h].double().cpu().numpy() for x in (q, k, v))
         st, c, o = O.prefill_pair(qf, kf, vf, hv, rc, scale)
         assert np.max(np.abs(cs[b, h].cpu().numpy() - c) / c) <= 1e-5
         assert np.max(np.abs(out[b, h].cpu().numpy() - o)) <= 2e-3
-        if not np.array_equal(g_pos[i], st.pos):
-            assert heavy_boundary_gap(O.to_f32(c), L, hv, rc) <= NEAR_TIE
+        check_prefill_pair(g, i, st, c, kf, vf, L, hv, rc, np.float16)
     B.h2o_cache_destroy(cache)

@@ -11,7 +11,7 @@ states so that all pairs' results are checked.
 import numpy as np
 import pytest
 
-from harness import NEAR_TIE, StepReport, compare_decode_step, heavy_boundary_gap, oracle_image, out_tol
+from harness import StepReport, check_other_victim, check_prefill_pair, compare_decode_step, oracle_image, out_tol
 from kv_cache_eviction_03_gb300 import binding as B
 from kv_cache_eviction_03_gb300 import workload as W
 from oracle import h2o_oracle as O
@@ -55,9 +55,8 @@ def run_workload(w, seed, sample, decode_steps, stepwise_at):
             assert np.max(np.abs(gc - c) / c) <= 1e-5
             go = out[i // w.heads, i % w.heads].cpu().numpy()
             assert np.max(np.abs(go - o)) <= tol
-            same = np.array_equal(g0["pos"][i], st.pos)
-            if not same:
-                assert heavy_boundary_gap(O.to_f32(c), L, w.heavy, w.recent) <= NEAR_TIE
+            same = check_prefill_pair(g0, i, st, c, kf[i].astype(np.float64), vf[i].astype(np.float64), L, w.heavy,
+                                      w.recent, w.np_dtype)
             states.append(st)
             alive.append(same)
         del out, cs
@@ -79,13 +78,16 @@ def run_workload(w, seed, sample, decode_steps, stepwise_at):
         sub = lambda a: a.reshape(P, D)[sidx][:, None, :]
         if t in stepwise_at:
             saved[t] = (ref.copy(), (qd, kd, vd))
+        before = ref
         ref, r_out, r_ev, gap = O.decode_step(ref, sub(qd), sub(kd), sub(vd), w.heavy, w.recent, w.scale)
         g_out = o_dev.cpu().numpy().reshape(P, D)[sidx]
         g_ev = e_dev.cpu().numpy().reshape(P)[sidx]
         for j in np.nonzero(alive)[0]:
             assert np.max(np.abs(g_out[j] - r_out[j])) <= tol, f"step {t} pair {sample[j]}"
             if g_ev[j] != r_ev[j]:
-                assert gap[j] <= NEAR_TIE
+                f64 = lambda a: sub(a)[j, 0].astype(np.float64)
+                check_other_victim(before.pair(j), f64(qd), f64(kd), f64(vd), w.scale, w.heavy, w.recent, g_ev[j],
+                                   r_ev[j], gap[j], where=f"step {t} pair {sample[j]}")
                 alive[j] = False
     B.h2o_cache_check(cache)
     # ---- step-wise from identical states (every pair holds a sampled state)

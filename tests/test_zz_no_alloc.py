@@ -14,6 +14,7 @@ import pytest
 
 from kv_cache_eviction_03_gb300 import binding as B
 from kv_cache_eviction_03_gb300 import workload as W
+from oracle import h2o_oracle as O
 
 pytestmark = pytest.mark.gpu
 
@@ -37,7 +38,8 @@ def static_colsum(w, q, k):
                                          B.H2O_F16 if w.dtype == "f16" else B.H2O_F32, w.scale, cs.data_ptr(),
                                          torch.cuda.current_stream().cuda_stream)
     assert code == 0, lib.h2o_last_error().decode()
-    torch.cuda.synchronize()
+    # no bounded wait of the call's kernels gave up (synchronises the stream)
+    B.h2o_prefill_colsum_static_check()
     return cs
 
 
@@ -56,6 +58,13 @@ def test_static_scratch_matches_allocating_path_twice(dtype):
         assert rel <= 1e-5, f"call {i}: relative difference {rel}"
         # and the column sums still carry the whole attention mass
         assert abs(got.double().sum(-1) - w.prompt).max().item() <= 1e-5 * w.prompt
+        # against the fp64 oracle on a few pairs (exact definition of the sums)
+        qf = q.double().cpu().numpy().reshape(w.pairs, w.prompt, w.head_dim)
+        kf = k.double().cpu().numpy().reshape(w.pairs, w.prompt, w.head_dim)
+        g = got.cpu().numpy().reshape(w.pairs, w.prompt).astype(np.float64)
+        for p in (0, w.pairs // 2, w.pairs - 1):
+            _, ref, _ = O.causal_attention_stats(qf[p], kf[p], np.zeros((w.prompt, 1)), w.scale)
+            assert np.max(np.abs(g[p] - ref) / ref) <= 1e-5, f"call {i} pair {p}: against the oracle"
 
 
 def test_static_scratch_rejects_oversize():
