@@ -208,6 +208,56 @@ def decode_sequence(w: Workload, start: int, steps: int, seed: int | None = None
 
 
 # ---------------------------------------------------------------- device draws
+class DeviceDraws:
+    """The same recipe drawn on the GPU with torch's generator, one layer's
+    prompt or one chunk of decode steps at a time (timed workloads).  The
+    per-head key-mean table E is drawn once per object."""
+
+    def __init__(self, w: Workload, seed: int, device="cuda"):
+        import torch
+
+        self.w, self.device = w, device
+        self.g = torch.Generator(device=device)
+        self.g.manual_seed(seed)
+        self.tdt = torch.float16 if w.dtype == "f16" else torch.float32
+        self.cdf = torch.from_numpy(_zipf_cdf(w.zipf_s)).to(device)
+        self.table = torch.randn((w.heads, VOCAB, w.head_dim), generator=self.g, device=device, dtype=torch.float32)
+        self.hidx = torch.arange(w.heads, device=device)
+
+    def _normal(self, shape):
+        import torch
+
+        return torch.randn(shape, generator=self.g, device=self.device)
+
+    def _keys(self, n_pos, rows):
+        """k = 0.5 * E[h][id] + N(0,1) for `rows` x n_pos Zipf ids: [rows, H, n, D] float32."""
+        import torch
+
+        u = torch.rand((rows, n_pos), generator=self.g, device=self.device, dtype=torch.float64)
+        ids = torch.searchsorted(self.cdf, u).clamp_(max=VOCAB - 1)
+        mean = self.table[self.hidx[None, :, None], ids[:, None, :]]
+        return KEY_MEAN_WEIGHT * mean + self._normal((rows, self.w.heads, n_pos, self.w.head_dim))
+
+    def prefill(self):
+        """q, k, v [B, H, L, D] in the K/V dtype."""
+        w = self.w
+        shp = (w.batch, w.heads, w.prompt, w.head_dim)
+        q = self._normal(shp).to(self.tdt)
+        k = self._keys(w.prompt, w.batch).to(self.tdt)
+        v = self._normal(shp).to(self.tdt)
+        return q, k, v
+
+    def decode(self, steps, layers=1):
+        """q, k_new, v_new [steps, layers, B, H, D] in the K/V dtype."""
+        w = self.w
+        shp = (steps, layers, w.batch, w.heads, w.head_dim)
+        q = self._normal(shp).to(self.tdt)
+        k = self._keys(steps * layers, w.batch).reshape(w.batch, w.heads, steps, layers, w.head_dim)
+        k = k.permute(2, 3, 0, 1, 4).contiguous().to(self.tdt)
+        v = self._normal(shp).to(self.tdt)
+        return q, k, v
+
+
 def device_inputs(w: Workload, seed: int, layers: int, device="cuda"):
     """Same recipe drawn on the GPU with torch's generator (timed workloads).
 
@@ -215,32 +265,12 @@ def device_inputs(w: Workload, seed: int, layers: int, device="cuda"):
     'decode' -> list of (q, k, v) [T, B, H, D], one entry per layer, all in the
     K/V dtype and resident on `device`.
     """
-    import torch
-
-    g = torch.Generator(device=device)
-    g.manual_seed(seed)
-    tdt = torch.float16 if w.dtype == "f16" else torch.float32
-    B, H, D, L, T = w.batch, w.heads, w.head_dim, w.prompt, w.decode
-    cdf = torch.from_numpy(_zipf_cdf(w.zipf_s)).to(device)
-    table = torch.randn((H, VOCAB, D), generator=g, device=device, dtype=torch.float32)
-    hidx = torch.arange(H, device=device)
-
-    def keys(n_pos):
-        u = torch.rand((B, n_pos), generator=g, device=device, dtype=torch.float64)
-        ids = torch.searchsorted(cdf, u).clamp_(max=VOCAB - 1)  # [B, n]
-        mean = table[hidx[None, :, None], ids[:, None, :]]  # [B, H, n, D]
-        return KEY_MEAN_WEIGHT * mean + torch.randn((B, H, n_pos, D), generator=g, device=device)
-
+    d = DeviceDraws(w, seed, device)
     out = {"prefill": [], "decode": []}
     for _ in range(layers):
-        if L > 0:
-            q = torch.randn((B, H, L, D), generator=g, device=device).to(tdt)
-            k = keys(L).to(tdt)
-            v = torch.randn((B, H, L, D), generator=g, device=device).to(tdt)
-            out["prefill"].append((q, k, v))
-        qd = torch.randn((T, B, H, D), generator=g, device=device).to(tdt)
-        kd = keys(T).permute(2, 0, 1, 3).contiguous().to(tdt)
-        vd = torch.randn((T, B, H, D), generator=g, device=device).to(tdt)
-        out["decode"].append((qd, kd, vd))
-    del table
+        if w.prompt > 0:
+            out["prefill"].append(d.prefill())
+        q, k, v = d.decode(w.decode, 1)
+        out["decode"].append((q[:, 0], k[:, 0], v[:, 0]))
+    del d
     return out
