@@ -37,22 +37,31 @@ def _deps() -> list[str]:
 
 
 def is_stale() -> bool:
-    if not os.path.exists(LIB):
+    return is_stale_at(LIB)
+
+
+def is_stale_at(path: str) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(path)
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    """Compile the library if needed; returns its path."""
-    if not force and not is_stale():
-        return LIB
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
+          variant: str | None = None) -> str:
+    """Compile the library if needed; returns its path.  `variant` builds a
+    separately named copy (e.g. a profiling build with extra defines) next to
+    the product library, with its own object files."""
+    out_lib = LIB if variant is None else os.path.join(OUT_DIR, f"libh2o_gb300_{variant}.so")
+    if not force and not is_stale_at(out_lib):
+        return out_lib
     nvcc = _nvcc()
-    os.makedirs(OUT_DIR, exist_ok=True)
+    obj_dir = OUT_DIR if variant is None else os.path.join(OUT_DIR, variant)
+    os.makedirs(obj_dir, exist_ok=True)
     objs = []
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(obj_dir, src.replace(".cu", ".o"))
         cmd = [nvcc, *ARCH, *FLAGS, *(extra or []), "-I", INCLUDE, "-I", CSRC, "-c",
                os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -64,13 +73,13 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + ".tmp"
+    tmp = out_lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out_lib)
+    return out_lib
 
 
 if __name__ == "__main__":

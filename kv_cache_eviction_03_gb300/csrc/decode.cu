@@ -59,6 +59,28 @@ namespace h2o {
 namespace {
 
 constexpr float kNeg = -3.0e38f;  // finite "minus infinity" for running maxima
+
+#ifdef H2O_DECODE_TIMELINE
+// Profiling build: per-CTA time stamps (ns) of the last launches, written by
+// thread 0 (consumer warp 0, lane 0) at: 0 entry, 1 grid dependency
+// released, 2 step inputs loaded, 3 first stage landed, 4 every consumer past
+// its loop, 5 pair's softmax normaliser known, 6 victim known, 7 exit.
+__device__ unsigned long long g_decode_tl[kTimelineSlots][kTimelineMaxCtas][kTimelineStamps];
+__device__ __forceinline__ void tl_stamp(const DecodeParams& prm, int i) {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
+  const int cta = static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x);
+  if (cta < kTimelineMaxCtas) g_decode_tl[prm.tl_slot & (kTimelineSlots - 1)][cta][i] = t;
+}
+#define H2O_TL(i)                        \
+  do {                                   \
+    if (threadIdx.x == 0) tl_stamp(prm, i); \
+  } while (0)
+#else
+#define H2O_TL(i) \
+  do {            \
+  } while (0)
+#endif
 // Every wait in this kernel is on work of this same grid (bulk copies it
 // issued, stages its own warps release), so it completes within microseconds;
 // 200k polls of <= 1 us each is a generous bound.
@@ -189,6 +211,16 @@ __device__ __forceinline__ void attend_tile(const unsigned char* sK, const unsig
   __syncwarp();  // wb is rewritten by the next stage
 }
 
+// Minimum over the warp of a 64-bit key (score bits << 32 | position), in
+// two 32-bit warp reductions: the high words, then the low words of the
+// lanes that hold the lowest high word.
+__device__ __forceinline__ unsigned long long warp_min_key(unsigned long long key) {
+  const unsigned hi = static_cast<unsigned>(key >> 32);
+  const unsigned mh = __reduce_min_sync(0xffffffffu, hi);
+  const unsigned ml = __reduce_min_sync(0xffffffffu, hi == mh ? static_cast<unsigned>(key) : 0xffffffffu);
+  return (static_cast<unsigned long long>(mh) << 32) | ml;
+}
+
 // Merge the row groups of a warp: afterwards every group holds the same
 // (m, l, o) over all rows the warp has seen.
 template <typename T, int D>
@@ -303,6 +335,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
   const int C = prm.C, R = prm.R;
   const int lo = rank * prm.chunk;
   const size_t slot0 = static_cast<size_t>(pair) * C + lo;
+  H2O_TL(0);
 
   if (tid == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
@@ -336,7 +369,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
     // ---------------------------------------------------------- producer warp
     if (lane == 0) {
       // The slot store is read before the grid-dependency wait only when the
-      // previous kernel on this stream did not touch this cache.
+      // previous kernel on this stream did not touch this cache.  The pair's
+      // count is read before the first copy on purpose: the consumers' small
+      // loads go out first instead of queueing behind the ring's bulk reads.
       if (!prm.prefetch) griddep_wait();
       const int cnt = prm.ctr[pair].count;
       const int nrows = max(min(lo + prm.chunk, cnt) - lo, 0);
@@ -379,13 +414,20 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
     int4 ctr = make_int4(0, 0, 0, 0);
     int nrows = 0;
     auto load_state = [&]() {
+      // The scores and positions are needed only in the epilogue: they come
+      // by asynchronous copies over the CTA's whole slot range (no wait for
+      // the count first), completed before the merge after the loop, so no
+      // consumer stalls on them before the grid-dependency wait.
+      const int cap = max(min(lo + prm.chunk, C) - lo, 0);
+      for (int j = tid; j < cap; j += NCW * 32) {
+        cp_async4(sc + j, prm.score + slot0 + j);
+        cp_async4(ps + j, prm.pos + slot0 + j);
+      }
+      cp_async_commit();
       ctr = *reinterpret_cast<const int4*>(prm.ctr + pair);  // {p, count, head, -}
       nrows = max(min(lo + prm.chunk, ctr.y) - lo, 0);
-      for (int j = tid; j < nrows; j += NCW * 32) {
-        sc[j] = prm.score[slot0 + j];
-        ps[j] = prm.pos[slot0 + j];
-        if constexpr (ROPE) rk[j] = prm.rank[slot0 + j];
-      }
+      if constexpr (ROPE)  // ranks are needed in the loop
+        for (int j = tid; j < nrows; j += NCW * 32) rk[j] = prm.rank[slot0 + j];
     };
     // warm L2 with this pair's q, k_new and v_new rows while waiting
     {
@@ -397,6 +439,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
     }
     if (prm.prefetch) load_state();
     griddep_wait();    // every earlier kernel on the stream has completed
+    H2O_TL(1);
     if (!prm.prefetch) load_state();
     // the slice of the new K (threads < LPR) or V row (LPR..2 LPR-1) that
     // this thread writes if this CTA owns the evicted slot
@@ -425,6 +468,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
     Vec16<T>::unpack(q4, qv);
 #pragma unroll
     for (int e = 0; e < EPV; ++e) qv[e] *= prm.qscale;  // exp2(logit) is the softmax numerator
+    H2O_TL(2);
     // position rolling: the query (and the new key) sit at rank `count`, after
     // every kept token
     const float2* rope_cs = nullptr;
@@ -464,6 +508,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
         ok = false;
         atomicOr(prm.err, ERR_MBAR_TIMEOUT);
       }
+      if (t == 0) H2O_TL(3);
       const unsigned char* sK = stage_base + static_cast<size_t>(s) * Cfg::STAGE;
       const int rows = ok ? min(TILE, nrows - t * TILE) : 0;
       attend_tile<T, D, TILE, ROPE>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lg + t * TILE, lane, rk + t * TILE,
@@ -487,7 +532,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
 #pragma unroll
       for (int e = 0; e < EPV; ++e) myred[4 + lig * EPV + e] = o[e];
     }
+    cp_async_wait<0>();  // this thread's score and position copies have landed
     consumer_sync(NCW * 32);
+    H2O_TL(4);
     if (tid < D) {
       float M = kNeg;
       for (int w = 0; w < NCW; ++w) M = fmaxf(M, red_of(w)[0]);
@@ -528,6 +575,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
   } else {
     __syncthreads();
   }
+  H2O_TL(5);
 
   // the pair's normaliser: merged over the cluster's CTAs, or, for a pair
   // handled by one CTA, this CTA's own (published before the barrier above)
@@ -578,12 +626,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
   }
   // warp minimum, and the slot of the lane that holds it (keys are unique:
   // positions are)
-  unsigned long long wk = kmin;
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    const unsigned long long other = __shfl_xor_sync(0xffffffffu, wk, off);
-    wk = other < wk ? other : wk;
-  }
+  const unsigned long long wk = warp_min_key(kmin);
   const unsigned holder = __ballot_sync(0xffffffffu, kmin == wk && kmin != ~0ull);
   const int wslot = __shfl_sync(0xffffffffu, smin, holder ? __ffs(holder) - 1 : 0);
   if (lane == 0) {
@@ -631,6 +674,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
     u = full ? bslot : count;
   }
   if (full && u < 0 && tid == 0) atomicOr(prm.err, ERR_NO_CANDIDATE);
+  H2O_TL(6);
   // Every byte pushed into this CTA has landed (both waits above) and no CTA
   // reads another's shared memory, so the CTAs of a cluster leave without a
   // cluster barrier.
@@ -667,6 +711,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
     *reinterpret_cast<int4*>(prm.ctr + pair) = make_int4(p + 1, full ? C : count + 1, (head + 1) % R, 0);
     if (prm.evicted) prm.evicted[pair] = full ? u : -1;
   }
+  H2O_TL(7);
 }
 
 // ------------------------------------------------------------ warp per pair
@@ -883,12 +928,7 @@ __global__ void __launch_bounds__(kWarpNW * 32, 1) decode_warp_kernel(const Deco
         }
       }
     }
-    unsigned long long wk = kmin;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xffffffffu, wk, off);
-      wk = other < wk ? other : wk;
-    }
+    const unsigned long long wk = warp_min_key(kmin);
     const unsigned holder = __ballot_sync(0xffffffffu, kmin == wk && kmin != ~0ull);
     const int wslot = __shfl_sync(0xffffffffu, smin, holder ? __ffs(holder) - 1 : 0);
     const int u = fullc ? (holder ? wslot : -1) : count;
@@ -1186,5 +1226,12 @@ cudaError_t launch_decode(const DecodeParams& prm, int dtype, int D, int pairs, 
 }
 
 int decode_threads(int splits) { return (consumer_warps(splits) + 1) * 32; }
+
+#ifdef H2O_DECODE_TIMELINE
+cudaError_t decode_timeline_read(void* dst, size_t bytes) {
+  const size_t n = bytes < sizeof(g_decode_tl) ? bytes : sizeof(g_decode_tl);
+  return cudaMemcpyFromSymbol(dst, g_decode_tl, n);
+}
+#endif
 
 }  // namespace h2o

@@ -48,6 +48,11 @@ struct NvtxRange {
   ~NvtxRange() { nvtxRangePop(); }
 };
 
+#ifdef H2O_DECODE_TIMELINE
+// Profiling build: the stamp buffer the next decode launch writes.
+std::atomic<long long> g_tl_next{0};
+#endif
+
 // Allocation-failure injection (h2o_debug_fail_alloc): the number of device
 // allocations still allowed before the next one fails, or -1 when disarmed.
 std::atomic<long long> g_alloc_budget{-1};
@@ -415,6 +420,9 @@ int h2o_decode_step(h2o_cache* c, const void* q, const void* k_new, const void* 
   dp.rank = c->rank;
   dp.rope = c->rope;
   dp.sp = c->sp;
+#ifdef H2O_DECODE_TIMELINE
+  dp.tl_slot = static_cast<int>(g_tl_next.fetch_add(1) % h2o::kTimelineSlots);
+#endif
   cudaError_t e = h2o::launch_decode(dp, c->dtype, c->D, c->P, splits, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "h2o_decode_step: launch");
   c->host_next_p += 1;
@@ -659,6 +667,20 @@ int h2o_cache_set_position_rolling(h2o_cache* c, float rope_base) {
   c->stages_override = 0;
   return H2O_OK;
 }
+
+#ifdef H2O_DECODE_TIMELINE
+// Profiling build only (not declared in h2o.h): copy the decode time stamps
+// [kTimelineSlots][kTimelineMaxCtas][kTimelineStamps] (uint64 ns) to host
+// memory and report the buffer the next decode launch will write.
+H2O_API int h2o_debug_decode_timeline(void* host_buf, size_t bytes, int* next_slot) {
+  if (!host_buf || !next_slot) return fail(H2O_EINVAL, "h2o_debug_decode_timeline: NULL argument");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = h2o::decode_timeline_read(host_buf, bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "h2o_debug_decode_timeline");
+  *next_slot = static_cast<int>(g_tl_next.load() % h2o::kTimelineSlots);
+  return H2O_OK;
+}
+#endif
 
 int h2o_debug_fail_alloc(int after) {
   if (after < -1) return fail(H2O_EINVAL, "h2o_debug_fail_alloc: after must be >= -1");

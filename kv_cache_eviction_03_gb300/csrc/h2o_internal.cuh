@@ -72,7 +72,21 @@ struct DecodeParams {
   int* rank;           // [P, C]
   const float2* rope;  // [C + 1, D / 2]
   StaticPattern sp;    // protected positions, never eviction candidates
+#ifdef H2O_DECODE_TIMELINE
+  int tl_slot;  // profiling build: which stamp buffer this launch writes
+#endif
 };
+
+#ifdef H2O_DECODE_TIMELINE
+// Profiling build only (compiled with -DH2O_DECODE_TIMELINE): every CTA of a
+// cluster-kernel decode launch records %globaltimer at kTimelineStamps fixed
+// points into buffer tl_slot of a device array; launches take the buffers
+// in turn, so the last kTimelineSlots launches can be read back.
+constexpr int kTimelineSlots = 4;
+constexpr int kTimelineMaxCtas = 4096;
+constexpr int kTimelineStamps = 8;
+cudaError_t decode_timeline_read(void* dst, size_t bytes);
+#endif
 
 struct PrefillParams {
   const void* q;  // [P, L, D]
