@@ -54,6 +54,10 @@ PER_CONFIG_REPS = (2, 5)
 # chunks whose inputs are drawn on the GPU between chunks (outside the timing)
 STREAM_CHUNK = 1024
 STREAM_WINDOW = 10 * 1024
+# shapes whose decode launch is also timed with position rolling on (rotary
+# embedding at in-cache ranks; base 10000), next to the plain launch
+ROLLING = ("opt-6.7b", "llama-7b-16k", "streaming")
+ROPE_BASE = 10000.0
 # oracle samples per workload: (batch rows, heads or None for all, decode steps or None for all)
 ORACLE_SAMPLE = {"tiny-ref": (1, None, None), "opt-6.7b": (4, None, None), "opt-30b": (8, None, None),
                  "llama-7b-16k": (1, 4, None)}
@@ -382,7 +386,29 @@ def measure_decode_shape(name, stream, peak, layers=None, seed=None):
         B.h2o_cache_check(c, stream=stream)
     launches = S * NL * reps
     info = B.h2o_cache_info(caches[0])
+    rolling = None
+    if name in ROLLING:  # same caches, rolling switched on after the prefill (ranks from positions)
+        for c in caches:
+            B.h2o_cache_set_position_rolling(c, ROPE_BASE)
+        with torch.cuda.stream(stream):
+            run(False)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                run(False)
+            for _ in range(warm):
+                g.replay()
+            t_rope = timed_replays(g.replay, stream, reps)
+        for c in caches:
+            B.h2o_cache_check(c, stream=stream)
+        rinfo = B.h2o_cache_info(caches[0])
+        rolling = decode_roofline(w, t_rope / launches * 1e6, peak)
+        rolling = {"us_per_launch": rolling["us_per_launch"], "frac": rolling["frac"],
+                   "vs_plain": t_rope / t_b2b, "launch": {"decode_splits": rinfo[6], "decode_stages": rinfo[7]},
+                   "rope_base": ROPE_BASE}
+        del g
     res = decode_roofline(w, t_b2b / launches * 1e6, peak)
+    if rolling:
+        res["rolling"] = rolling
     iso = decode_roofline(w, max(t_iso - t_fill, 1e-9) / launches * 1e6, peak)
     res["isolated"] = {k: iso[k] for k in ("us_per_launch", "achieved_gbs", "frac", "tokens_per_s_per_layer")}
     res["isolated"]["filler_us"] = t_fill / launches * 1e6
@@ -467,7 +493,24 @@ def measure_streaming(stream, peak, layers=None, seed=None, window=STREAM_WINDOW
         B.h2o_cache_check(c, stream=stream)
     g0 = B.unpack_state(caches[0], B.h2o_cache_export_state(caches[0], stream=stream))
     launches = window * NL
+    # position rolling on the same full caches: one chunk, twice
+    for c in caches:
+        B.h2o_cache_set_position_rolling(c, ROPE_BASE)
+    with torch.cuda.stream(stream):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            run(bufs[0])
+        g.replay()
+        t_rope = timed_replays(g.replay, stream, 2)
+    for c in caches:
+        B.h2o_cache_check(c, stream=stream)
+    rinfo = B.h2o_cache_info(caches[0])
+    del g
     res = decode_roofline(w, dec_s / launches * 1e6, peak)
+    r_us = t_rope / (2 * chunk * NL) * 1e6
+    res["rolling"] = {"us_per_launch": r_us, "frac": decode_roofline(w, r_us, peak)["frac"],
+                      "vs_plain": r_us / res["us_per_launch"], "decode_steps_timed": 2 * chunk,
+                      "launch": {"decode_splits": rinfo[6], "decode_stages": rinfo[7]}, "rope_base": ROPE_BASE}
     info = B.h2o_cache_info(caches[0])
     res.update({"layers": NL, "fill_steps": fill, "decode_steps_timed": window, "launches_timed": launches,
                 "position_after": int(g0["p"][0]), "full_after": bool(np.all(g0["count"] == w.cache_slots)),

@@ -120,18 +120,26 @@ struct DecodeCfg : RowGeom<T, D> {
 // wb to the lanes that weight V.  After the call the warp no longer reads the
 // stage.
 // Position rolling: rotate this lane's EPV/2 element pairs (2i, 2i+1) of a
-// row by the angles whose (cos, sin) sit at `cs` (the row's rank in the
-// table, the lane's pairs), as in the rotary embedding.
-template <int EPV>
-__device__ __forceinline__ void rope_rotate_lane(float (&x)[EPV], const float2* cs) {
+// row by r * theta_i, as in the rotary embedding, composed from the rank's
+// base-16 digits: rotation-table entry 16 * l + d holds (cos, sin) of
+// d * 16^l * theta_i (in shared memory, D/2 float2 per entry in lane order:
+// float4 h * LPR + lig holds this lane's pairs 2h and 2h + 1).
+template <int EPV, int D, int LPR>
+__device__ __forceinline__ void rope_rotate_digits(float (&x)[EPV], const float2* tab, int r, int levels, int lig) {
 #pragma unroll
-  for (int h = 0; h < EPV / 4; ++h) {
-    const float4 t = __ldg(reinterpret_cast<const float4*>(cs) + h);  // (cos, sin) of two pairs
-    const float a0 = x[4 * h], a1 = x[4 * h + 1], b0 = x[4 * h + 2], b1 = x[4 * h + 3];
-    x[4 * h] = a0 * t.x - a1 * t.y;
-    x[4 * h + 1] = a0 * t.y + a1 * t.x;
-    x[4 * h + 2] = b0 * t.z - b1 * t.w;
-    x[4 * h + 3] = b0 * t.w + b1 * t.z;
+  for (int lv = 0; lv < 5; ++lv) {
+    if (lv < levels) {
+      const float4* t = reinterpret_cast<const float4*>(tab + ((lv << 4) + ((r >> (4 * lv)) & 15)) * (D / 2)) + lig;
+#pragma unroll
+      for (int h = 0; h < EPV / 4; ++h) {
+        const float4 c = t[h * LPR];  // (cos, sin) of two pairs
+        const float a0 = x[4 * h], a1 = x[4 * h + 1], b0 = x[4 * h + 2], b1 = x[4 * h + 3];
+        x[4 * h] = a0 * c.x - a1 * c.y;
+        x[4 * h + 1] = a0 * c.y + a1 * c.x;
+        x[4 * h + 2] = b0 * c.z - b1 * c.w;
+        x[4 * h + 3] = b0 * c.w + b1 * c.z;
+      }
+    }
   }
 }
 
@@ -139,7 +147,7 @@ template <typename T, int D, int TILE, bool ROPE = false>
 __device__ __forceinline__ void attend_tile(const unsigned char* sK, const unsigned char* sV, int rows,
                                             const float (&qv)[RowGeom<T, D>::EPV], float& m, float& l,
                                             float (&o)[RowGeom<T, D>::EPV], float* wb, float* lg, int lane,
-                                            const int* rk = nullptr, const float2* rope = nullptr) {
+                                            const int* rk = nullptr, const float2* tab = nullptr, int levels = 0) {
   using Gm = RowGeom<T, D>;
   constexpr int EPV = Gm::EPV, LPR = Gm::LPR, ROWB = Gm::ROWB;
   constexpr int G = Gm::RPI;      // row groups per warp
@@ -155,7 +163,7 @@ __device__ __forceinline__ void attend_tile(const unsigned char* sK, const unsig
     float kf[EPV];
     Vec16<T>::unpack(*reinterpret_cast<const uint4*>(sK + row * ROWB + lig * 16), kf);
     if constexpr (ROPE) {  // key rotated to its rank inside the cache (lg, rk: this stage's rows)
-      if (row < rows) rope_rotate_lane<EPV>(kf, rope + static_cast<size_t>(rk[row]) * (D / 2) + lig * (EPV / 2));
+      if (row < rows) rope_rotate_digits<EPV, D, LPR>(kf, tab, rk[row], levels, lig);
     }
     float a = 0.f;
 #pragma unroll
@@ -261,7 +269,8 @@ struct Layout {
   static constexpr size_t empty = 8 * kMaxStages;              // kMaxStages mbarriers
   static constexpr size_t xbar = 16 * kMaxStages;              // mbarrier: the peers' partials have landed
   static constexpr size_t kbar = xbar + 8;                     // mbarrier: the peers' candidates have landed
-  static constexpr size_t xch = xbar + 16;
+  static constexpr size_t tbar = xbar + 16;                    // mbarrier: the rotation tables have landed
+  static constexpr size_t xch = xbar + 32;
   static constexpr size_t xo = xch + sizeof(Xch);              // this CTA's partial o[D]
   static constexpr size_t gm = (xo + D * 4 + 15) / 16 * 16;    // per-rank partials [16], candidates [16]
   static constexpr size_t blk = gm + 16 * 32;                  // block argmin scratch + counters
@@ -273,8 +282,15 @@ struct Layout {
   __host__ __device__ static size_t rows_in(int nstage, int chunk) {
     return (tail(nstage) + static_cast<size_t>(chunk) * PER_SLOT + 15) / 16 * 16;
   }
-  __host__ __device__ static size_t bytes(int nstage, int chunk, int splits) {
-    return rows_in(nstage, chunk) + (splits > 1 ? static_cast<size_t>(splits - 1) * D * 4 : 0);
+  // after the peers' rows: position rolling's rotation tables
+  __host__ __device__ static size_t tab(int nstage, int chunk, int splits) {
+    return (rows_in(nstage, chunk) + (splits > 1 ? static_cast<size_t>(splits - 1) * D * 4 : 0) + 15) / 16 * 16;
+  }
+  __host__ __device__ static size_t tab_bytes(int entries) {
+    return ROPE ? static_cast<size_t>(entries) * (D / 2) * sizeof(float2) : 0;
+  }
+  __host__ __device__ static size_t bytes(int nstage, int chunk, int splits, int entries) {
+    return tab(nstage, chunk, splits) + tab_bytes(entries);
   }
 };
 
@@ -315,6 +331,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
   uint4* kin = reinterpret_cast<uint4*>(smem + Lay::gm + 256);  // rank r's candidate (key, slot) at [r]
   uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + Lay::xbar);
   uint64_t* kbar = reinterpret_cast<uint64_t*>(smem + Lay::kbar);
+  uint64_t* tbar = reinterpret_cast<uint64_t*>(smem + Lay::tbar);
   unsigned long long* blk_key = reinterpret_cast<unsigned long long*>(smem + Lay::blk);
   int* blk_slot = reinterpret_cast<int*>(blk_key + NW);  // per-warp candidate slot
   int* blk_int = blk_slot + NW;                           // [1..3] p, count, head
@@ -329,6 +346,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
   const int S = static_cast<int>(cluster.num_blocks());
+  float2* rtab = reinterpret_cast<float2*>(smem + Lay::tab(NSTAGE, prm.chunk, S));  // rotation tables (rolling)
   const int pair = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grp = lane / LPR, lig = lane % LPR;
@@ -344,6 +362,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
     }
     mbar_init(xbar, 1);
     mbar_init(kbar, 1);
+    mbar_init(tbar, 1);
     fence_mbar_init();
     if (S > 1) {
       // the bytes the peers will push: (m, l, self) from each, the partial
@@ -368,6 +387,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
   if (warp == NCW) {
     // ---------------------------------------------------------- producer warp
     if (lane == 0) {
+      // position rolling: the rotation tables, constant while rolling is on,
+      // so they are copied before any wait
+      const uint32_t tbytes = static_cast<uint32_t>(Lay::tab_bytes(rope_entries_for(C)));
+      if constexpr (ROPE) {
+        mbar_arrive_expect_tx(tbar, tbytes);
+        bulk_g2s(rtab, prm.rope, tbytes, tbar);
+      }
       // The slot store is read before the grid-dependency wait only when the
       // previous kernel on this stream did not touch this cache.  The pair's
       // count is read before the first copy on purpose: the consumers' small
@@ -404,6 +430,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
       for (int t = max(issued - NSTAGE, 0); t < issued; ++t)
         if (!mbar_wait_bounded(&full_bar[t % NSTAGE], static_cast<uint32_t>((t / NSTAGE) & 1), kWaitLimit))
           atomicOr(prm.err, ERR_RING_TIMEOUT);
+      if constexpr (ROPE)
+        if (!mbar_wait_bounded(tbar, 0u, kWaitLimit)) atomicOr(prm.err, ERR_RING_TIMEOUT);
     }
     __syncwarp();
   } else {
@@ -471,16 +499,15 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
     H2O_TL(2);
     // position rolling: the query (and the new key) sit at rank `count`, after
     // every kept token
-    const float2* rope_cs = nullptr;
     if constexpr (ROPE) {
-      rope_cs = prm.rope + static_cast<size_t>(count) * (D / 2) + lig * (EPV / 2);
-      rope_rotate_lane<EPV>(qv, rope_cs);
+      if (!mbar_wait_bounded(tbar, 0u, kWaitLimit)) atomicOr(prm.err, ERR_MBAR_TIMEOUT);
+      rope_rotate_digits<EPV, D, LPR>(qv, rtab, count, prm.rope_levels, lig);
     }
     if (rank == 0 && warp == 0) {
       // the new token attends to itself: row group 0 of warp 0 starts from it
       float kf[EPV];
       Vec16<T>::unpack(k4, kf);
-      if constexpr (ROPE) rope_rotate_lane<EPV>(kf, rope_cs);
+      if constexpr (ROPE) rope_rotate_digits<EPV, D, LPR>(kf, rtab, count, prm.rope_levels, lig);
       float acc = 0.f;
 #pragma unroll
       for (int e = 0; e < EPV; ++e) acc = fmaf(qv[e], kf[e], acc);
@@ -512,7 +539,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
       const unsigned char* sK = stage_base + static_cast<size_t>(s) * Cfg::STAGE;
       const int rows = ok ? min(TILE, nrows - t * TILE) : 0;
       attend_tile<T, D, TILE, ROPE>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lg + t * TILE, lane, rk + t * TILE,
-                                    prm.rope);
+                                    rtab, prm.rope_levels);
       // stage s may be refilled; after a timeout the stage is not released,
       // so no new copy can target memory an unfinished copy still writes
       if (lane == 0 && ok) mbar_arrive(&empty_bar[s]);
@@ -1006,12 +1033,15 @@ struct Kern {
   using Lay = Layout<D, NCW, TILE, Cfg::STAGE, ROPE>;
   static constexpr auto fn = decode_kernel<T, D, NCW, TILE, ROPE>;
 
-  static size_t smem(int nstage, int chunk, int splits) { return Lay::bytes(nstage, chunk, splits); }
+  // entries: position rolling's rotation-table entries (0 when off)
+  static size_t smem(int nstage, int chunk, int splits, int entries) {
+    return Lay::bytes(nstage, chunk, splits, entries);
+  }
 
   static cudaError_t attrs() {
     // raised once for the largest configuration, so later launches (also
     // inside stream capture) make no attribute calls
-    size_t most = Lay::bytes(kMaxStages, kMaxChunk, 16);
+    size_t most = Lay::bytes(kMaxStages, kMaxChunk, 16, rope_entries_for(65536));
     if (most > 227 * 1024) most = 227 * 1024;
     return kernel_attrs(reinterpret_cast<const void*>(fn), most, true);
   }
@@ -1022,7 +1052,7 @@ struct Kern {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(splits, pairs, 1);
     cfg.blockDim = dim3(Cfg::NT, 1, 1);
-    cfg.dynamicSmemBytes = smem(prm.nstage, prm.chunk, splits);
+    cfg.dynamicSmemBytes = smem(prm.nstage, prm.chunk, splits, prm.rope ? rope_entries_for(prm.C) : 0);
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1037,9 +1067,9 @@ struct Kern {
   }
 
   // CTAs that can be resident at once for this shape (0 = cannot launch)
-  static int resident(int splits, int nstage, int chunk, int pairs, int sms) {
+  static int resident(int splits, int nstage, int chunk, int pairs, int sms, int entries) {
     if (attrs() != cudaSuccess) return 0;
-    const size_t bytes = smem(nstage, chunk, splits);
+    const size_t bytes = smem(nstage, chunk, splits, entries);
     if (bytes > 227 * 1024) return 0;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, Cfg::NT, bytes) != cudaSuccess) return 0;
@@ -1101,10 +1131,11 @@ int device_sms() {
   return sms;
 }
 
-int decode_resident(int dtype, int D, int splits, int nstage, int chunk, int pairs, bool rope) {
+int decode_resident(int dtype, int D, int splits, int nstage, int chunk, int pairs, int rope_entries) {
   const int sms = device_sms();
-  const int r =
-      dispatch(dtype, D, splits, rope, [&](auto k) { return decltype(k)::resident(splits, nstage, chunk, pairs, sms); });
+  const int r = dispatch(dtype, D, splits, rope_entries > 0, [&](auto k) {
+    return decltype(k)::resident(splits, nstage, chunk, pairs, sms, rope_entries);
+  });
   cudaGetLastError();
   return r;
 }
@@ -1156,7 +1187,7 @@ DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C, bool rope) {
   if (ctas <= 2LL * sms) {
     const int ch = chunk_for(C, sh.splits);
     for (int st : {12, ncw == 6 ? 6 : 8}) {
-      const int res = decode_resident(dtype, D, sh.splits, st, ch, pairs, rope);
+      const int res = decode_resident(dtype, D, sh.splits, st, ch, pairs, rope ? rope_entries_for(C) : 0);
       if (res >= 2 * sms || static_cast<long long>(res) >= ctas) {
         sh.stages = st;
         break;
@@ -1220,7 +1251,9 @@ cudaError_t launch_decode(const DecodeParams& prm, int dtype, int D, int pairs, 
     if (dtype == 1 && D == 128) return WarpKern<float, 128>::launch(prm, ctas, s);
     return WarpKern<float, 64>::launch(prm, ctas, s);
   }
-  if (prm.rope != nullptr && prm.rank == nullptr) return cudaErrorInvalidValue;
+  if (prm.rope != nullptr && (prm.rank == nullptr || prm.rope_levels < 1 || prm.rope_levels > 5 ||
+                              (1LL << (4 * prm.rope_levels)) <= prm.C))
+    return cudaErrorInvalidValue;
   return dispatch(dtype, D, splits, prm.rope != nullptr,
                   [&](auto k) { return decltype(k)::launch(prm, pairs, splits, s); });
 }

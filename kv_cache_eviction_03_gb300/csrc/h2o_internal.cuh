@@ -36,6 +36,20 @@ __host__ __device__ __forceinline__ bool is_protected(const StaticPattern& sp, i
   return k < sp.count && k * sp.stride == d;
 }
 
+// Position rolling: base-16 digits that every rank 0..max_rank needs (at
+// most 5, for ranks up to 65536), and the rotation-table entries they take:
+// 16 per level below the top one, and only as many as the top digit reaches
+// on the top level.
+__host__ __device__ __forceinline__ int rope_levels_for(int max_rank) {
+  int l = 1;
+  while (l < 5 && (1 << (4 * l)) <= max_rank) ++l;
+  return l;
+}
+__host__ __device__ __forceinline__ int rope_entries_for(int max_rank) {
+  const int l = rope_levels_for(max_rank);
+  return 16 * (l - 1) + (max_rank >> (4 * (l - 1))) + 1;
+}
+
 // Per-pair counters kept on the device so decode steps can be replayed from
 // a CUDA graph: next absolute position, occupied slots, ring head.
 struct PairCtr {
@@ -68,9 +82,14 @@ struct DecodeParams {
   int pairs;          // P
   // position rolling (rotary embedding at positions inside the cache), or
   // both nullptr: the rank of each slot among the kept tokens in text order,
-  // and cos / sin of rank * base^(-2i/D) for ranks 0..C and pairs i < D/2
+  // and the rotation tables of the ranks' base-16 digits: entry 16 * l + d
+  // holds (cos, sin) of d * 16^l * base^(-2i/D) for every pair i < D/2, in
+  // lane order (float4 h * LPR + g holds pairs g * EPV/2 + 2h and + 2h + 1,
+  // where a row's LPR lanes take EPV elements each), so that the lanes of a
+  // row read consecutive 16-byte words
   int* rank;           // [P, C]
-  const float2* rope;  // [C + 1, D / 2]
+  const float2* rope;  // [rope_entries_for(C), D / 2]
+  int rope_levels;     // base-16 digits of the largest rank, C (rope_levels_for)
   StaticPattern sp;    // protected positions, never eviction candidates
 #ifdef H2O_DECODE_TIMELINE
   int tl_slot;  // profiling build: which stamp buffer this launch writes
@@ -158,8 +177,9 @@ struct DecodeShape {
 // rope: the cache uses position rolling (cluster kernel only, one more int
 // of shared memory per slot)
 DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C, bool rope = false);
-// CTAs of this shape that fit on the device at once (0: cannot launch)
-int decode_resident(int dtype, int D, int splits, int nstage, int chunk, int pairs, bool rope = false);
+// CTAs of this shape that fit on the device at once (0: cannot launch);
+// rope_entries: position rolling's rotation-table entries, 0 when off
+int decode_resident(int dtype, int D, int splits, int nstage, int chunk, int pairs, int rope_entries = 0);
 int decode_chunk(int C, int splits);
 int decode_max_stages();
 int decode_stage_multiple(int splits);  // ring depths for this cluster size must be multiples of this
@@ -207,8 +227,8 @@ struct h2o_cache {
   int splits_override, stages_override;
   h2o::DecodeShape shape_auto;
   long long host_next_p;  // host mirror of the next position (overflow check)
-  // position rolling: slot ranks [P, C] and the (cos, sin) table [C + 1, D/2];
-  // nullptr when off
+  // position rolling: slot ranks [P, C] and the digit rotation tables
+  // [rope_levels_for(C), 16, D/2]; nullptr when off
   int* rank;
   float2* rope;
   float rope_base;

@@ -46,7 +46,8 @@ def load_timeline_build():
     return B, fn
 
 
-def run(workload: str, layers: int | None, steps: int, splits: int = 0, stages: int = 0, isolated: bool = False):
+def run(workload: str, layers: int | None, steps: int, splits: int = 0, stages: int = 0, isolated: bool = False,
+        rolling: float = 0.0):
     import torch
 
     B, read = load_timeline_build()
@@ -66,6 +67,11 @@ def run(workload: str, layers: int | None, steps: int, splits: int = 0, stages: 
         else:  # streaming shape: fill the cache first (eager), then time evicting steps
             B.h2o_cache_reset(c, stream=stream)
         caches.append(c)
+    if rolling > 0:  # position rolling, switched on after the prefill (ranks from positions)
+        for c in caches:
+            B.h2o_cache_set_position_rolling(c, rolling)
+            if splits or stages:
+                B.h2o_cache_set_decode_shape(c, splits, stages)
     info = B.h2o_cache_info(caches[0])
     if info[6] < 1:
         raise SystemExit("the timeline covers the cluster kernel only; this shape runs warp per pair")
@@ -133,10 +139,12 @@ def main():
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--stages", type=int, default=0)
     ap.add_argument("--isolated", action="store_true", help="a plain kernel between decode launches")
+    ap.add_argument("--rolling", type=float, default=0.0, help="position rolling with this rotary base (0: off)")
     a = ap.parse_args()
-    w, NL, info, grid, stamps = run(a.workload, a.layers, a.steps, a.splits, a.stages, a.isolated)
+    w, NL, info, grid, stamps = run(a.workload, a.layers, a.steps, a.splits, a.stages, a.isolated, a.rolling)
     print(f"workload {w.name}: {NL} layer caches, {w.pairs} pairs x {info[6]} CTAs = {grid} CTAs per launch, "
-          f"{info[7]} stages, {info[8]} threads{', isolated launches' if a.isolated else ''}")
+          f"{info[7]} stages, {info[8]} threads{', isolated launches' if a.isolated else ''}"
+          f"{f', position rolling (base {a.rolling:g})' if a.rolling else ''}")
     print("times in us after the previous launch's last CTA exit: median over CTAs / latest CTA")
     rows = phase_table(stamps)
     print("| stamp | " + " | ".join(f"launch {i + 1}" for i in range(len(rows))) + " |")
