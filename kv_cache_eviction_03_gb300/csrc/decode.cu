@@ -123,31 +123,38 @@ struct DecodeCfg : RowGeom<T, D> {
 // row by r * theta_i, as in the rotary embedding, composed from the rank's
 // base-16 digits: rotation-table entry 16 * l + d holds (cos, sin) of
 // d * 16^l * theta_i (in shared memory, D/2 float2 per entry in lane order:
-// float4 h * LPR + lig holds this lane's pairs 2h and 2h + 1).
+// float4 h * LPR + lig holds this lane's pairs 2h and 2h + 1).  Levels
+// LV0..LV1-1 of the rank, or LV0..levels-1 when LV1 is 0.
+template <int EPV, int D, int LPR>
+__device__ __forceinline__ void rope_rotate_level(float (&x)[EPV], const float2* tab, int entry, int lig) {
+  const float4* t = reinterpret_cast<const float4*>(tab + entry * (D / 2)) + lig;
+#pragma unroll
+  for (int h = 0; h < EPV / 4; ++h) {
+    const float4 c = t[h * LPR];  // (cos, sin) of two pairs
+    const float a0 = x[4 * h], a1 = x[4 * h + 1], b0 = x[4 * h + 2], b1 = x[4 * h + 3];
+    x[4 * h] = a0 * c.x - a1 * c.y;
+    x[4 * h + 1] = a0 * c.y + a1 * c.x;
+    x[4 * h + 2] = b0 * c.z - b1 * c.w;
+    x[4 * h + 3] = b0 * c.w + b1 * c.z;
+  }
+}
 template <int EPV, int D, int LPR>
 __device__ __forceinline__ void rope_rotate_digits(float (&x)[EPV], const float2* tab, int r, int levels, int lig) {
 #pragma unroll
-  for (int lv = 0; lv < 5; ++lv) {
-    if (lv < levels) {
-      const float4* t = reinterpret_cast<const float4*>(tab + ((lv << 4) + ((r >> (4 * lv)) & 15)) * (D / 2)) + lig;
-#pragma unroll
-      for (int h = 0; h < EPV / 4; ++h) {
-        const float4 c = t[h * LPR];  // (cos, sin) of two pairs
-        const float a0 = x[4 * h], a1 = x[4 * h + 1], b0 = x[4 * h + 2], b1 = x[4 * h + 3];
-        x[4 * h] = a0 * c.x - a1 * c.y;
-        x[4 * h + 1] = a0 * c.y + a1 * c.x;
-        x[4 * h + 2] = b0 * c.z - b1 * c.w;
-        x[4 * h + 3] = b0 * c.w + b1 * c.z;
-      }
-    }
-  }
+  for (int lv = 0; lv < 5; ++lv)
+    if (lv < levels) rope_rotate_level<EPV, D, LPR>(x, tab, (lv << 4) + ((r >> (4 * lv)) & 15), lig);
 }
 
-template <typename T, int D, int TILE, bool ROPE = false>
+// Position rolling (ROPE): the logit of a key at rank r is
+// Re sum_i conj(Q_i) T0[r & 15]_i K'_i over the lane's pairs as complex
+// numbers, Q the rotated query, T0 the level-0 table and K' the key rotated
+// by the rank's higher digits (KL levels): tab's level-0 entries then hold
+// P0[d] = conj(Q) T0[d], built once per step, so a key takes KL rotations.
+template <typename T, int D, int TILE, bool ROPE = false, int KL = 0>
 __device__ __forceinline__ void attend_tile(const unsigned char* sK, const unsigned char* sV, int rows,
                                             const float (&qv)[RowGeom<T, D>::EPV], float& m, float& l,
                                             float (&o)[RowGeom<T, D>::EPV], float* wb, float* lg, int lane,
-                                            const int* rk = nullptr, const float2* tab = nullptr, int levels = 0) {
+                                            const int* rk = nullptr, const float2* tab = nullptr) {
   using Gm = RowGeom<T, D>;
   constexpr int EPV = Gm::EPV, LPR = Gm::LPR, ROWB = Gm::ROWB;
   constexpr int G = Gm::RPI;      // row groups per warp
@@ -162,12 +169,25 @@ __device__ __forceinline__ void attend_tile(const unsigned char* sK, const unsig
     const int row = grp * RG + r;
     float kf[EPV];
     Vec16<T>::unpack(*reinterpret_cast<const uint4*>(sK + row * ROWB + lig * 16), kf);
-    if constexpr (ROPE) {  // key rotated to its rank inside the cache (lg, rk: this stage's rows)
-      if (row < rows) rope_rotate_digits<EPV, D, LPR>(kf, tab, rk[row], levels, lig);
-    }
     float a = 0.f;
+    if constexpr (ROPE) {  // key rotated to its rank inside the cache (rk: this stage's ranks)
+      const int rr = row < rows ? rk[row] : 0;
 #pragma unroll
-    for (int e = 0; e < EPV; ++e) a = fmaf(qv[e], kf[e], a);
+      for (int lv = 1; lv <= KL; ++lv)
+        rope_rotate_level<EPV, D, LPR>(kf, tab, (lv << 4) + ((rr >> (4 * lv)) & 15), lig);
+      const float4* z = reinterpret_cast<const float4*>(tab + (rr & 15) * (D / 2)) + lig;  // P0[d0]
+#pragma unroll
+      for (int h = 0; h < EPV / 4; ++h) {
+        const float4 c = z[h * LPR];
+        a = fmaf(c.x, kf[4 * h], a);
+        a = fmaf(-c.y, kf[4 * h + 1], a);
+        a = fmaf(c.z, kf[4 * h + 2], a);
+        a = fmaf(-c.w, kf[4 * h + 3], a);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) a = fmaf(qv[e], kf[e], a);
+    }
     acc[r] = row < rows ? a : 0.f;
   }
   // butterfly: halve the rows held per lane at each step
@@ -527,7 +547,25 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
     // prefetch now; triggering only after this step's inputs are loaded keeps
     // those small loads ahead of the next step's bulk traffic.
     griddep_launch();
-    if constexpr (ROPE) consumer_sync(NCW * 32);  // every rank in rk[] is in place
+    if constexpr (ROPE) {
+      // every rank in rk[] is in place, and every read of the level-0 table
+      // (query, new key) is done: the level-0 entries become
+      // P0[d] = conj(Q) T0[d], digit d built by row group (warp * G + grp)
+      // when d is congruent to it modulo the consumers' row groups
+      consumer_sync(NCW * 32);
+      constexpr int NG = NCW * Cfg::RPI;
+      for (int d = warp * Cfg::RPI + grp; d < 16; d += NG) {
+        float4* e = reinterpret_cast<float4*>(rtab + d * (D / 2)) + lig;
+#pragma unroll
+        for (int h = 0; h < EPV / 4; ++h) {
+          const float4 c = e[h * LPR];
+          const float qa = qv[4 * h], qb = qv[4 * h + 1], qc = qv[4 * h + 2], qd = qv[4 * h + 3];
+          // conj(qa + i qb) (c.x + i c.y) and conj(qc + i qd) (c.z + i c.w)
+          e[h * LPR] = make_float4(qa * c.x + qb * c.y, qa * c.y - qb * c.x, qc * c.z + qd * c.w, qc * c.w - qd * c.z);
+        }
+      }
+      consumer_sync(NCW * 32);
+    }
     bool ok = true;
     for (int t = warp; t < ntiles; t += NCW) {
       const int s = t % NSTAGE;
@@ -538,8 +576,19 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
       if (t == 0) H2O_TL(3);
       const unsigned char* sK = stage_base + static_cast<size_t>(s) * Cfg::STAGE;
       const int rows = ok ? min(TILE, nrows - t * TILE) : 0;
-      attend_tile<T, D, TILE, ROPE>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lg + t * TILE, lane, rk + t * TILE,
-                                    rtab, prm.rope_levels);
+      if constexpr (ROPE) {
+        const int* rks = rk + t * TILE;
+        float* lgs = lg + t * TILE;
+        switch (prm.rope_levels) {  // key-side rotations: the digits above the lowest
+          case 1: attend_tile<T, D, TILE, true, 0>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab); break;
+          case 2: attend_tile<T, D, TILE, true, 1>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab); break;
+          case 3: attend_tile<T, D, TILE, true, 2>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab); break;
+          case 4: attend_tile<T, D, TILE, true, 3>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab); break;
+          default: attend_tile<T, D, TILE, true, 4>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab); break;
+        }
+      } else {
+        attend_tile<T, D, TILE>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lg + t * TILE, lane);
+      }
       // stage s may be refilled; after a timeout the stage is not released,
       // so no new copy can target memory an unfinished copy still writes
       if (lane == 0 && ok) mbar_arrive(&empty_bar[s]);
