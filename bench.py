@@ -84,6 +84,8 @@ def parse():
                     help="comma-separated workloads measured under per_config")
     ap.add_argument("--only-per-config", default=None,
                     help="profiling aid: measure this one workload's decode launch and print it, nothing else")
+    ap.add_argument("--stream-window", type=int, default=STREAM_WINDOW,
+                    help="steady-state decode steps timed on the streaming shape (a multiple of 1024)")
     ap.add_argument("--decode-only", action="store_true", help="profiling aid: replay only the decode graph")
     return ap.parse_args()
 
@@ -527,12 +529,12 @@ def measure_streaming(stream, peak, layers=None, seed=None, window=STREAM_WINDOW
     return res
 
 
-def run_per_config(names, stream, peak, oracle=None, layers=None, seed=None):
+def run_per_config(names, stream, peak, oracle=None, layers=None, seed=None, stream_window=STREAM_WINDOW):
     res = {}
     for name in names:
         w = W.WORKLOADS[name]
         if name == "streaming":
-            r = measure_streaming(stream, peak, layers=layers, seed=seed)
+            r = measure_streaming(stream, peak, layers=layers, seed=seed, window=stream_window)
         else:
             r = measure_decode_shape(name, stream, peak, layers=layers, seed=seed)
         r["workload"] = describe(w)
@@ -704,7 +706,8 @@ def run_ours(args, rank, world, local_rank):
     # ---- the decode launch in isolation, and every other workload shape
     if rank == 0 and world == 1 and not args.no_per_config:
         names = [n for n in args.per_config.split(",") if n]
-        pc = run_per_config(names, stream, peak, oracle=args.oracle_per_config, seed=args.seed)
+        pc = run_per_config(names, stream, peak, oracle=args.oracle_per_config, seed=args.seed,
+                            stream_window=args.stream_window)
         result["per_config"] = pc
         if args.config in pc:
             result["roofline"]["isolated"] = dict(pc[args.config]["isolated"],
@@ -843,7 +846,8 @@ def main():
         torch.cuda.set_device(local_rank)
         stream = torch.cuda.Stream()
         peak, _ = measured_peak()
-        pc = run_per_config([args.only_per_config], stream, peak, layers=args.layers, seed=args.seed)
+        pc = run_per_config([args.only_per_config], stream, peak, layers=args.layers, seed=args.seed,
+                            stream_window=args.stream_window)
         print(json.dumps({"per_config": pc}))
         return
     if args.impl == "reference":
