@@ -415,18 +415,32 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
         bulk_g2s(rtab, prm.rope, tbytes, tbar);
       }
       // The slot store is read before the grid-dependency wait only when the
-      // previous kernel on this stream did not touch this cache.  The pair's
-      // count is read before the first copy on purpose: the consumers' small
-      // loads go out first instead of queueing behind the ring's bulk reads.
-      if (!prm.prefetch) griddep_wait();
-      const int cnt = prm.ctr[pair].count;
-      const int nrows = max(min(lo + prm.chunk, cnt) - lo, 0);
-      const int ntiles = (nrows + TILE - 1) / TILE;
+      // previous kernel on this stream did not touch this cache.  Then the
+      // first tile of the CTA's slot range is requested at once, before the
+      // pair's count is known (a full cache uses it; rows past the count are
+      // never read), so the first stage does not wait for that load.  The
+      // rest follows the count: a whole ring requested that early would put
+      // the consumers' small loads behind megabytes of bulk reads.
       const unsigned char* gK = static_cast<const unsigned char*>(prm.K) + slot0 * ROWB;
       const unsigned char* gV = static_cast<const unsigned char*>(prm.V) + slot0 * ROWB;
       const uint64_t policy = policy_evict_first();
-      int issued = 0;
-      for (int t = 0; t < ntiles; ++t) {
+      int issued = 0, rows0 = 0;
+      if (prm.prefetch) {
+        rows0 = min(TILE, max(min(lo + prm.chunk, C) - lo, 0));  // inside the pair's slots
+        if (rows0 > 0) {
+          const uint32_t bytes = static_cast<uint32_t>(rows0 * ROWB);
+          mbar_arrive_expect_tx(&full_bar[0], 2 * bytes);
+          bulk_g2s_stream(stage_base, gK, bytes, &full_bar[0], policy);
+          bulk_g2s_stream(stage_base + TILE * ROWB, gV, bytes, &full_bar[0], policy);
+          issued = 1;
+        }
+      } else {
+        griddep_wait();
+      }
+      const int cnt = prm.ctr[pair].count;
+      const int nrows = max(min(lo + prm.chunk, cnt) - lo, 0);
+      const int ntiles = (nrows + TILE - 1) / TILE;
+      for (int t = issued; t < ntiles; ++t) {
         const int s = t % NSTAGE, k = t / NSTAGE;
         // stages are only released once the consumers are past the
         // grid-dependency wait, whose length depends on earlier kernels: wait
