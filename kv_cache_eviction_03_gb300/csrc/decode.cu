@@ -121,10 +121,9 @@ struct DecodeCfg : RowGeom<T, D> {
 // stage.
 // Position rolling: rotate this lane's EPV/2 element pairs (2i, 2i+1) of a
 // row by r * theta_i, as in the rotary embedding, composed from the rank's
-// base-16 digits: rotation-table entry 16 * l + d holds (cos, sin) of
-// d * 16^l * theta_i (in shared memory, D/2 float2 per entry in lane order:
-// float4 h * LPR + lig holds this lane's pairs 2h and 2h + 1).  Levels
-// LV0..LV1-1 of the rank, or LV0..levels-1 when LV1 is 0.
+// digits: the rotation-table entry of level l's digit (rope_entry) holds
+// (cos, sin) of the digit's angle (in shared memory, D/2 float2 per entry in
+// lane order: float4 h * LPR + lig holds this lane's pairs 2h and 2h + 1).
 template <int EPV, int D, int LPR>
 __device__ __forceinline__ void rope_rotate_level(float (&x)[EPV], const float2* tab, int entry, int lig) {
   const float4* t = reinterpret_cast<const float4*>(tab + entry * (D / 2)) + lig;
@@ -139,14 +138,15 @@ __device__ __forceinline__ void rope_rotate_level(float (&x)[EPV], const float2*
   }
 }
 template <int EPV, int D, int LPR>
-__device__ __forceinline__ void rope_rotate_digits(float (&x)[EPV], const float2* tab, int r, int levels, int lig) {
+__device__ __forceinline__ void rope_rotate_digits(float (&x)[EPV], const float2* tab, int r, int levels, int low,
+                                                   int lig) {
 #pragma unroll
-  for (int lv = 0; lv < 5; ++lv)
-    if (lv < levels) rope_rotate_level<EPV, D, LPR>(x, tab, (lv << 4) + ((r >> (4 * lv)) & 15), lig);
+  for (int lv = 0; lv < 6; ++lv)
+    if (lv < levels) rope_rotate_level<EPV, D, LPR>(x, tab, rope_entry(r, lv, low), lig);
 }
 
 // Position rolling (ROPE): the logit of a key at rank r is
-// Re sum_i conj(Q_i) T0[r & 15]_i K'_i over the lane's pairs as complex
+// Re sum_i conj(Q_i) T0[lowest digit of r]_i K'_i over the lane's pairs as complex
 // numbers, Q the rotated query, T0 the level-0 table and K' the key rotated
 // by the rank's higher digits (KL levels): tab's level-0 entries then hold
 // P0[d] = conj(Q) T0[d], built once per step, so a key takes KL rotations.
@@ -154,7 +154,7 @@ template <typename T, int D, int TILE, bool ROPE = false, int KL = 0>
 __device__ __forceinline__ void attend_tile(const unsigned char* sK, const unsigned char* sV, int rows,
                                             const float (&qv)[RowGeom<T, D>::EPV], float& m, float& l,
                                             float (&o)[RowGeom<T, D>::EPV], float* wb, float* lg, int lane,
-                                            const int* rk = nullptr, const float2* tab = nullptr) {
+                                            const int* rk = nullptr, const float2* tab = nullptr, int low = 4) {
   using Gm = RowGeom<T, D>;
   constexpr int EPV = Gm::EPV, LPR = Gm::LPR, ROWB = Gm::ROWB;
   constexpr int G = Gm::RPI;      // row groups per warp
@@ -173,9 +173,8 @@ __device__ __forceinline__ void attend_tile(const unsigned char* sK, const unsig
     if constexpr (ROPE) {  // key rotated to its rank inside the cache (rk: this stage's ranks)
       const int rr = row < rows ? rk[row] : 0;
 #pragma unroll
-      for (int lv = 1; lv <= KL; ++lv)
-        rope_rotate_level<EPV, D, LPR>(kf, tab, (lv << 4) + ((rr >> (4 * lv)) & 15), lig);
-      const float4* z = reinterpret_cast<const float4*>(tab + (rr & 15) * (D / 2)) + lig;  // P0[d0]
+      for (int lv = 1; lv <= KL; ++lv) rope_rotate_level<EPV, D, LPR>(kf, tab, rope_entry(rr, lv, low), lig);
+      const float4* z = reinterpret_cast<const float4*>(tab + rope_entry(rr, 0, low) * (D / 2)) + lig;  // P0[d0]
 #pragma unroll
       for (int h = 0; h < EPV / 4; ++h) {
         const float4 c = z[h * LPR];
@@ -409,7 +408,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
     if (lane == 0) {
       // position rolling: the rotation tables, constant while rolling is on,
       // so they are copied before any wait
-      const uint32_t tbytes = static_cast<uint32_t>(Lay::tab_bytes(rope_entries_for(C)));
+      const uint32_t tbytes = static_cast<uint32_t>(Lay::tab_bytes(rope_entries_for(C, prm.rope_low_bits)));
       if constexpr (ROPE) {
         mbar_arrive_expect_tx(tbar, tbytes);
         bulk_g2s(rtab, prm.rope, tbytes, tbar);
@@ -535,13 +534,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
     // every kept token
     if constexpr (ROPE) {
       if (!mbar_wait_bounded(tbar, 0u, kWaitLimit)) atomicOr(prm.err, ERR_MBAR_TIMEOUT);
-      rope_rotate_digits<EPV, D, LPR>(qv, rtab, count, prm.rope_levels, lig);
+      rope_rotate_digits<EPV, D, LPR>(qv, rtab, count, prm.rope_levels, prm.rope_low_bits, lig);
     }
     if (rank == 0 && warp == 0) {
       // the new token attends to itself: row group 0 of warp 0 starts from it
       float kf[EPV];
       Vec16<T>::unpack(k4, kf);
-      if constexpr (ROPE) rope_rotate_digits<EPV, D, LPR>(kf, rtab, count, prm.rope_levels, lig);
+      if constexpr (ROPE) rope_rotate_digits<EPV, D, LPR>(kf, rtab, count, prm.rope_levels, prm.rope_low_bits, lig);
       float acc = 0.f;
 #pragma unroll
       for (int e = 0; e < EPV; ++e) acc = fmaf(qv[e], kf[e], acc);
@@ -568,7 +567,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
       // when d is congruent to it modulo the consumers' row groups
       consumer_sync(NCW * 32);
       constexpr int NG = NCW * Cfg::RPI;
-      for (int d = warp * Cfg::RPI + grp; d < 16; d += NG) {
+      const int n0 = prm.rope_levels > 1 ? 1 << prm.rope_low_bits : C + 1;  // level-0 entries
+      for (int d = warp * Cfg::RPI + grp; d < n0; d += NG) {
         float4* e = reinterpret_cast<float4*>(rtab + d * (D / 2)) + lig;
 #pragma unroll
         for (int h = 0; h < EPV / 4; ++h) {
@@ -593,12 +593,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
       if constexpr (ROPE) {
         const int* rks = rk + t * TILE;
         float* lgs = lg + t * TILE;
+        const int low = prm.rope_low_bits;
         switch (prm.rope_levels) {  // key-side rotations: the digits above the lowest
-          case 1: attend_tile<T, D, TILE, true, 0>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab); break;
-          case 2: attend_tile<T, D, TILE, true, 1>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab); break;
-          case 3: attend_tile<T, D, TILE, true, 2>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab); break;
-          case 4: attend_tile<T, D, TILE, true, 3>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab); break;
-          default: attend_tile<T, D, TILE, true, 4>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab); break;
+          case 1: attend_tile<T, D, TILE, true, 0>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low); break;
+          case 2: attend_tile<T, D, TILE, true, 1>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low); break;
+          case 3: attend_tile<T, D, TILE, true, 2>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low); break;
+          case 4: attend_tile<T, D, TILE, true, 3>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low); break;
+          default: attend_tile<T, D, TILE, true, 4>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low); break;
         }
       } else {
         attend_tile<T, D, TILE>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lg + t * TILE, lane);
@@ -1104,7 +1105,7 @@ struct Kern {
   static cudaError_t attrs() {
     // raised once for the largest configuration, so later launches (also
     // inside stream capture) make no attribute calls
-    size_t most = Lay::bytes(kMaxStages, kMaxChunk, 16, rope_entries_for(65536));
+    size_t most = Lay::bytes(kMaxStages, kMaxChunk, 16, rope_entries_for(65536, rope_low_bits_for(65536)));
     if (most > 227 * 1024) most = 227 * 1024;
     return kernel_attrs(reinterpret_cast<const void*>(fn), most, true);
   }
@@ -1115,7 +1116,8 @@ struct Kern {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(splits, pairs, 1);
     cfg.blockDim = dim3(Cfg::NT, 1, 1);
-    cfg.dynamicSmemBytes = smem(prm.nstage, prm.chunk, splits, prm.rope ? rope_entries_for(prm.C) : 0);
+    cfg.dynamicSmemBytes =
+        smem(prm.nstage, prm.chunk, splits, prm.rope ? rope_entries_for(prm.C, prm.rope_low_bits) : 0);
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1250,7 +1252,8 @@ DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C, bool rope) {
   if (ctas <= 2LL * sms) {
     const int ch = chunk_for(C, sh.splits);
     for (int st : {12, ncw == 6 ? 6 : 8}) {
-      const int res = decode_resident(dtype, D, sh.splits, st, ch, pairs, rope ? rope_entries_for(C) : 0);
+      const int res =
+          decode_resident(dtype, D, sh.splits, st, ch, pairs, rope ? rope_entries_for(C, rope_low_bits_for(C)) : 0);
       if (res >= 2 * sms || static_cast<long long>(res) >= ctas) {
         sh.stages = st;
         break;
@@ -1314,8 +1317,9 @@ cudaError_t launch_decode(const DecodeParams& prm, int dtype, int D, int pairs, 
     if (dtype == 1 && D == 128) return WarpKern<float, 128>::launch(prm, ctas, s);
     return WarpKern<float, 64>::launch(prm, ctas, s);
   }
-  if (prm.rope != nullptr && (prm.rank == nullptr || prm.rope_levels < 1 || prm.rope_levels > 5 ||
-                              (1LL << (4 * prm.rope_levels)) <= prm.C))
+  if (prm.rope != nullptr &&
+      (prm.rank == nullptr || (prm.rope_low_bits != 4 && prm.rope_low_bits != 5) ||
+       prm.rope_levels != rope_levels_for(prm.C, prm.rope_low_bits) || prm.rope_levels > 5))
     return cudaErrorInvalidValue;
   return dispatch(dtype, D, splits, prm.rope != nullptr,
                   [&](auto k) { return decltype(k)::launch(prm, pairs, splits, s); });

@@ -419,7 +419,8 @@ int h2o_decode_step(h2o_cache* c, const void* q, const void* k_new, const void* 
   dp.pairs = c->P;
   dp.rank = c->rank;
   dp.rope = c->rope;
-  dp.rope_levels = c->rope ? h2o::rope_levels_for(c->C) : 0;
+  dp.rope_low_bits = h2o::rope_low_bits_for(c->C);
+  dp.rope_levels = c->rope ? h2o::rope_levels_for(c->C, dp.rope_low_bits) : 0;
   dp.sp = c->sp;
 #ifdef H2O_DECODE_TIMELINE
   dp.tl_slot = static_cast<int>(g_tl_next.fetch_add(1) % h2o::kTimelineSlots);
@@ -576,7 +577,7 @@ int h2o_cache_set_decode_shape(h2o_cache* c, int splits, int stages) {
       return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: %d splits leave more than %d slots per CTA", s,
                   h2o::decode_max_chunk());
     if (h2o::decode_resident(c->dtype, c->D, s, n, chunk_for(c->C, s), c->P,
-                             c->rope ? h2o::rope_entries_for(c->C) : 0) < s)
+                             c->rope ? h2o::rope_entries_for(c->C, h2o::rope_low_bits_for(c->C)) : 0) < s)
       return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: %d CTAs per pair with %d stages cannot be scheduled", s,
                   n);
   }
@@ -629,7 +630,9 @@ int h2o_cache_set_position_rolling(h2o_cache* c, float rope_base) {
     return H2O_OK;
   }
   const size_t nslot = static_cast<size_t>(c->P) * c->C;
-  const int entries = h2o::rope_entries_for(c->C);  // table entries the ranks' base-16 digits take
+  const int low = h2o::rope_low_bits_for(c->C);           // bits of the ranks' lowest digit
+  const int levels = h2o::rope_levels_for(c->C, low);     // digits of the ranks 0..C
+  const int entries = h2o::rope_entries_for(c->C, low);   // table entries those digits take
   const size_t ntab = static_cast<size_t>(entries) * (c->D / 2);
   // Everything is built into new buffers and swapped in only once it is
   // complete, so a failure leaves the cache exactly as it was.
@@ -643,20 +646,25 @@ int h2o_cache_set_position_rolling(h2o_cache* c, float rope_base) {
   if ((e = dev_alloc(&rank, nslot * sizeof(int))) != cudaSuccess ||
       (e = dev_alloc(&rope, ntab * sizeof(float2))) != cudaSuccess)
     return give_up(e, "h2o_cache_set_position_rolling: cudaMalloc");
-  // rotation tables of the ranks' base-16 digits: entry 16 * l + d holds, for
-  // every pair i, (cos, sin) of d * 16^l * base^(-2i/D), computed in double
-  // and stored as float in the order the decode lanes read them: a row's
-  // LPR lanes take EPV elements (EPV / 2 pairs) each, and float4 h * LPR + g
-  // of an entry holds lane g's pairs 2h and 2h + 1
+  // rotation tables of the ranks' digits: the entry of level l's digit d
+  // (h2o::rope_entry) holds, for every pair i, (cos, sin) of
+  // d * w_l * base^(-2i/D), w_0 = 1 and w_l = 2^(low + 4(l-1)), computed in
+  // double and stored as float in the order the decode lanes read them: a
+  // row's LPR lanes take EPV elements (EPV / 2 pairs) each, and float4
+  // h * LPR + g of an entry holds lane g's pairs 2h and 2h + 1
   const int epv = 16 / c->elem, lpr = c->D * c->elem / 16;
   std::vector<float2> tab(ntab);
   for (int e = 0; e < entries; ++e) {
-    const int lv = e / 16, d = e % 16;
+    int lv = 0, d = e;  // level and digit of entry e
+    if (levels > 1 && e >= (1 << low)) {
+      lv = 1 + (e - (1 << low)) / 16;
+      d = (e - (1 << low)) % 16;
+    }
+    const double w = lv == 0 ? 1.0 : std::ldexp(1.0, low + 4 * (lv - 1));
     for (int i = 0; i < c->D / 2; ++i) {
-      const double ang = std::ldexp(static_cast<double>(d), 4 * lv) *
-                         std::pow(static_cast<double>(rope_base), -2.0 * i / c->D);
-      const int g = i / (epv / 2), h = (i % (epv / 2)) / 2, w = i % 2;  // lane, float4 of the lane, half
-      tab[static_cast<size_t>(e) * (c->D / 2) + (static_cast<size_t>(h) * lpr + g) * 2 + w] =
+      const double ang = d * w * std::pow(static_cast<double>(rope_base), -2.0 * i / c->D);
+      const int g = i / (epv / 2), h = (i % (epv / 2)) / 2, x = i % 2;  // lane, float4 of the lane, half
+      tab[static_cast<size_t>(e) * (c->D / 2) + (static_cast<size_t>(h) * lpr + g) * 2 + x] =
           make_float2(static_cast<float>(std::cos(ang)), static_cast<float>(std::sin(ang)));
     }
   }

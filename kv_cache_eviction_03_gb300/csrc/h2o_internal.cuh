@@ -36,18 +36,29 @@ __host__ __device__ __forceinline__ bool is_protected(const StaticPattern& sp, i
   return k < sp.count && k * sp.stride == d;
 }
 
-// Position rolling: base-16 digits that every rank 0..max_rank needs (at
-// most 5, for ranks up to 65536), and the rotation-table entries they take:
-// 16 per level below the top one, and only as many as the top digit reaches
-// on the top level.
-__host__ __device__ __forceinline__ int rope_levels_for(int max_rank) {
+// Position rolling: a rank r is split into digits, the lowest of `low` bits
+// (4 or 5) and base-16 digits above it; level l's digit selects one entry of
+// that level's rotation table.  rope_levels_for: the digits every rank
+// 0..max_rank needs; rope_entries_for: the table entries they take (2^low on
+// level 0, 16 on the levels between, and only as many as the top digit
+// reaches on the top level); rope_low_bits_for: 5 when that saves a level
+// (e.g. ranks up to 511 in two digits instead of three), else 4.
+__host__ __device__ __forceinline__ int rope_levels_for(int max_rank, int low) {
   int l = 1;
-  while (l < 5 && (1 << (4 * l)) <= max_rank) ++l;
+  while (l < 6 && (1 << (low + 4 * (l - 1))) <= max_rank) ++l;
   return l;
 }
-__host__ __device__ __forceinline__ int rope_entries_for(int max_rank) {
-  const int l = rope_levels_for(max_rank);
-  return 16 * (l - 1) + (max_rank >> (4 * (l - 1))) + 1;
+__host__ __device__ __forceinline__ int rope_entries_for(int max_rank, int low) {
+  const int l = rope_levels_for(max_rank, low);
+  if (l == 1) return max_rank + 1;
+  return (1 << low) + 16 * (l - 2) + (max_rank >> (low + 4 * (l - 2))) + 1;
+}
+__host__ __device__ __forceinline__ int rope_low_bits_for(int max_rank) {
+  return rope_levels_for(max_rank, 5) < rope_levels_for(max_rank, 4) ? 5 : 4;
+}
+// entry of level l's digit of rank r (see above)
+__host__ __device__ __forceinline__ int rope_entry(int r, int l, int low) {
+  return l == 0 ? (r & ((1 << low) - 1)) : (1 << low) + 16 * (l - 1) + ((r >> (low + 4 * (l - 1))) & 15);
 }
 
 // Per-pair counters kept on the device so decode steps can be replayed from
@@ -82,14 +93,16 @@ struct DecodeParams {
   int pairs;          // P
   // position rolling (rotary embedding at positions inside the cache), or
   // both nullptr: the rank of each slot among the kept tokens in text order,
-  // and the rotation tables of the ranks' base-16 digits: entry 16 * l + d
-  // holds (cos, sin) of d * 16^l * base^(-2i/D) for every pair i < D/2, in
+  // and the rotation tables of the ranks' digits: entry rope_entry(., l, low)
+  // of digit d holds (cos, sin) of d * (weight of level l) * base^(-2i/D),
+  // level 0 weighing 1 and level l 2^(low + 4(l-1)), for every pair i < D/2, in
   // lane order (float4 h * LPR + g holds pairs g * EPV/2 + 2h and + 2h + 1,
   // where a row's LPR lanes take EPV elements each), so that the lanes of a
   // row read consecutive 16-byte words
   int* rank;           // [P, C]
-  const float2* rope;  // [rope_entries_for(C), D / 2]
-  int rope_levels;     // base-16 digits of the largest rank, C (rope_levels_for)
+  const float2* rope;  // [rope_entries_for(C, rope_low_bits), D / 2]
+  int rope_levels;     // digits of the largest rank, C (rope_levels_for)
+  int rope_low_bits;   // bits of the lowest digit (rope_low_bits_for)
   StaticPattern sp;    // protected positions, never eviction candidates
 #ifdef H2O_DECODE_TIMELINE
   int tl_slot;  // profiling build: which stamp buffer this launch writes

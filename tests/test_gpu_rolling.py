@@ -114,6 +114,11 @@ STEPWISE = [
     ("sw-f16-d128-auto", 1, 3, 128, "f16", 20, 12, 64, 0),
     ("sw-f32-d64-s2", 2, 2, 64, "f32", 24, 16, 60, 2),
     ("sw-f16-d128-s8", 1, 2, 128, "f16", 70, 30, 130, 8),
+    # ranks 0..C in two digits with a 5-bit lowest one (C in 256..511), and in
+    # a single 5-bit digit (C in 16..31): the tables' other layouts
+    ("sw-f16-d128-low5", 1, 2, 128, "f16", 180, 120, 330, 0),
+    ("sw-f32-d128-low5-s2", 1, 2, 128, "f32", 260, 200, 480, 2),
+    ("sw-f16-d64-one-level", 1, 3, 64, "f16", 12, 8, 45, 0),
 ]
 
 
