@@ -154,7 +154,8 @@ H2O_API int h2o_cache_check(h2o_cache* cache, void* stream);
  * cluster) share a pair, each streaming its slots through a ring of `stages`
  * 16-row shared-memory stages; splits must be 1, 2, 4, 8 or 16, and stages a
  * multiple of the kernel's consumer warps up to 18: 6, 12 or 18 for one CTA
- * per pair (six consumer warps), 4, 8, 12 or 16 for clusters (four).  Or splits =
+ * per pair (six consumer warps), 4, 8, 12 or 16 for clusters (four), and 8
+ * or 16 for either while position rolling is on (eight).  Or splits =
  * H2O_DECODE_WARP_PER_PAIR: one warp streams a whole pair through its own
  * ring of `stages` (2..8) and then takes its next pair, for many pairs of at
  * most 1024 slots.  0 = automatic for either value (the automatic choice
@@ -175,8 +176,8 @@ H2O_API int h2o_cache_set_decode_shape(h2o_cache* cache, int splits, int stages)
  * rank the kept tokens.  While it is on, h2o_prefill, h2o_prefill_ex and
  * h2o_prefill_ragged return H2O_ESTATE (they apply no rotary embedding;
  * decode from an empty or reset cache), and decode runs on the cluster
- * kernel (a warp-per-pair shape is refused; turning it on resets the shape
- * to automatic).  Returns H2O_EINVAL for a negative or non-finite base. */
+ * kernel (a warp-per-pair shape is refused; turning it on or off resets the
+ * shape to automatic).  Returns H2O_EINVAL for a negative or non-finite base. */
 H2O_API int h2o_cache_set_position_rolling(h2o_cache* cache, float rope_base);
 
 /* Static sparse pattern combined with heavy hitters ("... 深度解读报告",

@@ -271,8 +271,14 @@ constexpr int kMaxStages = 18;
 // (two stages of the 12-stage ring in flight per warp), the CTAs of a
 // cluster four (three each): measured, six is 2.5% faster than four for one
 // CTA per pair (OPT-6.7B shape) and four is 1-3% faster in 2- and 8-CTA
-// clusters (streaming, LLaMA-16K shapes).
-__host__ __device__ constexpr int consumer_warps(int splits) { return splits > 1 ? 4 : 6; }
+// clusters (streaming, LLaMA-16K shapes).  With position rolling the loop is
+// bound by the latency of each key's rotation, not by memory, and eight warps
+// (one stage each of an 8-stage ring) hide it best: measured 12-17% faster
+// than six or four on those three shapes; ten were no faster, and twelve
+// no longer fit two CTAs on an SM.
+__host__ __device__ constexpr int consumer_warps(int splits, bool rope = false) {
+  return rope ? 8 : (splits > 1 ? 4 : 6);
+}
 
 // A CTA's merged partial softmax (max, normaliser, self logit).
 struct __align__(16) Xch {
@@ -327,7 +333,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 }
 
 template <typename T, int D, int NCW, int TILE, bool ROPE>
-__global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel(const DecodeParams prm) {
+__global__ void __launch_bounds__((NCW + 1) * 32, NCW > 6 ? 2 : (NCW > 4 ? 3 : 4)) decode_kernel(const DecodeParams prm) {
   using Cfg = DecodeCfg<T, D, NCW, TILE>;
   using Lay = Layout<D, NCW, TILE, Cfg::STAGE, ROPE>;
   // Stage s is always consumed by warp s % NCW: with a ring depth that is a
@@ -475,20 +481,20 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
     int4 ctr = make_int4(0, 0, 0, 0);
     int nrows = 0;
     auto load_state = [&]() {
-      // The scores and positions are needed only in the epilogue: they come
-      // by asynchronous copies over the CTA's whole slot range (no wait for
-      // the count first), completed before the merge after the loop, so no
-      // consumer stalls on them before the grid-dependency wait.
+      // The scores and positions are needed only in the epilogue, the ranks
+      // (position rolling) from the loop on: they come by asynchronous copies
+      // over the CTA's whole slot range (no wait for the count first), so no
+      // consumer stalls on them before the grid-dependency wait; each thread
+      // completes its own copies before the first use.
       const int cap = max(min(lo + prm.chunk, C) - lo, 0);
       for (int j = tid; j < cap; j += NCW * 32) {
         cp_async4(sc + j, prm.score + slot0 + j);
         cp_async4(ps + j, prm.pos + slot0 + j);
+        if constexpr (ROPE) cp_async4(rk + j, prm.rank + slot0 + j);
       }
       cp_async_commit();
       ctr = *reinterpret_cast<const int4*>(prm.ctr + pair);  // {p, count, head, -}
       nrows = max(min(lo + prm.chunk, ctr.y) - lo, 0);
-      if constexpr (ROPE)  // ranks are needed in the loop
-        for (int j = tid; j < nrows; j += NCW * 32) rk[j] = prm.rank[slot0 + j];
     };
     // warm L2 with this pair's q, k_new and v_new rows while waiting
     {
@@ -561,10 +567,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 4 ? 3 : 4) decode_kernel
     // those small loads ahead of the next step's bulk traffic.
     griddep_launch();
     if constexpr (ROPE) {
-      // every rank in rk[] is in place, and every read of the level-0 table
-      // (query, new key) is done: the level-0 entries become
+      // after the barrier every rank in rk[] is in place, and every read of
+      // the level-0 table (query, new key) is done: the level-0 entries become
       // P0[d] = conj(Q) T0[d], digit d built by row group (warp * G + grp)
       // when d is congruent to it modulo the consumers' row groups
+      cp_async_wait<0>();
       consumer_sync(NCW * 32);
       constexpr int NG = NCW * Cfg::RPI;
       const int n0 = prm.rope_levels > 1 ? 1 << prm.rope_low_bits : C + 1;  // level-0 entries
@@ -1172,9 +1179,11 @@ auto dispatch_ncw(int dtype, int D, F&& f) -> decltype(f(Kern<__half, 128, NCW, 
 // the kernel instance for a dtype, head width, cluster size and position rolling
 template <typename F>
 auto dispatch(int dtype, int D, int splits, bool rope, F&& f) -> decltype(f(Kern<__half, 128, 4, false>{})) {
-  if (consumer_warps(splits) == 4)
-    return rope ? dispatch_ncw<4, true>(dtype, D, f) : dispatch_ncw<4, false>(dtype, D, f);
-  return rope ? dispatch_ncw<6, true>(dtype, D, f) : dispatch_ncw<6, false>(dtype, D, f);
+  if (rope)
+    return splits > 1 ? dispatch_ncw<consumer_warps(2, true), true>(dtype, D, f)
+                      : dispatch_ncw<consumer_warps(1, true), true>(dtype, D, f);
+  return splits > 1 ? dispatch_ncw<consumer_warps(2), false>(dtype, D, f)
+                    : dispatch_ncw<consumer_warps(1), false>(dtype, D, f);
 }
 
 }  // namespace
@@ -1184,7 +1193,7 @@ int decode_max_chunk() { return kMaxChunk; }
 int decode_chunk(int C, int splits) { return chunk_for(C, splits); }
 
 int decode_max_stages() { return kMaxStages; }
-int decode_stage_multiple(int splits) { return consumer_warps(splits); }
+int decode_stage_multiple(int splits, bool rope) { return consumer_warps(splits, rope); }
 
 int device_sms() {
   int sms = 0, dev = 0;
@@ -1247,11 +1256,12 @@ DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C, bool rope) {
   }
   while (sh.splits < 16 && chunk_for(C, sh.splits) > kMaxChunk) sh.splits *= 2;
   const long long ctas = static_cast<long long>(pairs) * sh.splits;
-  const int ncw = consumer_warps(sh.splits);
+  const int ncw = consumer_warps(sh.splits, rope);
   sh.stages = ncw;
   if (ctas <= 2LL * sms) {
     const int ch = chunk_for(C, sh.splits);
-    for (int st : {12, ncw == 6 ? 6 : 8}) {
+    const int deep = ncw <= 12 ? 12 / ncw * ncw : ncw;
+    for (int st : {deep, ncw == 4 ? 8 : ncw}) {
       const int res =
           decode_resident(dtype, D, sh.splits, st, ch, pairs, rope ? rope_entries_for(C, rope_low_bits_for(C)) : 0);
       if (res >= 2 * sms || static_cast<long long>(res) >= ctas) {
@@ -1325,7 +1335,7 @@ cudaError_t launch_decode(const DecodeParams& prm, int dtype, int D, int pairs, 
                   [&](auto k) { return decltype(k)::launch(prm, pairs, splits, s); });
 }
 
-int decode_threads(int splits) { return (consumer_warps(splits) + 1) * 32; }
+int decode_threads(int splits, bool rope) { return (consumer_warps(splits, rope) + 1) * 32; }
 
 #ifdef H2O_DECODE_TIMELINE
 cudaError_t decode_timeline_read(void* dst, size_t bytes) {

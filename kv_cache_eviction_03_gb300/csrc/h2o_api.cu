@@ -556,7 +556,7 @@ int h2o_cache_set_decode_shape(h2o_cache* c, int splits, int stages) {
       n = c->shape_auto.stages;
     else
       n = s == h2o::kDecodeWarpPerPair ? h2o::decode_warp_default_stages(c->dtype, c->D, c->C, c->P)
-                                      : h2o::decode_stage_multiple(s);
+                                      : h2o::decode_stage_multiple(s, c->rope != nullptr);
   }
   if (s == h2o::kDecodeWarpPerPair) {
     if (c->rope)
@@ -570,9 +570,9 @@ int h2o_cache_set_decode_shape(h2o_cache* c, int splits, int stages) {
     if (h2o::decode_warp_resident(c->dtype, c->D, n, c->C) <= 0)
       return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: warp per pair with %d stages cannot be scheduled", n);
   } else {
-    if (n < 0 || n > h2o::decode_max_stages() || n % h2o::decode_stage_multiple(s) != 0)
+    if (n < 0 || n > h2o::decode_max_stages() || n % h2o::decode_stage_multiple(s, c->rope != nullptr) != 0)
       return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: stages must be a multiple of %d in 0..%d",
-                  h2o::decode_stage_multiple(s), h2o::decode_max_stages());
+                  h2o::decode_stage_multiple(s, c->rope != nullptr), h2o::decode_max_stages());
     if (chunk_for(c->C, s) > h2o::decode_max_chunk())
       return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: %d splits leave more than %d slots per CTA", s,
                   h2o::decode_max_chunk());
@@ -608,7 +608,7 @@ int h2o_cache_info(const h2o_cache* c, int32_t* info) {
   info[5] = c->dtype;
   info[6] = splits_in_use(c);
   info[7] = stages_in_use(c);
-  info[8] = splits_in_use(c) == h2o::kDecodeWarpPerPair ? 128 : h2o::decode_threads(splits_in_use(c));
+  info[8] = splits_in_use(c) == h2o::kDecodeWarpPerPair ? 128 : h2o::decode_threads(splits_in_use(c), c->rope != nullptr);
   info[9] = 0;
   return H2O_OK;
 }
@@ -626,7 +626,11 @@ int h2o_cache_set_position_rolling(h2o_cache* c, float rope_base) {
     c->rank = nullptr;
     c->rope = nullptr;
     c->rope_base = 0.f;
+    // the plain kernel's own launch shape: an explicit one set for rolling
+    // (ring depths in multiples of its consumer warps) goes back to automatic
     c->shape_auto = h2o::decode_pick_shape(c->dtype, c->D, c->P, c->C, false);
+    c->splits_override = 0;
+    c->stages_override = 0;
     return H2O_OK;
   }
   const size_t nslot = static_cast<size_t>(c->P) * c->C;

@@ -195,9 +195,9 @@ DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C, bool rope = fa
 int decode_resident(int dtype, int D, int splits, int nstage, int chunk, int pairs, int rope_entries = 0);
 int decode_chunk(int C, int splits);
 int decode_max_stages();
-int decode_stage_multiple(int splits);  // ring depths for this cluster size must be multiples of this
+int decode_stage_multiple(int splits, bool rope = false);  // ring depths for this cluster size must be multiples of this
 int decode_max_chunk();
-int decode_threads(int splits);  // threads per CTA of the cluster kernel
+int decode_threads(int splits, bool rope = false);  // threads per CTA of the cluster kernel
 // warp-per-pair kernel: limits, and whether a shape can run (0 = no)
 int decode_warp_max_slots();
 int decode_warp_min_stages();
