@@ -99,10 +99,10 @@ struct RowGeom {
   static_assert(LPR >= 1 && LPR <= 32, "row must be 16..512 bytes");
 };
 
-template <typename T, int D, int NCW, int TILE>
+template <typename T, int D, int NCW, int TILE, int NP = 1>
 struct DecodeCfg : RowGeom<T, D> {
   using G = RowGeom<T, D>;
-  static constexpr int NW = NCW + 1;     // consumer warps + one producer warp
+  static constexpr int NW = NCW + NP;    // consumer warps + NP producer warps
   static constexpr int NT = NW * 32;
   static constexpr int STAGE = 2 * TILE * G::ROWB;
   static_assert(TILE % G::RPI == 0, "a stage holds whole row groups");
@@ -110,31 +110,41 @@ struct DecodeCfg : RowGeom<T, D> {
   static_assert(TILE <= 64, "per-warp weight buffer holds 64 rows");
 };
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // One warp attends to one stage of `rows` (<= TILE) K/V rows: the logits
 // q . k_r (q pre-scaled into the base-2 domain) are kept in lg[0..rows), and
-// the warp's running softmax state (m, l, o) absorbs the rows.  Row group g
+// each row group's running softmax state (m, l, o) absorbs its rows.  Row group g
 // of the warp (LPR lanes) owns RG rows; every lane accumulates partial dot
 // products of those rows over its 16 bytes of the row, a butterfly exchange
 // sums them so that lane-group members end up holding whole-row logits (DUP
 // copies of each), and the probabilities go through the warp's shared buffer
 // wb to the lanes that weight V.  After the call the warp no longer reads the
-// stage.
+// stage.  With k_empty / v_full (position rolling) the stage's halves have
+// barriers of their own: the K half is released on k_empty as soon as the
+// logits are formed, and the V half is waited for (v_full, phase parity
+// v_par) only before the V rows are weighted; false if that wait gave up
+// (the V rows are then not read).
 // Position rolling: rotate this lane's EPV/2 element pairs (2i, 2i+1) of a
 // row by r * theta_i, as in the rotary embedding, composed from the rank's
 // digits: the rotation-table entry of level l's digit (rope_entry) holds
-// (cos, sin) of the digit's angle (in shared memory, D/2 float2 per entry in
-// lane order: float4 h * LPR + lig holds this lane's pairs 2h and 2h + 1).
+// cos and sin of the digit's angle for every pair, in shared memory in lane
+// order: float4 h * LPR + lig of an entry holds, for this lane's pairs 2h and
+// 2h + 1, (cos, cos, sin, sin), so that two pairs rotate in packed f32x2
+// arithmetic.
 template <int EPV, int D, int LPR>
 __device__ __forceinline__ void rope_rotate_level(float (&x)[EPV], const float2* tab, int entry, int lig) {
   const float4* t = reinterpret_cast<const float4*>(tab + entry * (D / 2)) + lig;
 #pragma unroll
   for (int h = 0; h < EPV / 4; ++h) {
-    const float4 c = t[h * LPR];  // (cos, sin) of two pairs
+    const float4 c = t[h * LPR];  // cos, cos, sin, sin of two pairs
     const float a0 = x[4 * h], a1 = x[4 * h + 1], b0 = x[4 * h + 2], b1 = x[4 * h + 3];
-    x[4 * h] = a0 * c.x - a1 * c.y;
-    x[4 * h + 1] = a0 * c.y + a1 * c.x;
-    x[4 * h + 2] = b0 * c.z - b1 * c.w;
-    x[4 * h + 3] = b0 * c.w + b1 * c.z;
+    x[4 * h] = a0 * c.x - a1 * c.z;
+    x[4 * h + 1] = a0 * c.z + a1 * c.x;
+    x[4 * h + 2] = b0 * c.y - b1 * c.w;
+    x[4 * h + 3] = b0 * c.w + b1 * c.y;
   }
 }
 template <int EPV, int D, int LPR>
@@ -144,17 +154,39 @@ __device__ __forceinline__ void rope_rotate_digits(float (&x)[EPV], const float2
   for (int lv = 0; lv < 6; ++lv)
     if (lv < levels) rope_rotate_level<EPV, D, LPR>(x, tab, rope_entry(r, lv, low), lig);
 }
+// The same rotation on a key held as real parts re[h] = (x[4h], x[4h+2]) and
+// imaginary parts im[h] = (x[4h+1], x[4h+3]) of its pairs, two pairs per
+// f32x2 instruction (each lane of an f32x2 operation rounds as the scalar
+// fp32 operation would).
+template <int NH, int D, int LPR>
+__device__ __forceinline__ void rope_rotate_level2(float2 (&re)[NH], float2 (&im)[NH], const float2* tab, int entry,
+                                                   int lig) {
+  const float4* t = reinterpret_cast<const float4*>(tab + entry * (D / 2)) + lig;
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    const float4 c = t[h * LPR];
+    const float2 cs = make_float2(c.x, c.y), sn = make_float2(c.z, c.w);
+    const float2 rc = mul_f32x2(re[h], cs), rs = mul_f32x2(re[h], sn);
+    const float2 nim = mul_f32x2(im[h], make_float2(-1.f, -1.f));
+    re[h] = fma_f32x2(nim, sn, rc);    // re cos - im sin
+    im[h] = fma_f32x2(im[h], cs, rs);  // re sin + im cos
+  }
+}
 
 // Position rolling (ROPE): the logit of a key at rank r is
 // Re sum_i conj(Q_i) T0[lowest digit of r]_i K'_i over the lane's pairs as complex
 // numbers, Q the rotated query, T0 the level-0 table and K' the key rotated
 // by the rank's higher digits (KL levels): tab's level-0 entries then hold
 // P0[d] = conj(Q) T0[d], built once per step, so a key takes KL rotations.
+// P0 is stored per two pairs as (Re, Re, -Im, -Im), and the rotations, the
+// P0 dot product and the V accumulation run in f32x2.
 template <typename T, int D, int TILE, bool ROPE = false, int KL = 0>
-__device__ __forceinline__ void attend_tile(const unsigned char* sK, const unsigned char* sV, int rows,
+__device__ __forceinline__ bool attend_tile(const unsigned char* sK, const unsigned char* sV, int rows,
                                             const float (&qv)[RowGeom<T, D>::EPV], float& m, float& l,
                                             float (&o)[RowGeom<T, D>::EPV], float* wb, float* lg, int lane,
-                                            const int* rk = nullptr, const float2* tab = nullptr, int low = 4) {
+                                            const int* rk = nullptr, const float2* tab = nullptr, int low = 4,
+                                            uint64_t* k_empty = nullptr, uint64_t* v_full = nullptr,
+                                            uint32_t v_par = 0) {
   using Gm = RowGeom<T, D>;
   constexpr int EPV = Gm::EPV, LPR = Gm::LPR, ROWB = Gm::ROWB;
   constexpr int G = Gm::RPI;      // row groups per warp
@@ -172,17 +204,24 @@ __device__ __forceinline__ void attend_tile(const unsigned char* sK, const unsig
     float a = 0.f;
     if constexpr (ROPE) {  // key rotated to its rank inside the cache (rk: this stage's ranks)
       const int rr = row < rows ? rk[row] : 0;
+      constexpr int NH = EPV / 4;
+      float2 re[NH], im[NH];
 #pragma unroll
-      for (int lv = 1; lv <= KL; ++lv) rope_rotate_level<EPV, D, LPR>(kf, tab, rope_entry(rr, lv, low), lig);
-      const float4* z = reinterpret_cast<const float4*>(tab + rope_entry(rr, 0, low) * (D / 2)) + lig;  // P0[d0]
-#pragma unroll
-      for (int h = 0; h < EPV / 4; ++h) {
-        const float4 c = z[h * LPR];
-        a = fmaf(c.x, kf[4 * h], a);
-        a = fmaf(-c.y, kf[4 * h + 1], a);
-        a = fmaf(c.z, kf[4 * h + 2], a);
-        a = fmaf(-c.w, kf[4 * h + 3], a);
+      for (int h = 0; h < NH; ++h) {
+        re[h] = make_float2(kf[4 * h], kf[4 * h + 2]);
+        im[h] = make_float2(kf[4 * h + 1], kf[4 * h + 3]);
       }
+#pragma unroll
+      for (int lv = 1; lv <= KL; ++lv) rope_rotate_level2<NH, D, LPR>(re, im, tab, rope_entry(rr, lv, low), lig);
+      const float4* z = reinterpret_cast<const float4*>(tab + rope_entry(rr, 0, low) * (D / 2)) + lig;  // P0[d0]
+      float2 a2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const float4 c = z[h * LPR];
+        a2 = fma_f32x2(re[h], make_float2(c.x, c.y), a2);
+        a2 = fma_f32x2(im[h], make_float2(c.z, c.w), a2);
+      }
+      a = a2.x + a2.y;
     } else {
 #pragma unroll
       for (int e = 0; e < EPV; ++e) a = fmaf(qv[e], kf[e], a);
@@ -206,12 +245,19 @@ __device__ __forceinline__ void attend_tile(const unsigned char* sK, const unsig
       acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], off);
     }
   }
+  // every lane's K reads are complete (their sums went through the exchange)
+  if (k_empty != nullptr) {
+    __syncwarp();
+    if (lane == 0 && rows > 0) mbar_arrive(k_empty);
+  }
   const int rown = grp * RG + lig / DUP;  // the row whose logit this lane holds
   const bool valid = rown < rows;
   const float x = valid ? acc[0] : kNeg;
+  // running maximum per row group (its lanes weight only its own rows; the
+  // groups' states are merged after the loop)
   float mx = x;
 #pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  for (int off = LPR / 2; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   const float mn = fmaxf(m, mx);
   const float corr = exp2f(m - mn);
   m = mn;
@@ -221,21 +267,46 @@ __device__ __forceinline__ void attend_tile(const unsigned char* sK, const unsig
   }
   __syncwarp();
   l *= corr;
+  if constexpr (ROPE) {
 #pragma unroll
-  for (int e = 0; e < EPV; ++e) o[e] *= corr;
+    for (int e = 0; e < EPV; e += 2) {
+      const float2 oc = mul_f32x2(make_float2(o[e], o[e + 1]), make_float2(corr, corr));
+      o[e] = oc.x;
+      o[e + 1] = oc.y;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) o[e] *= corr;
+  }
+  int vrows = rows;
+  bool v_ok = true;
+  if (v_full != nullptr && rows > 0 && !mbar_wait_bounded(v_full, v_par, kWaitLimit)) {
+    v_ok = false;
+    vrows = 0;
+  }
 #pragma unroll
   for (int r = 0; r < RG; ++r) {
     const int row = grp * RG + r;
-    if (row < rows) {
+    if (row < vrows) {
       const float w = wb[row];
       l += w;
       float vf[EPV];
       Vec16<T>::unpack(*reinterpret_cast<const uint4*>(sV + row * ROWB + lig * 16), vf);
+      if constexpr (ROPE) {
 #pragma unroll
-      for (int e = 0; e < EPV; ++e) o[e] = fmaf(w, vf[e], o[e]);
+        for (int e = 0; e < EPV; e += 2) {
+          const float2 oe = fma_f32x2(make_float2(w, w), make_float2(vf[e], vf[e + 1]), make_float2(o[e], o[e + 1]));
+          o[e] = oe.x;
+          o[e + 1] = oe.y;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) o[e] = fmaf(w, vf[e], o[e]);
+      }
     }
   }
   __syncwarp();  // wb is rewritten by the next stage
+  return v_ok;
 }
 
 // Minimum over the warp of a 64-bit key (score bits << 32 | position), in
@@ -279,6 +350,13 @@ constexpr int kMaxStages = 18;
 __host__ __device__ constexpr int consumer_warps(int splits, bool rope = false) {
   return rope ? 8 : (splits > 1 ? 4 : 6);
 }
+// Producer warps: two (K rows and V rows under barriers of their own) where
+// the stage halves are released separately, else one.  Measured: separate
+// halves take the rolling kernel 4-7% faster (its logits are slow, and the K
+// half refills meanwhile) and the plain kernel 9-17% slower, so only
+// position rolling uses them.
+__host__ __device__ constexpr bool split_halves(bool rope) { return rope; }
+__host__ __device__ constexpr int producer_warps(bool rope) { return split_halves(rope) ? 2 : 1; }
 
 // A CTA's merged partial softmax (max, normaliser, self logit).
 struct __align__(16) Xch {
@@ -290,16 +368,18 @@ struct __align__(16) Xch {
 template <int D, int NCW, int TILE, int STAGE, bool ROPE>
 struct Layout {
   static constexpr int PER_SLOT = ROPE ? 16 : 12;  // logit, score, position (, rank)
-  static constexpr size_t full = 0;                            // kMaxStages mbarriers
-  static constexpr size_t empty = 8 * kMaxStages;              // kMaxStages mbarriers
-  static constexpr size_t xbar = 16 * kMaxStages;              // mbarrier: the peers' partials have landed
+  static constexpr size_t full = 0;                            // kMaxStages mbarriers (K and V, or K)
+  static constexpr size_t empty = 8 * kMaxStages;              // kMaxStages mbarriers (K and V, or K)
+  static constexpr size_t fullv = 16 * kMaxStages;             // kMaxStages mbarriers (V, rolling)
+  static constexpr size_t emptyv = 24 * kMaxStages;            // kMaxStages mbarriers (V, rolling)
+  static constexpr size_t xbar = 32 * kMaxStages;              // mbarrier: the peers' partials have landed
   static constexpr size_t kbar = xbar + 8;                     // mbarrier: the peers' candidates have landed
   static constexpr size_t tbar = xbar + 16;                    // mbarrier: the rotation tables have landed
   static constexpr size_t xch = xbar + 32;
   static constexpr size_t xo = xch + sizeof(Xch);              // this CTA's partial o[D]
   static constexpr size_t gm = (xo + D * 4 + 15) / 16 * 16;    // per-rank partials [16], candidates [16]
   static constexpr size_t blk = gm + 16 * 32;                  // block argmin scratch + counters
-  static constexpr size_t wbuf = (blk + 12 * (NCW + 1) + 16 + 15) / 16 * 16;  // per-warp row weights
+  static constexpr size_t wbuf = (blk + 12 * (NCW + 2) + 16 + 15) / 16 * 16;  // per-warp row weights
   static constexpr size_t stages = (wbuf + NCW * TILE * 4 + 127) / 128 * 128;
   __host__ __device__ static size_t tail(int nstage) { return stages + static_cast<size_t>(nstage) * STAGE; }
   // after the logits, scores and positions of the CTA's slots: rank 0's
@@ -328,13 +408,12 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 
 template <typename T, int D, int NCW, int TILE, bool ROPE>
-__global__ void __launch_bounds__((NCW + 1) * 32, NCW > 6 ? 2 : (NCW > 4 ? 3 : 4)) decode_kernel(const DecodeParams prm) {
-  using Cfg = DecodeCfg<T, D, NCW, TILE>;
+__global__ void __launch_bounds__((NCW + producer_warps(ROPE)) * 32, NCW > 6 ? 2 : (NCW > 4 ? 3 : 4))
+    decode_kernel(const DecodeParams prm) {
+  constexpr bool SPLIT = split_halves(ROPE);
+  using Cfg = DecodeCfg<T, D, NCW, TILE, producer_warps(ROPE)>;
   using Lay = Layout<D, NCW, TILE, Cfg::STAGE, ROPE>;
   // Stage s is always consumed by warp s % NCW: with a ring depth that is a
   // multiple of NCW a warp never waits two phases ahead on a stage another
@@ -350,6 +429,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 6 ? 2 : (NCW > 4 ? 3 : 4
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + Lay::full);
   uint64_t* empty_bar = reinterpret_cast<uint64_t*>(smem + Lay::empty);
+  uint64_t* fullv_bar = reinterpret_cast<uint64_t*>(smem + Lay::fullv);
+  uint64_t* emptyv_bar = reinterpret_cast<uint64_t*>(smem + Lay::emptyv);
   Xch* xch = reinterpret_cast<Xch*>(smem + Lay::xch);
   float* xo = reinterpret_cast<float*>(smem + Lay::xo);
   Xch* xin = reinterpret_cast<Xch*>(smem + Lay::gm);         // rank r's (m, l, self) at [r]
@@ -384,6 +465,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 6 ? 2 : (NCW > 4 ? 3 : 4
     for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
+      if constexpr (SPLIT) {
+        mbar_init(&fullv_bar[s], 1);
+        mbar_init(&emptyv_bar[s], 1);
+      }
     }
     mbar_init(xbar, 1);
     mbar_init(kbar, 1);
@@ -409,15 +494,26 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 6 ? 2 : (NCW > 4 ? 3 : 4
   int p = 0, count = 0, head = 0;
   uint4 newrow = make_uint4(0, 0, 0, 0);
 
-  if (warp == NCW) {
-    // ---------------------------------------------------------- producer warp
+  if (warp >= NCW) {
+    // -------------------------------------------------------- producer warp(s)
+    // One warp copies each tile's K and V rows into its stage under one pair
+    // of barriers (full_bar / empty_bar).  With position rolling, where a
+    // tile's logits take much longer than its memory, warp NCW copies the K
+    // rows (full_bar / empty_bar) and warp NCW + 1 the V rows (fullv_bar /
+    // emptyv_bar): the K half of a stage is refilled while its consumer still
+    // weights the V half.
+    const int part = SPLIT ? warp - NCW : 2;  // 0: K rows, 1: V rows, 2: both
     if (lane == 0) {
+      uint64_t* fb = part == 1 ? fullv_bar : full_bar;
+      uint64_t* eb = part == 1 ? emptyv_bar : empty_bar;
       // position rolling: the rotation tables, constant while rolling is on,
       // so they are copied before any wait
       const uint32_t tbytes = static_cast<uint32_t>(Lay::tab_bytes(rope_entries_for(C, prm.rope_low_bits)));
       if constexpr (ROPE) {
-        mbar_arrive_expect_tx(tbar, tbytes);
-        bulk_g2s(rtab, prm.rope, tbytes, tbar);
+        if (part == 0) {
+          mbar_arrive_expect_tx(tbar, tbytes);
+          bulk_g2s(rtab, prm.rope, tbytes, tbar);
+        }
       }
       // The slot store is read before the grid-dependency wait only when the
       // previous kernel on this stream did not touch this cache.  Then the
@@ -429,14 +525,19 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 6 ? 2 : (NCW > 4 ? 3 : 4
       const unsigned char* gK = static_cast<const unsigned char*>(prm.K) + slot0 * ROWB;
       const unsigned char* gV = static_cast<const unsigned char*>(prm.V) + slot0 * ROWB;
       const uint64_t policy = policy_evict_first();
-      int issued = 0, rows0 = 0;
+      auto issue = [&](int t, int s, int rows) {
+        const uint32_t bytes = static_cast<uint32_t>(rows * ROWB);
+        unsigned char* st = stage_base + static_cast<size_t>(s) * Cfg::STAGE;
+        const size_t off = static_cast<size_t>(t) * TILE * ROWB;
+        mbar_arrive_expect_tx(&fb[s], part == 2 ? 2 * bytes : bytes);
+        if (part != 1) bulk_g2s_stream(st, gK + off, bytes, &fb[s], policy);
+        if (part != 0) bulk_g2s_stream(st + TILE * ROWB, gV + off, bytes, &fb[s], policy);
+      };
+      int issued = 0;
       if (prm.prefetch) {
-        rows0 = min(TILE, max(min(lo + prm.chunk, C) - lo, 0));  // inside the pair's slots
+        const int rows0 = min(TILE, max(min(lo + prm.chunk, C) - lo, 0));  // inside the pair's slots
         if (rows0 > 0) {
-          const uint32_t bytes = static_cast<uint32_t>(rows0 * ROWB);
-          mbar_arrive_expect_tx(&full_bar[0], 2 * bytes);
-          bulk_g2s_stream(stage_base, gK, bytes, &full_bar[0], policy);
-          bulk_g2s_stream(stage_base + TILE * ROWB, gV, bytes, &full_bar[0], policy);
+          issue(0, 0, rows0);
           issued = 1;
         }
       } else {
@@ -451,26 +552,21 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 6 ? 2 : (NCW > 4 ? 3 : 4
         // grid-dependency wait, whose length depends on earlier kernels: wait
         // for the dependency here too before waiting on a stage
         if (k == 1 && s == 0 && prm.prefetch) griddep_wait();
-        if (k > 0 && !mbar_wait_bounded(&empty_bar[s], static_cast<uint32_t>((k - 1) & 1), kWaitLimit)) {
+        if (k > 0 && !mbar_wait_bounded(&eb[s], static_cast<uint32_t>((k - 1) & 1), kWaitLimit)) {
           atomicOr(prm.err, ERR_RING_TIMEOUT);
           break;
         }
-        const int rows = min(TILE, nrows - t * TILE);
-        const uint32_t bytes = static_cast<uint32_t>(rows * ROWB);
-        unsigned char* st = stage_base + static_cast<size_t>(s) * Cfg::STAGE;
-        mbar_arrive_expect_tx(&full_bar[s], 2 * bytes);
-        bulk_g2s_stream(st, gK + static_cast<size_t>(t) * TILE * ROWB, bytes, &full_bar[s], policy);
-        bulk_g2s_stream(st + TILE * ROWB, gV + static_cast<size_t>(t) * TILE * ROWB, bytes, &full_bar[s], policy);
+        issue(t, s, min(TILE, nrows - t * TILE));
         issued = t + 1;
       }
       // no copy may still be landing in shared memory when the CTA exits: the
       // last phase of every stage used has completed (immediately true once
       // the consumers have read it)
       for (int t = max(issued - NSTAGE, 0); t < issued; ++t)
-        if (!mbar_wait_bounded(&full_bar[t % NSTAGE], static_cast<uint32_t>((t / NSTAGE) & 1), kWaitLimit))
+        if (!mbar_wait_bounded(&fb[t % NSTAGE], static_cast<uint32_t>((t / NSTAGE) & 1), kWaitLimit))
           atomicOr(prm.err, ERR_RING_TIMEOUT);
       if constexpr (ROPE)
-        if (!mbar_wait_bounded(tbar, 0u, kWaitLimit)) atomicOr(prm.err, ERR_RING_TIMEOUT);
+        if (part == 0 && !mbar_wait_bounded(tbar, 0u, kWaitLimit)) atomicOr(prm.err, ERR_RING_TIMEOUT);
     }
     __syncwarp();
   } else {
@@ -579,10 +675,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 6 ? 2 : (NCW > 4 ? 3 : 4
         float4* e = reinterpret_cast<float4*>(rtab + d * (D / 2)) + lig;
 #pragma unroll
         for (int h = 0; h < EPV / 4; ++h) {
-          const float4 c = e[h * LPR];
+          const float4 c = e[h * LPR];  // cos, cos, sin, sin of pairs 2h, 2h + 1
           const float qa = qv[4 * h], qb = qv[4 * h + 1], qc = qv[4 * h + 2], qd = qv[4 * h + 3];
-          // conj(qa + i qb) (c.x + i c.y) and conj(qc + i qd) (c.z + i c.w)
-          e[h * LPR] = make_float4(qa * c.x + qb * c.y, qa * c.y - qb * c.x, qc * c.z + qd * c.w, qc * c.w - qd * c.z);
+          // conj(qa + i qb) (cos + i sin) and conj(qc + i qd) (cos + i sin):
+          // real parts, then negated imaginary parts
+          e[h * LPR] = make_float4(qa * c.x + qb * c.z, qc * c.y + qd * c.w, qb * c.x - qa * c.z, qd * c.y - qc * c.w);
         }
       }
       consumer_sync(NCW * 32);
@@ -601,19 +698,38 @@ __global__ void __launch_bounds__((NCW + 1) * 32, NCW > 6 ? 2 : (NCW > 4 ? 3 : 4
         const int* rks = rk + t * TILE;
         float* lgs = lg + t * TILE;
         const int low = prm.rope_low_bits;
+        uint64_t* ke = &empty_bar[s];  // the K half goes back inside attend_tile
+        uint64_t* vf = &fullv_bar[s];
+        const uint32_t par = static_cast<uint32_t>((t / NSTAGE) & 1);
+        bool v_ok = true;
         switch (prm.rope_levels) {  // key-side rotations: the digits above the lowest
-          case 1: attend_tile<T, D, TILE, true, 0>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low); break;
-          case 2: attend_tile<T, D, TILE, true, 1>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low); break;
-          case 3: attend_tile<T, D, TILE, true, 2>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low); break;
-          case 4: attend_tile<T, D, TILE, true, 3>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low); break;
-          default: attend_tile<T, D, TILE, true, 4>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low); break;
+          case 1: v_ok = attend_tile<T, D, TILE, true, 0>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low, ke, vf, par); break;
+          case 2: v_ok = attend_tile<T, D, TILE, true, 1>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low, ke, vf, par); break;
+          case 3: v_ok = attend_tile<T, D, TILE, true, 2>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low, ke, vf, par); break;
+          case 4: v_ok = attend_tile<T, D, TILE, true, 3>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low, ke, vf, par); break;
+          default: v_ok = attend_tile<T, D, TILE, true, 4>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low, ke, vf, par); break;
         }
+        if (!v_ok) {
+          ok = false;
+          if (lane == 0) atomicOr(prm.err, ERR_MBAR_TIMEOUT);
+        }
+        // the V half may be refilled; after a timeout it is not released
+        if (lane == 0 && ok) mbar_arrive(&emptyv_bar[s]);
+      } else if constexpr (SPLIT) {
+        const bool v_ok = attend_tile<T, D, TILE>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lg + t * TILE, lane,
+                                                  nullptr, nullptr, 4, &empty_bar[s], &fullv_bar[s],
+                                                  static_cast<uint32_t>((t / NSTAGE) & 1));
+        if (!v_ok) {
+          ok = false;
+          if (lane == 0) atomicOr(prm.err, ERR_MBAR_TIMEOUT);
+        }
+        if (lane == 0 && ok) mbar_arrive(&emptyv_bar[s]);
       } else {
         attend_tile<T, D, TILE>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lg + t * TILE, lane);
+        // stage s may be refilled; after a timeout the stage is not released,
+        // so no new copy can target memory an unfinished copy still writes
+        if (lane == 0 && ok) mbar_arrive(&empty_bar[s]);
       }
-      // stage s may be refilled; after a timeout the stage is not released,
-      // so no new copy can target memory an unfinished copy still writes
-      if (lane == 0 && ok) mbar_arrive(&empty_bar[s]);
     }
 
     merge_groups<T, D>(m, l, o);  // identical result in every row group
@@ -1100,7 +1216,7 @@ struct WarpKern {
 template <typename T, int D, int NCW, bool ROPE>
 struct Kern {
   static constexpr int TILE = 16;
-  using Cfg = DecodeCfg<T, D, NCW, TILE>;
+  using Cfg = DecodeCfg<T, D, NCW, TILE, producer_warps(ROPE)>;
   using Lay = Layout<D, NCW, TILE, Cfg::STAGE, ROPE>;
   static constexpr auto fn = decode_kernel<T, D, NCW, TILE, ROPE>;
 
@@ -1335,7 +1451,7 @@ cudaError_t launch_decode(const DecodeParams& prm, int dtype, int D, int pairs, 
                   [&](auto k) { return decltype(k)::launch(prm, pairs, splits, s); });
 }
 
-int decode_threads(int splits, bool rope) { return (consumer_warps(splits, rope) + 1) * 32; }
+int decode_threads(int splits, bool rope) { return (consumer_warps(splits, rope) + producer_warps(rope)) * 32; }
 
 #ifdef H2O_DECODE_TIMELINE
 cudaError_t decode_timeline_read(void* dst, size_t bytes) {

@@ -651,11 +651,12 @@ int h2o_cache_set_position_rolling(h2o_cache* c, float rope_base) {
       (e = dev_alloc(&rope, ntab * sizeof(float2))) != cudaSuccess)
     return give_up(e, "h2o_cache_set_position_rolling: cudaMalloc");
   // rotation tables of the ranks' digits: the entry of level l's digit d
-  // (h2o::rope_entry) holds, for every pair i, (cos, sin) of
+  // (h2o::rope_entry) holds, for every pair i, cos and sin of
   // d * w_l * base^(-2i/D), w_0 = 1 and w_l = 2^(low + 4(l-1)), computed in
   // double and stored as float in the order the decode lanes read them: a
   // row's LPR lanes take EPV elements (EPV / 2 pairs) each, and float4
-  // h * LPR + g of an entry holds lane g's pairs 2h and 2h + 1
+  // h * LPR + g of an entry holds lane g's pairs 2h and 2h + 1 as
+  // (cos, cos, sin, sin)
   const int epv = 16 / c->elem, lpr = c->D * c->elem / 16;
   std::vector<float2> tab(ntab);
   for (int e = 0; e < entries; ++e) {
@@ -667,9 +668,11 @@ int h2o_cache_set_position_rolling(h2o_cache* c, float rope_base) {
     const double w = lv == 0 ? 1.0 : std::ldexp(1.0, low + 4 * (lv - 1));
     for (int i = 0; i < c->D / 2; ++i) {
       const double ang = d * w * std::pow(static_cast<double>(rope_base), -2.0 * i / c->D);
-      const int g = i / (epv / 2), h = (i % (epv / 2)) / 2, x = i % 2;  // lane, float4 of the lane, half
-      tab[static_cast<size_t>(e) * (c->D / 2) + (static_cast<size_t>(h) * lpr + g) * 2 + x] =
-          make_float2(static_cast<float>(std::cos(ang)), static_cast<float>(std::sin(ang)));
+      const int g = i / (epv / 2), h = (i % (epv / 2)) / 2, x = i % 2;  // lane, float4 of the lane, pair in it
+      float* f4 = reinterpret_cast<float*>(tab.data() + static_cast<size_t>(e) * (c->D / 2)) +
+                  (static_cast<size_t>(h) * lpr + g) * 4;
+      f4[x] = static_cast<float>(std::cos(ang));
+      f4[2 + x] = static_cast<float>(std::sin(ang));
     }
   }
   std::vector<int> pos(nslot), ranks;

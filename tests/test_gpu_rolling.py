@@ -174,7 +174,8 @@ def test_rolling_refuses_prefill_and_warp_per_pair():
 
 
 def test_rolling_launch_shape_rules():
-    """Rolling runs eight consumer warps (one stage each of the ring): ring
+    """Rolling runs eight consumer warps (one stage each of the ring) and two
+    producer warps (K rows, V rows): ring
     depths are multiples of eight while it is on, and the plain kernel's
     rules come back when it is switched off."""
     cache = B.h2o_cache_create(1, 2, 128, 40, 24, B.H2O_F16)
@@ -183,12 +184,12 @@ def test_rolling_launch_shape_rules():
     B.h2o_cache_set_decode_shape(cache, 1, 12)
     B.h2o_cache_set_position_rolling(cache, BASE)
     info = B.h2o_cache_info(cache)
-    assert info[8] == 9 * 32 and info[7] % 8 == 0  # the explicit shape went back to the automatic one
+    assert info[8] == 10 * 32 and info[7] % 8 == 0  # the explicit shape went back to the automatic one
     for splits in (1, 2):
         with pytest.raises(B.H2OError):
             B.h2o_cache_set_decode_shape(cache, splits, 12)
         B.h2o_cache_set_decode_shape(cache, splits, 8)
-        assert B.h2o_cache_info(cache)[6:9] == [splits, 8, 9 * 32]
+        assert B.h2o_cache_info(cache)[6:9] == [splits, 8, 10 * 32]
     B.h2o_cache_set_decode_shape(cache, 1, 8)
     B.h2o_cache_set_position_rolling(cache, 0.0)  # off: the rolling shape does not carry over
     info = B.h2o_cache_info(cache)
