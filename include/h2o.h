@@ -180,6 +180,26 @@ H2O_API int h2o_cache_set_decode_shape(h2o_cache* cache, int splits, int stages)
  * shape to automatic).  Returns H2O_EINVAL for a negative or non-finite base. */
 H2O_API int h2o_cache_set_position_rolling(h2o_cache* cache, float rope_base);
 
+/* Tuning of position rolling (no counterpart in the pages; the result of a
+ * decode step does not depend on it).  A kept token's rank r is rotated as
+ * a product of per-digit rotations: the lowest digit of `low_bits` bits is
+ * folded into the query once per step, and each higher digit of `hi_bits`
+ * bits costs every key one rotation; the tables take 2^low_bits entries,
+ * 2^hi_bits per middle level and what the top digit reaches, each D/2 cos,
+ * sin pairs of shared memory per CTA.  Both in 4..6, or both 0 for the
+ * automatic choice (the fewest levels whose tables keep the automatic
+ * launch shape as resident as the smallest tables would; rolling starts
+ * with it).  Synchronous, like h2o_cache_set_position_rolling, and resets
+ * the launch shape to automatic.  Returns H2O_ESTATE when rolling is off,
+ * H2O_EINVAL for other widths or for widths whose tables cannot be
+ * scheduled. */
+H2O_API int h2o_cache_set_rolling_digits(h2o_cache* cache, int low_bits, int hi_bits);
+
+/* The digit layout in use: digits[0] low_bits, [1] hi_bits, [2] levels
+ * (digits of the largest rank), [3] table entries; all 0 when rolling is
+ * off.  digits: int32[4], host memory. */
+H2O_API int h2o_cache_rolling_digits(const h2o_cache* cache, int32_t* digits);
+
 /* Static sparse pattern combined with heavy hitters ("... 深度解读报告",
  * section 4.5, Table 2: Sparse Transformer strided / fixed patterns plus H2).
  * Positions offset, offset + stride, ..., offset + (count - 1) * stride are

@@ -47,6 +47,8 @@ SIGNATURES = {
                                            _c_void_p, _c_void_p]),
     "h2o_prefill_colsum_static_check": (_c_int, [_c_void_p]),
     "h2o_cache_set_position_rolling": (_c_int, [_c_void_p, _c_float]),
+    "h2o_cache_set_rolling_digits": (_c_int, [_c_void_p, _c_int, _c_int]),
+    "h2o_cache_rolling_digits": (_c_int, [_c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     "h2o_cache_set_static_pattern": (_c_int, [_c_void_p, _c_int, _c_int, _c_int]),
     "h2o_selftest_wait_timeout": (_c_int, [ctypes.c_uint, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_ulonglong)]),
     "h2o_debug_fail_alloc": (_c_int, [_c_int]),
@@ -239,6 +241,18 @@ def h2o_cache_set_decode_shape(cache: Cache, splits: int = 0, stages: int = 0):
 def h2o_cache_set_position_rolling(cache: Cache, rope_base: float):
     """Rotary embedding at positions inside the cache (0 turns it off)."""
     _check(lib().h2o_cache_set_position_rolling(cache.handle, float(rope_base)))
+
+
+def h2o_cache_set_rolling_digits(cache: Cache, low_bits: int = 0, hi_bits: int = 0):
+    """Digit widths of position rolling's rank decomposition (0, 0: automatic)."""
+    _check(lib().h2o_cache_set_rolling_digits(cache.handle, int(low_bits), int(hi_bits)))
+
+
+def h2o_cache_rolling_digits(cache: Cache) -> list[int]:
+    """[low_bits, hi_bits, levels, table entries] of position rolling (zeros when off)."""
+    d = (ctypes.c_int32 * 4)()
+    _check(lib().h2o_cache_rolling_digits(cache.handle, d))
+    return list(d)
 
 
 def h2o_cache_set_static_pattern(cache: Cache, offset: int, stride: int, count: int):

@@ -47,7 +47,9 @@
 #include <cuda_fp16.h>
 
 #include <array>
+#include <algorithm>
 #include <map>
+#include <vector>
 #include <mutex>
 
 #include "h2o_internal.cuh"
@@ -149,10 +151,10 @@ __device__ __forceinline__ void rope_rotate_level(float (&x)[EPV], const float2*
 }
 template <int EPV, int D, int LPR>
 __device__ __forceinline__ void rope_rotate_digits(float (&x)[EPV], const float2* tab, int r, int levels, int low,
-                                                   int lig) {
+                                                   int hi, int lig) {
 #pragma unroll
   for (int lv = 0; lv < 6; ++lv)
-    if (lv < levels) rope_rotate_level<EPV, D, LPR>(x, tab, rope_entry(r, lv, low), lig);
+    if (lv < levels) rope_rotate_level<EPV, D, LPR>(x, tab, rope_entry(r, lv, low, hi), lig);
 }
 // The same rotation on a key held as real parts re[h] = (x[4h], x[4h+2]) and
 // imaginary parts im[h] = (x[4h+1], x[4h+3]) of its pairs, two pairs per
@@ -185,7 +187,7 @@ __device__ __forceinline__ bool attend_tile(const unsigned char* sK, const unsig
                                             const float (&qv)[RowGeom<T, D>::EPV], float& m, float& l,
                                             float (&o)[RowGeom<T, D>::EPV], float* wb, float* lg, int lane,
                                             const int* rk = nullptr, const float2* tab = nullptr, int low = 4,
-                                            uint64_t* k_empty = nullptr, uint64_t* v_full = nullptr,
+                                            int hi = 4, uint64_t* k_empty = nullptr, uint64_t* v_full = nullptr,
                                             uint32_t v_par = 0) {
   using Gm = RowGeom<T, D>;
   constexpr int EPV = Gm::EPV, LPR = Gm::LPR, ROWB = Gm::ROWB;
@@ -212,8 +214,9 @@ __device__ __forceinline__ bool attend_tile(const unsigned char* sK, const unsig
         im[h] = make_float2(kf[4 * h + 1], kf[4 * h + 3]);
       }
 #pragma unroll
-      for (int lv = 1; lv <= KL; ++lv) rope_rotate_level2<NH, D, LPR>(re, im, tab, rope_entry(rr, lv, low), lig);
-      const float4* z = reinterpret_cast<const float4*>(tab + rope_entry(rr, 0, low) * (D / 2)) + lig;  // P0[d0]
+      for (int lv = 1; lv <= KL; ++lv)
+        rope_rotate_level2<NH, D, LPR>(re, im, tab, rope_entry(rr, lv, low, hi), lig);
+      const float4* z = reinterpret_cast<const float4*>(tab + rope_entry(rr, 0, low, hi) * (D / 2)) + lig;  // P0[d0]
       float2 a2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
@@ -508,7 +511,8 @@ __global__ void __launch_bounds__((NCW + producer_warps(ROPE)) * 32, NCW > 6 ? 2
       uint64_t* eb = part == 1 ? emptyv_bar : empty_bar;
       // position rolling: the rotation tables, constant while rolling is on,
       // so they are copied before any wait
-      const uint32_t tbytes = static_cast<uint32_t>(Lay::tab_bytes(rope_entries_for(C, prm.rope_low_bits)));
+      const uint32_t tbytes =
+          static_cast<uint32_t>(Lay::tab_bytes(rope_entries_for(C, prm.rope_low_bits, prm.rope_hi_bits)));
       if constexpr (ROPE) {
         if (part == 0) {
           mbar_arrive_expect_tx(tbar, tbytes);
@@ -636,13 +640,14 @@ __global__ void __launch_bounds__((NCW + producer_warps(ROPE)) * 32, NCW > 6 ? 2
     // every kept token
     if constexpr (ROPE) {
       if (!mbar_wait_bounded(tbar, 0u, kWaitLimit)) atomicOr(prm.err, ERR_MBAR_TIMEOUT);
-      rope_rotate_digits<EPV, D, LPR>(qv, rtab, count, prm.rope_levels, prm.rope_low_bits, lig);
+      rope_rotate_digits<EPV, D, LPR>(qv, rtab, count, prm.rope_levels, prm.rope_low_bits, prm.rope_hi_bits, lig);
     }
     if (rank == 0 && warp == 0) {
       // the new token attends to itself: row group 0 of warp 0 starts from it
       float kf[EPV];
       Vec16<T>::unpack(k4, kf);
-      if constexpr (ROPE) rope_rotate_digits<EPV, D, LPR>(kf, rtab, count, prm.rope_levels, prm.rope_low_bits, lig);
+      if constexpr (ROPE)
+        rope_rotate_digits<EPV, D, LPR>(kf, rtab, count, prm.rope_levels, prm.rope_low_bits, prm.rope_hi_bits, lig);
       float acc = 0.f;
 #pragma unroll
       for (int e = 0; e < EPV; ++e) acc = fmaf(qv[e], kf[e], acc);
@@ -697,32 +702,23 @@ __global__ void __launch_bounds__((NCW + producer_warps(ROPE)) * 32, NCW > 6 ? 2
       if constexpr (ROPE) {
         const int* rks = rk + t * TILE;
         float* lgs = lg + t * TILE;
-        const int low = prm.rope_low_bits;
+        const int low = prm.rope_low_bits, hi = prm.rope_hi_bits;
         uint64_t* ke = &empty_bar[s];  // the K half goes back inside attend_tile
         uint64_t* vf = &fullv_bar[s];
         const uint32_t par = static_cast<uint32_t>((t / NSTAGE) & 1);
         bool v_ok = true;
         switch (prm.rope_levels) {  // key-side rotations: the digits above the lowest
-          case 1: v_ok = attend_tile<T, D, TILE, true, 0>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low, ke, vf, par); break;
-          case 2: v_ok = attend_tile<T, D, TILE, true, 1>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low, ke, vf, par); break;
-          case 3: v_ok = attend_tile<T, D, TILE, true, 2>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low, ke, vf, par); break;
-          case 4: v_ok = attend_tile<T, D, TILE, true, 3>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low, ke, vf, par); break;
-          default: v_ok = attend_tile<T, D, TILE, true, 4>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low, ke, vf, par); break;
+          case 1: v_ok = attend_tile<T, D, TILE, true, 0>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low, hi, ke, vf, par); break;
+          case 2: v_ok = attend_tile<T, D, TILE, true, 1>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low, hi, ke, vf, par); break;
+          case 3: v_ok = attend_tile<T, D, TILE, true, 2>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low, hi, ke, vf, par); break;
+          case 4: v_ok = attend_tile<T, D, TILE, true, 3>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low, hi, ke, vf, par); break;
+          default: v_ok = attend_tile<T, D, TILE, true, 4>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lgs, lane, rks, rtab, low, hi, ke, vf, par); break;
         }
         if (!v_ok) {
           ok = false;
           if (lane == 0) atomicOr(prm.err, ERR_MBAR_TIMEOUT);
         }
         // the V half may be refilled; after a timeout it is not released
-        if (lane == 0 && ok) mbar_arrive(&emptyv_bar[s]);
-      } else if constexpr (SPLIT) {
-        const bool v_ok = attend_tile<T, D, TILE>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lg + t * TILE, lane,
-                                                  nullptr, nullptr, 4, &empty_bar[s], &fullv_bar[s],
-                                                  static_cast<uint32_t>((t / NSTAGE) & 1));
-        if (!v_ok) {
-          ok = false;
-          if (lane == 0) atomicOr(prm.err, ERR_MBAR_TIMEOUT);
-        }
         if (lane == 0 && ok) mbar_arrive(&emptyv_bar[s]);
       } else {
         attend_tile<T, D, TILE>(sK, sK + TILE * ROWB, rows, qv, m, l, o, wb, lg + t * TILE, lane);
@@ -1228,7 +1224,7 @@ struct Kern {
   static cudaError_t attrs() {
     // raised once for the largest configuration, so later launches (also
     // inside stream capture) make no attribute calls
-    size_t most = Lay::bytes(kMaxStages, kMaxChunk, 16, rope_entries_for(65536, rope_low_bits_for(65536)));
+    size_t most = Lay::bytes(kMaxStages, kMaxChunk, 16, rope_entries_for(65536, kRopeMinBits, kRopeMinBits));
     if (most > 227 * 1024) most = 227 * 1024;
     return kernel_attrs(reinterpret_cast<const void*>(fn), most, true);
   }
@@ -1240,7 +1236,8 @@ struct Kern {
     cfg.gridDim = dim3(splits, pairs, 1);
     cfg.blockDim = dim3(Cfg::NT, 1, 1);
     cfg.dynamicSmemBytes =
-        smem(prm.nstage, prm.chunk, splits, prm.rope ? rope_entries_for(prm.C, prm.rope_low_bits) : 0);
+        smem(prm.nstage, prm.chunk, splits,
+             prm.rope ? rope_entries_for(prm.C, prm.rope_low_bits, prm.rope_hi_bits) : 0);
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1350,7 +1347,8 @@ int decode_warp_default_stages(int dtype, int D, int C, int pairs) {
   return 2;
 }
 
-DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C, bool rope) {
+DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C, int rope_entries) {
+  const bool rope = rope_entries > 0;
   const int sms = device_sms();
   // position rolling runs on the cluster kernel only
   if (!rope && sms > 0 && C <= kWarpMaxSlots && pairs >= 4 * sms && decode_warp_resident(dtype, D, 2, C) > 0) {
@@ -1378,8 +1376,7 @@ DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C, bool rope) {
     const int ch = chunk_for(C, sh.splits);
     const int deep = ncw <= 12 ? 12 / ncw * ncw : ncw;
     for (int st : {deep, ncw == 4 ? 8 : ncw}) {
-      const int res =
-          decode_resident(dtype, D, sh.splits, st, ch, pairs, rope ? rope_entries_for(C, rope_low_bits_for(C)) : 0);
+      const int res = decode_resident(dtype, D, sh.splits, st, ch, pairs, rope_entries);
       if (res >= 2 * sms || static_cast<long long>(res) >= ctas) {
         sh.stages = st;
         break;
@@ -1387,6 +1384,40 @@ DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C, bool rope) {
     }
   }
   return sh;
+}
+
+RopeRadix decode_pick_rope_radix(int dtype, int D, int pairs, int C) {
+  // candidates by levels, then entries; the smallest tables set the bar
+  struct Cand {
+    int levels, entries, low, hi;
+  };
+  Cand best{0, 0, 0, 0}, least{0, 0, 0, 0};
+  std::vector<Cand> all;
+  for (int low = kRopeMinBits; low <= kRopeMaxBits; ++low)
+    for (int hi = kRopeMinBits; hi <= kRopeMaxBits; ++hi)
+      all.push_back({rope_levels_for(C, low, hi), rope_entries_for(C, low, hi), low, hi});
+  std::sort(all.begin(), all.end(), [](const Cand& a, const Cand& b) {
+    if (a.levels != b.levels) return a.levels < b.levels;
+    if (a.entries != b.entries) return a.entries < b.entries;
+    return a.low != b.low ? a.low < b.low : a.hi < b.hi;
+  });
+  for (const Cand& c : all)
+    if (least.entries == 0 || c.entries < least.entries) least = c;
+  auto resident = [&](int entries) {
+    const DecodeShape sh = decode_pick_shape(dtype, D, pairs, C, entries);
+    return std::make_pair(sh.stages, decode_resident(dtype, D, sh.splits, sh.stages, chunk_for(C, sh.splits), pairs,
+                                                     entries));
+  };
+  const auto bar = resident(least.entries);
+  best = least;
+  for (const Cand& c : all) {
+    const auto r = resident(c.entries);
+    if (r.first >= bar.first && r.second >= bar.second) {
+      best = c;
+      break;
+    }
+  }
+  return RopeRadix{best.low, best.hi};
 }
 
 int decode_warp_max_slots() { return kWarpMaxSlots; }
@@ -1444,8 +1475,9 @@ cudaError_t launch_decode(const DecodeParams& prm, int dtype, int D, int pairs, 
     return WarpKern<float, 64>::launch(prm, ctas, s);
   }
   if (prm.rope != nullptr &&
-      (prm.rank == nullptr || (prm.rope_low_bits != 4 && prm.rope_low_bits != 5) ||
-       prm.rope_levels != rope_levels_for(prm.C, prm.rope_low_bits) || prm.rope_levels > 5))
+      (prm.rank == nullptr || prm.rope_low_bits < kRopeMinBits || prm.rope_low_bits > kRopeMaxBits ||
+       prm.rope_hi_bits < kRopeMinBits || prm.rope_hi_bits > kRopeMaxBits ||
+       prm.rope_levels != rope_levels_for(prm.C, prm.rope_low_bits, prm.rope_hi_bits) || prm.rope_levels > 5))
     return cudaErrorInvalidValue;
   return dispatch(dtype, D, splits, prm.rope != nullptr,
                   [&](auto k) { return decltype(k)::launch(prm, pairs, splits, s); });

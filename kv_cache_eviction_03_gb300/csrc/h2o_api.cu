@@ -419,8 +419,9 @@ int h2o_decode_step(h2o_cache* c, const void* q, const void* k_new, const void* 
   dp.pairs = c->P;
   dp.rank = c->rank;
   dp.rope = c->rope;
-  dp.rope_low_bits = h2o::rope_low_bits_for(c->C);
-  dp.rope_levels = c->rope ? h2o::rope_levels_for(c->C, dp.rope_low_bits) : 0;
+  dp.rope_low_bits = c->rope_low;
+  dp.rope_hi_bits = c->rope_hi;
+  dp.rope_levels = c->rope ? h2o::rope_levels_for(c->C, c->rope_low, c->rope_hi) : 0;
   dp.sp = c->sp;
 #ifdef H2O_DECODE_TIMELINE
   dp.tl_slot = static_cast<int>(g_tl_next.fetch_add(1) % h2o::kTimelineSlots);
@@ -577,7 +578,7 @@ int h2o_cache_set_decode_shape(h2o_cache* c, int splits, int stages) {
       return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: %d splits leave more than %d slots per CTA", s,
                   h2o::decode_max_chunk());
     if (h2o::decode_resident(c->dtype, c->D, s, n, chunk_for(c->C, s), c->P,
-                             c->rope ? h2o::rope_entries_for(c->C, h2o::rope_low_bits_for(c->C)) : 0) < s)
+                             c->rope ? h2o::rope_entries_for(c->C, c->rope_low, c->rope_hi) : 0) < s)
       return fail(H2O_EINVAL, "h2o_cache_set_decode_shape: %d CTAs per pair with %d stages cannot be scheduled", s,
                   n);
   }
@@ -613,13 +614,18 @@ int h2o_cache_info(const h2o_cache* c, int32_t* info) {
   return H2O_OK;
 }
 
-int h2o_cache_set_position_rolling(h2o_cache* c, float rope_base) {
-  NvtxRange nvtx("h2o_cache_set_position_rolling");
-  if (!c) return fail(H2O_EINVAL, "h2o_cache_set_position_rolling: cache is NULL");
-  if (!(rope_base >= 0.f) || !std::isfinite(rope_base))
-    return fail(H2O_EINVAL, "h2o_cache_set_position_rolling: rope_base must be finite and >= 0 (0 = off)");
+namespace {
+// Position rolling on with this base and these digit widths (0, 0: the
+// automatic ones), or off (base 0): ranks from the positions, rotation
+// tables, launch shape.  `who` names the calling entry point in errors.
+int set_rolling(h2o_cache* c, float rope_base, int low_req, int hi_req, const char* who) {
+  char what_buf[160];
+  auto what = [&](const char* step) {
+    snprintf(what_buf, sizeof(what_buf), "%s: %s", who, step);
+    return what_buf;
+  };
   cudaError_t e = cudaDeviceSynchronize();  // the positions are read back below
-  if (e != cudaSuccess) return cuda_fail(e, "h2o_cache_set_position_rolling: synchronise");
+  if (e != cudaSuccess) return cuda_fail(e, what("synchronise"));
   if (rope_base == 0.f) {
     cudaFree(c->rank);
     cudaFree(c->rope);
@@ -628,31 +634,33 @@ int h2o_cache_set_position_rolling(h2o_cache* c, float rope_base) {
     c->rope_base = 0.f;
     // the plain kernel's own launch shape: an explicit one set for rolling
     // (ring depths in multiples of its consumer warps) goes back to automatic
-    c->shape_auto = h2o::decode_pick_shape(c->dtype, c->D, c->P, c->C, false);
+    c->shape_auto = h2o::decode_pick_shape(c->dtype, c->D, c->P, c->C, 0);
     c->splits_override = 0;
     c->stages_override = 0;
     return H2O_OK;
   }
   const size_t nslot = static_cast<size_t>(c->P) * c->C;
-  const int low = h2o::rope_low_bits_for(c->C);           // bits of the ranks' lowest digit
-  const int levels = h2o::rope_levels_for(c->C, low);     // digits of the ranks 0..C
-  const int entries = h2o::rope_entries_for(c->C, low);   // table entries those digits take
+  const h2o::RopeRadix radix = low_req > 0 ? h2o::RopeRadix{low_req, hi_req}
+                                           : h2o::decode_pick_rope_radix(c->dtype, c->D, c->P, c->C);
+  const int low = radix.low, hi = radix.hi;                  // bits of the ranks' lowest digit, of the others
+  const int levels = h2o::rope_levels_for(c->C, low, hi);    // digits of the ranks 0..C
+  const int entries = h2o::rope_entries_for(c->C, low, hi);  // table entries those digits take
   const size_t ntab = static_cast<size_t>(entries) * (c->D / 2);
   // Everything is built into new buffers and swapped in only once it is
   // complete, so a failure leaves the cache exactly as it was.
   int* rank = nullptr;
   float2* rope = nullptr;
-  auto give_up = [&](cudaError_t err, const char* what) {
+  auto give_up = [&](cudaError_t err, const char* step) {
     cudaFree(rank);
     cudaFree(rope);
-    return cuda_fail(err, what);
+    return cuda_fail(err, what(step));
   };
   if ((e = dev_alloc(&rank, nslot * sizeof(int))) != cudaSuccess ||
       (e = dev_alloc(&rope, ntab * sizeof(float2))) != cudaSuccess)
-    return give_up(e, "h2o_cache_set_position_rolling: cudaMalloc");
+    return give_up(e, "cudaMalloc");
   // rotation tables of the ranks' digits: the entry of level l's digit d
   // (h2o::rope_entry) holds, for every pair i, cos and sin of
-  // d * w_l * base^(-2i/D), w_0 = 1 and w_l = 2^(low + 4(l-1)), computed in
+  // d * w_l * base^(-2i/D), w_0 = 1 and w_l = 2^(low + hi(l-1)), computed in
   // double and stored as float in the order the decode lanes read them: a
   // row's LPR lanes take EPV elements (EPV / 2 pairs) each, and float4
   // h * LPR + g of an entry holds lane g's pairs 2h and 2h + 1 as
@@ -662,10 +670,10 @@ int h2o_cache_set_position_rolling(h2o_cache* c, float rope_base) {
   for (int e = 0; e < entries; ++e) {
     int lv = 0, d = e;  // level and digit of entry e
     if (levels > 1 && e >= (1 << low)) {
-      lv = 1 + (e - (1 << low)) / 16;
-      d = (e - (1 << low)) % 16;
+      lv = 1 + (e - (1 << low)) / (1 << hi);
+      d = (e - (1 << low)) % (1 << hi);
     }
-    const double w = lv == 0 ? 1.0 : std::ldexp(1.0, low + 4 * (lv - 1));
+    const double w = lv == 0 ? 1.0 : std::ldexp(1.0, low + hi * (lv - 1));
     for (int i = 0; i < c->D / 2; ++i) {
       const double ang = d * w * std::pow(static_cast<double>(rope_base), -2.0 * i / c->D);
       const int g = i / (epv / 2), h = (i % (epv / 2)) / 2, x = i % 2;  // lane, float4 of the lane, pair in it
@@ -677,21 +685,62 @@ int h2o_cache_set_position_rolling(h2o_cache* c, float rope_base) {
   }
   std::vector<int> pos(nslot), ranks;
   if ((e = cudaMemcpy(pos.data(), c->pos, nslot * sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
-    return give_up(e, "h2o_cache_set_position_rolling: read positions");
+    return give_up(e, "read positions");
   ranks_from_positions(pos.data(), c->P, c->C, ranks);
   if ((e = cudaMemcpy(rope, tab.data(), ntab * sizeof(float2), cudaMemcpyHostToDevice)) != cudaSuccess ||
       (e = cudaMemcpy(rank, ranks.data(), nslot * sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess)
-    return give_up(e, "h2o_cache_set_position_rolling: upload");
+    return give_up(e, "upload");
   cudaFree(c->rank);
   cudaFree(c->rope);
   c->rank = rank;
   c->rope = rope;
   c->rope_base = rope_base;
+  c->rope_low = low;
+  c->rope_hi = hi;
   // the cluster kernel with one more int of shared memory per slot; a
   // warp-per-pair or explicit shape goes back to the automatic one
-  c->shape_auto = h2o::decode_pick_shape(c->dtype, c->D, c->P, c->C, true);
+  c->shape_auto = h2o::decode_pick_shape(c->dtype, c->D, c->P, c->C, entries);
   c->splits_override = 0;
   c->stages_override = 0;
+  return H2O_OK;
+}
+}  // namespace
+
+int h2o_cache_set_position_rolling(h2o_cache* c, float rope_base) {
+  NvtxRange nvtx("h2o_cache_set_position_rolling");
+  if (!c) return fail(H2O_EINVAL, "h2o_cache_set_position_rolling: cache is NULL");
+  if (!(rope_base >= 0.f) || !std::isfinite(rope_base))
+    return fail(H2O_EINVAL, "h2o_cache_set_position_rolling: rope_base must be finite and >= 0 (0 = off)");
+  return set_rolling(c, rope_base, 0, 0, "h2o_cache_set_position_rolling");
+}
+
+int h2o_cache_set_rolling_digits(h2o_cache* c, int low_bits, int hi_bits) {
+  NvtxRange nvtx("h2o_cache_set_rolling_digits");
+  if (!c) return fail(H2O_EINVAL, "h2o_cache_set_rolling_digits: cache is NULL");
+  if (!c->rope) return fail(H2O_ESTATE, "h2o_cache_set_rolling_digits: position rolling is off");
+  const bool automatic = low_bits == 0 && hi_bits == 0;
+  if (!automatic && (low_bits < h2o::kRopeMinBits || low_bits > h2o::kRopeMaxBits || hi_bits < h2o::kRopeMinBits ||
+                     hi_bits > h2o::kRopeMaxBits))
+    return fail(H2O_EINVAL, "h2o_cache_set_rolling_digits: digit widths must be %d..%d bits (or both 0)",
+                h2o::kRopeMinBits, h2o::kRopeMaxBits);
+  if (!automatic) {
+    const int levels = h2o::rope_levels_for(c->C, low_bits, hi_bits);
+    const h2o::DecodeShape sh =
+        h2o::decode_pick_shape(c->dtype, c->D, c->P, c->C, h2o::rope_entries_for(c->C, low_bits, hi_bits));
+    if (levels > 5 || h2o::decode_resident(c->dtype, c->D, sh.splits, sh.stages, chunk_for(c->C, sh.splits), c->P,
+                                           h2o::rope_entries_for(c->C, low_bits, hi_bits)) < sh.splits)
+      return fail(H2O_EINVAL, "h2o_cache_set_rolling_digits: %d + %d-bit digits cannot be scheduled for %d slots",
+                  low_bits, hi_bits, c->C);
+  }
+  return set_rolling(c, c->rope_base, low_bits, hi_bits, "h2o_cache_set_rolling_digits");
+}
+
+int h2o_cache_rolling_digits(const h2o_cache* c, int32_t* digits) {
+  if (!c || !digits) return fail(H2O_EINVAL, "h2o_cache_rolling_digits: NULL argument");
+  digits[0] = c->rope ? c->rope_low : 0;
+  digits[1] = c->rope ? c->rope_hi : 0;
+  digits[2] = c->rope ? h2o::rope_levels_for(c->C, c->rope_low, c->rope_hi) : 0;
+  digits[3] = c->rope ? h2o::rope_entries_for(c->C, c->rope_low, c->rope_hi) : 0;
   return H2O_OK;
 }
 

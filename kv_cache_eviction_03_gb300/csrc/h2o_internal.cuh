@@ -37,29 +37,27 @@ __host__ __device__ __forceinline__ bool is_protected(const StaticPattern& sp, i
 }
 
 // Position rolling: a rank r is split into digits, the lowest of `low` bits
-// (4 or 5) and base-16 digits above it; level l's digit selects one entry of
-// that level's rotation table.  rope_levels_for: the digits every rank
+// and digits of `hi` bits above it; level l's digit selects one entry of that
+// level's rotation table.  rope_levels_for: the digits every rank
 // 0..max_rank needs; rope_entries_for: the table entries they take (2^low on
-// level 0, 16 on the levels between, and only as many as the top digit
-// reaches on the top level); rope_low_bits_for: 5 when that saves a level
-// (e.g. ranks up to 511 in two digits instead of three), else 4.
-__host__ __device__ __forceinline__ int rope_levels_for(int max_rank, int low) {
+// level 0, 2^hi on the levels between, and only as many as the top digit
+// reaches on the top level).  rope_entry: the entry of level l's digit of r.
+__host__ __device__ __forceinline__ int rope_levels_for(int max_rank, int low, int hi) {
   int l = 1;
-  while (l < 6 && (1 << (low + 4 * (l - 1))) <= max_rank) ++l;
+  while (l < 6 && (1LL << (low + hi * (l - 1))) <= max_rank) ++l;
   return l;
 }
-__host__ __device__ __forceinline__ int rope_entries_for(int max_rank, int low) {
-  const int l = rope_levels_for(max_rank, low);
+__host__ __device__ __forceinline__ int rope_entries_for(int max_rank, int low, int hi) {
+  const int l = rope_levels_for(max_rank, low, hi);
   if (l == 1) return max_rank + 1;
-  return (1 << low) + 16 * (l - 2) + (max_rank >> (low + 4 * (l - 2))) + 1;
+  return (1 << low) + (1 << hi) * (l - 2) + (max_rank >> (low + hi * (l - 2))) + 1;
 }
-__host__ __device__ __forceinline__ int rope_low_bits_for(int max_rank) {
-  return rope_levels_for(max_rank, 5) < rope_levels_for(max_rank, 4) ? 5 : 4;
+__host__ __device__ __forceinline__ int rope_entry(int r, int l, int low, int hi) {
+  return l == 0 ? (r & ((1 << low) - 1))
+                : (1 << low) + (1 << hi) * (l - 1) + ((r >> (low + hi * (l - 1))) & ((1 << hi) - 1));
 }
-// entry of level l's digit of rank r (see above)
-__host__ __device__ __forceinline__ int rope_entry(int r, int l, int low) {
-  return l == 0 ? (r & ((1 << low) - 1)) : (1 << low) + 16 * (l - 1) + ((r >> (low + 4 * (l - 1))) & 15);
-}
+// digit widths the kernel takes: low 4..6 bits, hi 4..6 bits
+constexpr int kRopeMinBits = 4, kRopeMaxBits = 6;
 
 // Per-pair counters kept on the device so decode steps can be replayed from
 // a CUDA graph: next absolute position, occupied slots, ring head.
@@ -93,16 +91,18 @@ struct DecodeParams {
   int pairs;          // P
   // position rolling (rotary embedding at positions inside the cache), or
   // both nullptr: the rank of each slot among the kept tokens in text order,
-  // and the rotation tables of the ranks' digits: entry rope_entry(., l, low)
-  // of digit d holds (cos, sin) of d * (weight of level l) * base^(-2i/D),
-  // level 0 weighing 1 and level l 2^(low + 4(l-1)), for every pair i < D/2, in
-  // lane order (float4 h * LPR + g holds pairs g * EPV/2 + 2h and + 2h + 1,
-  // where a row's LPR lanes take EPV elements each), so that the lanes of a
-  // row read consecutive 16-byte words
+  // and the rotation tables of the ranks' digits: entry rope_entry(., l, low,
+  // hi) of digit d holds cos and sin of d * (weight of level l) *
+  // base^(-2i/D), level 0 weighing 1 and level l 2^(low + hi(l-1)), for every
+  // pair i < D/2, in lane order (float4 h * LPR + g holds the cosines, then
+  // the sines, of pairs g * EPV/2 + 2h and + 2h + 1, where a row's LPR lanes
+  // take EPV elements each), so that the lanes of a row read consecutive
+  // 16-byte words
   int* rank;           // [P, C]
-  const float2* rope;  // [rope_entries_for(C, rope_low_bits), D / 2]
+  const float2* rope;  // [rope_entries_for(C, rope_low_bits, rope_hi_bits), D / 2]
   int rope_levels;     // digits of the largest rank, C (rope_levels_for)
-  int rope_low_bits;   // bits of the lowest digit (rope_low_bits_for)
+  int rope_low_bits;   // bits of the lowest digit
+  int rope_hi_bits;    // bits of each digit above it
   StaticPattern sp;    // protected positions, never eviction candidates
 #ifdef H2O_DECODE_TIMELINE
   int tl_slot;  // profiling build: which stamp buffer this launch writes
@@ -187,9 +187,16 @@ struct DecodeShape {
   int splits;  // CTAs (one cluster) per pair, or kDecodeWarpPerPair
   int stages;  // shared-memory ring depth per CTA (per warp in warp-per-pair mode)
 };
-// rope: the cache uses position rolling (cluster kernel only, one more int
-// of shared memory per slot)
-DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C, bool rope = false);
+// rope_entries: position rolling's rotation-table entries (cluster kernel
+// only, one more int of shared memory per slot), 0 when off
+DecodeShape decode_pick_shape(int dtype, int D, int pairs, int C, int rope_entries = 0);
+// Position rolling's digit widths for a shape: the fewest levels whose
+// tables still leave the automatic launch shape as many resident CTAs as the
+// smallest tables do, then the fewest entries.
+struct RopeRadix {
+  int low, hi;
+};
+RopeRadix decode_pick_rope_radix(int dtype, int D, int pairs, int C);
 // CTAs of this shape that fit on the device at once (0: cannot launch);
 // rope_entries: position rolling's rotation-table entries, 0 when off
 int decode_resident(int dtype, int D, int splits, int nstage, int chunk, int pairs, int rope_entries = 0);
@@ -241,9 +248,10 @@ struct h2o_cache {
   h2o::DecodeShape shape_auto;
   long long host_next_p;  // host mirror of the next position (overflow check)
   // position rolling: slot ranks [P, C] and the digit rotation tables
-  // [rope_levels_for(C), 16, D/2]; nullptr when off
+  // [rope_entries_for(C, rope_low, rope_hi), D/2]; nullptr when off
   int* rank;
   float2* rope;
   float rope_base;
+  int rope_low, rope_hi;  // the ranks' digit widths (decode_pick_rope_radix)
   h2o::StaticPattern sp;  // static sparse pattern (count 0: none)
 };

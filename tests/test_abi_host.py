@@ -62,6 +62,9 @@ def test_null_cache_is_rejected_everywhere():
     assert lib.h2o_cache_check(None, None) == -1
     assert lib.h2o_cache_set_decode_shape(None, 2, 0) == -1
     assert lib.h2o_cache_info(None, None) == -1
+    assert lib.h2o_cache_set_position_rolling(None, 10000.0) == -1
+    assert lib.h2o_cache_set_rolling_digits(None, 4, 4) == -1
+    assert lib.h2o_cache_rolling_digits(None, None) == -1
     assert lib.h2o_cache_state_bytes(None) == 0
     lib.h2o_cache_destroy(None)  # NULL-safe
     with pytest.raises(B.H2OError) as ei:

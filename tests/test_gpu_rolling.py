@@ -110,15 +110,19 @@ def test_rolling_after_import_mid_stream():
 
 
 STEPWISE = [
-    # name, batch, heads, D, dtype, heavy, recent, steps, CTAs per pair (0: automatic)
-    ("sw-f16-d128-auto", 1, 3, 128, "f16", 20, 12, 64, 0),
-    ("sw-f32-d64-s2", 2, 2, 64, "f32", 24, 16, 60, 2),
-    ("sw-f16-d128-s8", 1, 2, 128, "f16", 70, 30, 130, 8),
-    # ranks 0..C in two digits with a 5-bit lowest one (C in 256..511), and in
-    # a single 5-bit digit (C in 16..31): the tables' other layouts
-    ("sw-f16-d128-low5", 1, 2, 128, "f16", 180, 120, 330, 0),
-    ("sw-f32-d128-low5-s2", 1, 2, 128, "f32", 260, 200, 480, 2),
-    ("sw-f16-d64-one-level", 1, 3, 64, "f16", 12, 8, 45, 0),
+    # name, batch, heads, D, dtype, heavy, recent, steps, CTAs per pair (0: automatic),
+    # digit widths (low, hi) of the ranks (None: automatic)
+    ("sw-f16-d128-auto", 1, 3, 128, "f16", 20, 12, 64, 0, None),
+    ("sw-f32-d64-s2", 2, 2, 64, "f32", 24, 16, 60, 2, None),
+    ("sw-f16-d128-s8", 1, 2, 128, "f16", 70, 30, 130, 8, None),
+    # ranks 0..C (C = 300, 460) in two digits (automatic: 4 + 5 bits), three
+    # (4 + 4 + 4 bits: two key-side rotations) and two with a wide lowest
+    # digit (6 + 4); and in a single digit (C = 20)
+    ("sw-f16-d128-two-levels", 1, 2, 128, "f16", 180, 120, 330, 0, None),
+    ("sw-f16-d128-three-levels", 1, 2, 128, "f16", 180, 120, 330, 0, (4, 4)),
+    ("sw-f32-d128-three-levels-s2", 1, 2, 128, "f32", 260, 200, 480, 2, (4, 4)),
+    ("sw-f16-d64-wide-low-s4", 1, 2, 64, "f16", 260, 200, 480, 4, (6, 4)),
+    ("sw-f16-d64-one-level", 1, 3, 64, "f16", 12, 8, 45, 0, None),
 ]
 
 
@@ -129,11 +133,16 @@ def test_rolling_stepwise_from_oracle_states(case):
     it, so ranks and positions differ: outputs, victims (a different one only
     at a near tie, and only an equally low candidate), scores, slots, ring and
     counters through the step-wise comparison."""
-    name, Bn, H, D, dt, heavy, recent, steps, splits = case
+    name, Bn, H, D, dt, heavy, recent, steps, splits, digits = case
     w = W.Workload(name, Bn, H, D, dt, 0, steps, heavy, recent, 1.1)
     code = B.H2O_F16 if dt == "f16" else B.H2O_F32
     cache = B.h2o_cache_create(Bn, H, D, heavy, recent, code)
     B.h2o_cache_set_position_rolling(cache, BASE)
+    if digits:
+        B.h2o_cache_set_rolling_digits(cache, *digits)
+        low, hi, levels, entries = B.h2o_cache_rolling_digits(cache)
+        C = heavy + recent
+        assert (low, hi) == digits and (1 << (low + hi * (levels - 2))) <= C < (1 << (low + hi * (levels - 1)))
     if splits:
         B.h2o_cache_set_decode_shape(cache, splits)
     st = O.empty_cache(w.pairs, heavy, recent, D)
@@ -196,4 +205,39 @@ def test_rolling_launch_shape_rules():
     assert info[8] in (5 * 32, 7 * 32) and info[7] % (info[8] // 32 - 1) == 0
     B.h2o_cache_set_decode_shape(cache, 1, 12)
     assert B.h2o_cache_info(cache)[7:9] == [12, 7 * 32]
+    B.h2o_cache_destroy(cache)
+
+
+def test_rolling_digit_choice():
+    """The automatic digit widths: one level when every rank fits the lowest
+    digit, two where those tables still fit beside the ring (the OPT-6.7B
+    cache shape, 1000 slots of 128-wide heads), three where two levels'
+    tables would cost resident CTAs (the LLaMA-7B 16K shape, 1640 slots, whose
+    two-level tables miss two CTAs per SM by a few entries; 2048 slots).
+    Explicit widths are checked and reported; the automatic ones come back
+    with (0, 0)."""
+    def digits(Bn, H, D, heavy, recent):
+        cache = B.h2o_cache_create(Bn, H, D, heavy, recent, B.H2O_F16)
+        assert B.h2o_cache_rolling_digits(cache) == [0, 0, 0, 0]
+        with pytest.raises(B.H2OError):
+            B.h2o_cache_set_rolling_digits(cache, 4, 4)  # rolling is off
+        B.h2o_cache_set_position_rolling(cache, BASE)
+        d = B.h2o_cache_rolling_digits(cache)
+        B.h2o_cache_destroy(cache)
+        return d
+    assert digits(1, 2, 64, 12, 8)[2] == 1
+    assert digits(8, 32, 128, 205, 205)[2] == 2
+    assert digits(1, 32, 128, 500, 500)[2] == 2
+    assert digits(1, 32, 128, 820, 820)[2] == 3
+    assert digits(4, 32, 128, 1024, 1024)[2] == 3
+    cache = B.h2o_cache_create(1, 2, 64, 100, 60, B.H2O_F16)
+    B.h2o_cache_set_position_rolling(cache, BASE)
+    auto = B.h2o_cache_rolling_digits(cache)
+    for bad in ((3, 4), (4, 7), (0, 4)):
+        with pytest.raises(B.H2OError):
+            B.h2o_cache_set_rolling_digits(cache, *bad)
+    B.h2o_cache_set_rolling_digits(cache, 4, 4)
+    assert B.h2o_cache_rolling_digits(cache) == [4, 4, 2, 16 + (160 >> 4) + 1]
+    B.h2o_cache_set_rolling_digits(cache, 0, 0)
+    assert B.h2o_cache_rolling_digits(cache) == auto
     B.h2o_cache_destroy(cache)
