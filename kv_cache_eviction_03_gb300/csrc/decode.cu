@@ -745,17 +745,31 @@ __global__ void __launch_bounds__((NCW + producer_warps(ROPE)) * 32, NCW > 6 ? 2
     cp_async_wait<0>();  // this thread's score and position copies have landed
     consumer_sync(NCW * 32);
     H2O_TL(4);
+    // A pair handled by one CTA needs no cluster or distributed shared
+    // memory.  In a cluster, every CTA pushes its partial softmax (m, l) into
+    // each peer's xin[rank] as soon as it is merged over the warps, and the
+    // other ranks then push their partial output rows into rank 0, all with
+    // st.async counted on the receiver's xbar: each CTA waits only for the
+    // bytes it receives, never on a cluster barrier.  Threads below D (whole
+    // consumer warps) do all of a CTA's pushes.
     if (tid < D) {
       float M = kNeg;
       for (int w = 0; w < NCW; ++w) M = fmaxf(M, red_of(w)[0]);
-      float Ls = 0.f, Od = 0.f;
-      for (int w = 0; w < NCW; ++w) {
-        const float* rw = red_of(w);
-        const float a = exp2f(rw[0] - M);
-        Ls = fmaf(rw[1], a, Ls);
-        Od = fmaf(rw[4 + tid], a, Od);
+      float Ls = 0.f;
+      for (int w = 0; w < NCW; ++w) Ls = fmaf(red_of(w)[1], exp2f(red_of(w)[0] - M), Ls);
+      if (S > 1) {
+        cluster_wait_acquire();  // every peer has started and set up its barriers
+        if (tid < S && tid != rank) {
+          const uint4 v = make_uint4(__float_as_uint(M), __float_as_uint(Ls), __float_as_uint(s_self), 0u);
+          st_async_v4(mapa_shared(smem_u32(&xin[rank]), tid), v, mapa_shared(smem_u32(xbar), tid));
+        }
       }
+      float Od = 0.f;
+      for (int w = 0; w < NCW; ++w) Od = fmaf(red_of(w)[4 + tid], exp2f(red_of(w)[0] - M), Od);
       xo[tid] = Od;
+      if (S > 1 && rank != 0)
+        st_async_b32(mapa_shared(smem_u32(xo_in + (rank - 1) * D + tid), 0), __float_as_uint(Od),
+                     mapa_shared(smem_u32(xbar), 0));
       if (tid == 0) {
         xch->m = M;
         xch->l = Ls;
@@ -764,27 +778,9 @@ __global__ void __launch_bounds__((NCW + producer_warps(ROPE)) * 32, NCW > 6 ? 2
       }
     }
   }
-  // A pair handled by one CTA needs no cluster or distributed shared
-  // memory.  In a cluster, every CTA pushes its partial softmax (m, l) into
-  // each peer's xin[rank] and the other ranks push their partial output rows
-  // into rank 0, all with st.async counted on the receiver's xbar: each CTA
-  // waits only for the bytes it receives, never on a cluster barrier.
   const bool clustered = S > 1;
-  if (clustered) {
-    __syncthreads();         // xo / xch of this CTA are complete (all threads)
-    cluster_wait_acquire();  // every peer has started and set up its barriers
-    if (tid < S && tid != rank) {
-      const uint4 v = make_uint4(__float_as_uint(xch->m), __float_as_uint(xch->l), __float_as_uint(xch->s_self), 0u);
-      st_async_v4(mapa_shared(smem_u32(&xin[rank]), tid), v, mapa_shared(smem_u32(xbar), tid));
-    }
-    if (rank != 0 && tid < D / 4) {
-      const uint4 v = *reinterpret_cast<const uint4*>(xo + tid * 4);
-      st_async_v4(mapa_shared(smem_u32(xo_in + (rank - 1) * D + tid * 4), 0), v, mapa_shared(smem_u32(xbar), 0));
-    }
-    if (!mbar_wait_cluster_bounded(xbar, 0, kWaitLimit) && tid == 0) atomicOr(prm.err, ERR_XCH_TIMEOUT);
-  } else {
-    __syncthreads();
-  }
+  __syncthreads();  // xo / xch / xin[rank] of this CTA are complete (all threads)
+  if (clustered && !mbar_wait_cluster_bounded(xbar, 0, kWaitLimit) && tid == 0) atomicOr(prm.err, ERR_XCH_TIMEOUT);
   H2O_TL(5);
 
   // the pair's normaliser: merged over the cluster's CTAs, or, for a pair
@@ -807,33 +803,79 @@ __global__ void __launch_bounds__((NCW + producer_warps(ROPE)) * 32, NCW > 6 ? 2
   const float inv = 1.f / Ls;
   const float p_self = exp2f(sself - M) * inv;
 
-  if (rank == 0 && tid < D) {
-    float acc = xo[tid];
-    if (clustered) {
-      acc = 0.f;
-      for (int r = 0; r < S; ++r) acc = fmaf(r == 0 ? xo[tid] : xo_in[(r - 1) * D + tid], exp2f(xin[r].m - M), acc);
+  // the pair's output row (rank 0): with position rolling written once this
+  // CTA's candidate is on its way to the peers (measured faster there), else
+  // right away (measured faster for the plain kernel's 8-CTA clusters)
+  auto write_output = [&]() {
+    if (rank == 0 && tid < D) {
+      float acc = xo[tid];
+      if (clustered) {
+        acc = 0.f;
+        for (int r = 0; r < S; ++r)
+          acc = fmaf(r == 0 ? xo[tid] : xo_in[(r - 1) * D + tid], exp2f(xin[r].m - M), acc);
+      }
+      prm.out[static_cast<size_t>(pair) * D + tid] = acc * inv;
     }
-    prm.out[static_cast<size_t>(pair) * D + tid] = acc * inv;
-  }
+  };
+  if constexpr (!ROPE) write_output();
 
   // probabilities -> accumulated scores, stored at once (the evicted slot's
   // score is overwritten with the newcomer's below, after the block barrier
   // that orders the two stores); local minimum candidate key
+  // For a pair on one CTA, or more than two slots per thread, four slots per
+  // thread and pass (the per-slot arrays start 16-byte aligned and hold a
+  // multiple of four entries; the scores go out as one 16-byte store where
+  // the slots' global address allows it); else one slot per thread, which
+  // measured faster for the short slot ranges of 8-CTA clusters.
   const int limit = p - R;  // candidates: kept positions <= p - R outside the static pattern
   unsigned long long kmin = ~0ull;
   int smin = -1;
-  for (int j = tid; j < nrows; j += NT) {
-    const float ns = sc[j] + exp2f(lg[j] - M) * inv;
-    prm.score[slot0 + j] = ns;
-    if (full && ps[j] <= limit && !is_protected(prm.sp, ps[j])) {
-      const unsigned long long key =
-          (static_cast<unsigned long long>(__float_as_uint(ns)) << 32) | static_cast<uint32_t>(ps[j]);
-      if (key < kmin) {
-        kmin = key;
-        smin = lo + j;
+  if (S == 1 || nrows > 2 * NT) {
+    const bool vec_store = (reinterpret_cast<uintptr_t>(prm.score + slot0) & 15u) == 0;
+    for (int j0 = tid * 4; j0 < nrows; j0 += NT * 4) {
+      const float4 s4 = *reinterpret_cast<const float4*>(sc + j0);
+      const float4 l4 = *reinterpret_cast<const float4*>(lg + j0);
+      const int4 p4 = *reinterpret_cast<const int4*>(ps + j0);
+      const float sv[4] = {s4.x, s4.y, s4.z, s4.w}, lv[4] = {l4.x, l4.y, l4.z, l4.w};
+      const int pv[4] = {p4.x, p4.y, p4.z, p4.w};
+      float ns[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) ns[k] = sv[k] + exp2f(lv[k] - M) * inv;
+      if (vec_store && j0 + 4 <= nrows) {
+        *reinterpret_cast<float4*>(prm.score + slot0 + j0) = make_float4(ns[0], ns[1], ns[2], ns[3]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (j0 + k < nrows) prm.score[slot0 + j0 + k] = ns[k];
+      }
+      if (full) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (j0 + k < nrows && pv[k] <= limit && !is_protected(prm.sp, pv[k])) {
+            const unsigned long long key =
+                (static_cast<unsigned long long>(__float_as_uint(ns[k])) << 32) | static_cast<uint32_t>(pv[k]);
+            if (key < kmin) {
+              kmin = key;
+              smin = lo + j0 + k;
+            }
+          }
+      }
+    }
+  } else {
+    for (int j = tid; j < nrows; j += NT) {
+      const float ns = sc[j] + exp2f(lg[j] - M) * inv;
+      prm.score[slot0 + j] = ns;
+      if (full && ps[j] <= limit && !is_protected(prm.sp, ps[j])) {
+        const unsigned long long key =
+            (static_cast<unsigned long long>(__float_as_uint(ns)) << 32) | static_cast<uint32_t>(ps[j]);
+        if (key < kmin) {
+          kmin = key;
+          smin = lo + j;
+        }
       }
     }
   }
+  H2O_TL(8);
   // warp minimum, and the slot of the lane that holds it (keys are unique:
   // positions are)
   const unsigned long long wk = warp_min_key(kmin);
@@ -851,6 +893,7 @@ __global__ void __launch_bounds__((NCW + producer_warps(ROPE)) * 32, NCW > 6 ? 2
       bk = blk_key[w];
       bslot = blk_slot[w];
     }
+  H2O_TL(9);
   // position rolling: the candidate's rank inside the cache travels with it
   int brank = -1;
   if constexpr (ROPE) brank = bslot >= 0 ? rk[bslot - lo] : -1;
@@ -864,6 +907,8 @@ __global__ void __launch_bounds__((NCW + producer_warps(ROPE)) * 32, NCW > 6 ? 2
                                  static_cast<uint32_t>(bslot), static_cast<uint32_t>(brank));
       st_async_v4(mapa_shared(smem_u32(&kin[rank]), tid), v, mapa_shared(smem_u32(kbar), tid));
     }
+    H2O_TL(10);
+    if constexpr (ROPE) write_output();
     if (!mbar_wait_cluster_bounded(kbar, 0, kWaitLimit) && tid == 0) atomicOr(prm.err, ERR_XCH_TIMEOUT);
     if (full) {
       unsigned long long best = ~0ull;
@@ -882,6 +927,7 @@ __global__ void __launch_bounds__((NCW + producer_warps(ROPE)) * 32, NCW > 6 ? 2
     }
   } else {
     u = full ? bslot : count;
+    if constexpr (ROPE) write_output();
   }
   if (full && u < 0 && tid == 0) atomicOr(prm.err, ERR_NO_CANDIDATE);
   H2O_TL(6);
@@ -893,13 +939,25 @@ __global__ void __launch_bounds__((NCW + producer_warps(ROPE)) * 32, NCW > 6 ? 2
   // victim move down one place and the newcomer takes the last rank, C - 1;
   // while filling, every rank stays and the newcomer takes rank `count`
   if constexpr (ROPE) {
-    if (full && u >= 0)
-      for (int j = tid; j < nrows; j += NT) {
-        int r = rk[j];
-        if (r > urank) --r;
-        if (lo + j == u) r = C - 1;
-        prm.rank[slot0 + j] = r;
+    if (full && u >= 0) {
+      const bool vec = (reinterpret_cast<uintptr_t>(prm.rank + slot0) & 15u) == 0;
+      for (int j0 = tid * 4; j0 < nrows; j0 += NT * 4) {
+        const int4 r4 = *reinterpret_cast<const int4*>(rk + j0);
+        int rv[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (rv[k] > urank) --rv[k];
+          if (lo + j0 + k == u) rv[k] = C - 1;
+        }
+        if (vec && j0 + 4 <= nrows) {
+          *reinterpret_cast<int4*>(prm.rank + slot0 + j0) = make_int4(rv[0], rv[1], rv[2], rv[3]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (j0 + k < nrows) prm.rank[slot0 + j0 + k] = rv[k];
+        }
       }
+    }
   }
   // the new token into slot u
   if (u >= lo && u < lo + prm.chunk && u >= 0) {

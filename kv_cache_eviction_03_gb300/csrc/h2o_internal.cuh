@@ -116,7 +116,7 @@ struct DecodeParams {
 // in turn, so the last kTimelineSlots launches can be read back.
 constexpr int kTimelineSlots = 4;
 constexpr int kTimelineMaxCtas = 4096;
-constexpr int kTimelineStamps = 8;
+constexpr int kTimelineStamps = 11;
 cudaError_t decode_timeline_read(void* dst, size_t bytes);
 #endif
 

@@ -48,6 +48,12 @@ __device__ __forceinline__ void st_async_v4(uint32_t raddr, uint4 v, uint32_t rb
                "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(rbar)
                : "memory");
 }
+// The same for one 4-byte word.
+__device__ __forceinline__ void st_async_b32(uint32_t raddr, uint32_t v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(raddr), "r"(v),
+               "r"(rbar)
+               : "memory");
+}
 // Poll of a phase completed by stores of other CTAs of the cluster.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;

@@ -5,9 +5,10 @@
 Builds a copy of the library compiled with H2O_DECODE_TIMELINE next to the
 product library (libh2o_gb300_timeline.so; the product build is not
 touched), in which thread 0 of every decode CTA records %globaltimer at
-eight points: entry, grid dependency released, step inputs loaded, first
+eleven points: entry, grid dependency released, step inputs loaded, first
 stage landed, every consumer past its loop, the pair's softmax normaliser
-known, the victim known, exit.  It then runs the workload's decode rotation
+known, the CTA's scores stored, its block minimum found, its candidate
+pushed to the cluster peers, the victim known, exit.  It then runs the workload's decode rotation
 (one cache per attention layer, every decode step visiting the layers in
 turn, from a CUDA graph, as the benchmark does) and prints, for the last
 launches, each phase's time in microseconds relative to the end of the
@@ -27,9 +28,11 @@ import numpy as np
 from . import _build
 from . import workload as W
 
-STAMPS = ["entry", "dependency released", "inputs loaded", "first stage landed", "loop done",
-          "normaliser known", "victim known", "exit"]
-SLOTS, MAX_CTAS, NSTAMP = 4, 4096, 8
+# (name, stamp index) in the order a CTA passes them
+STAMPS = [("entry", 0), ("dependency released", 1), ("inputs loaded", 2), ("first stage landed", 3),
+          ("loop done", 4), ("normaliser known", 5), ("scores stored", 8), ("block minimum", 9),
+          ("candidate pushed", 10), ("victim known", 6), ("exit", 7)]
+SLOTS, MAX_CTAS, NSTAMP, EXIT = 4, 4096, 11, 7
 
 
 def load_timeline_build():
@@ -124,10 +127,10 @@ def phase_table(stamps):
     previous launch's last exit (us), median and latest over CTAs."""
     rows = []
     for prev, cur in zip(stamps[:-1], stamps[1:]):
-        prev_end = int(prev[:, 7].max())
+        prev_end = int(prev[:, EXIT].max())
         rel = (cur - prev_end) / 1e3
-        rows.append({name: (float(statistics.median(rel[:, i])), float(rel[:, i].max()))
-                     for i, name in enumerate(STAMPS)})
+        rows.append({name: (float(statistics.median(rel[:, i])), float(rel[:, i].max())) if cur[:, i].any() else None
+                     for name, i in STAMPS})  # None: a stamp this kernel shape never passes
     return rows
 
 
@@ -149,8 +152,9 @@ def main():
     rows = phase_table(stamps)
     print("| stamp | " + " | ".join(f"launch {i + 1}" for i in range(len(rows))) + " |")
     print("|---|" + "---|" * len(rows))
-    for name in STAMPS:
-        print(f"| {name} | " + " | ".join(f"{r[name][0]:.2f} / {r[name][1]:.2f}" for r in rows) + " |")
+    for name, _ in STAMPS:
+        print(f"| {name} | " + " | ".join(f"{r[name][0]:.2f} / {r[name][1]:.2f}" if r[name] else "-" for r in rows)
+              + " |")
     spans = [r["exit"][1] for r in rows]
     print(f"launch-to-launch (last exit to last exit): {', '.join(f'{x:.2f}' for x in spans)} us")
 
